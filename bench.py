@@ -1,0 +1,433 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA forward library on B300.
+
+Headline: chunkwise prefill at the K3 layer shape (B=4, H=96, T=8192, d_k=d_v=128, C=64, bf16
+inputs, fp32 state) -- tokens/s of one `kda_chunk_fwd` pass over the batch, inputs resident in
+HBM. Secondary lines in the same JSON object: the one-token decode step (256 sequences x 96
+heads, state resident and updated in place, 64 consecutive steps) as % of HBM bandwidth, and the
+packed long-context prefill (8 sequences, T_total = 131072, C = 128).
+
+`python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]`. Under torchrun each
+rank runs its own batch (weak scaling, no data-path collective); rank 0 prints one JSON line.
+`--impl reference` times the fp64 CPU oracle instead (the only other arm available).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import kda_synth  # noqa: E402
+
+# Algorithmic bytes per token-head (bf16 q, k, g, v, beta in; o out) and useful FLOPs.
+D = 128
+BYTES_PER_TOKEN_HEAD = 3 * D * 2 + D * 2 + 2 + D * 2  # 1282
+STATE_BYTES = D * D * 4
+
+
+def useful_flops_per_token_head(C, dk=D, dv=D):
+    return C * (3 * dk + 2 * dv) + 6 * dk * dv
+
+
+def decode_bytes_per_head(dk=D, dv=D):
+    return 2 * dk * dv * 4 + (3 * dk + dv) * 2 + 2 + dv * 2  # 132354
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
+
+
+def _kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_delta_rule_167_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def _recorded_traffic(kernel_key):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on this source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+        ent = rec.get(kernel_key)
+        if ent and ent.get("source_hash") == _kernel_source_hash():
+            return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while the timed region runs."""
+
+    REASONS = {
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+        0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+        0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
+    }
+
+    def __init__(self, index, period=0.02):
+        self.index, self.period = index, period
+        self.samples, self.reasons = [], set()
+        self._stop = threading.Event()
+        self._thread = None
+        self.max_mhz = None
+        try:
+            import pynvml
+
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+        except Exception:
+            self.nv = None
+
+    def _run(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                mask = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for bit, name in self.REASONS.items():
+                    if mask & bit and bit != 0x1:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.nv is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._thread:
+            self._thread.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+def _dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() and args.impl != "reference" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def _max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _timed(fn, steps, warmup, world, device, stream):
+    """W untimed warm-up calls, then K timed calls bracketed by barrier + synchronize; the
+    duration comes from CUDA events on the launching stream. Returns (total_ms, clocks)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize(device)
+    _barrier(world)
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device.index) as cs:
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+    _barrier(world)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1)
+    return _max_over_ranks(ms, world, device), cs.summary()
+
+
+# ------------------------------------------------------------------------ CPU oracle arm
+
+
+def _cpu_sample(T, n_heads, seed=0):
+    inp = kda_synth.make_prefill_inputs(1, T, n_heads, D, D, "bf16", seed=seed, g_bias=True)
+    return [kda_synth.to_f64_numpy(inp[n]) for n in ("q", "k", "v", "g", "beta")]
+
+
+def cpu_baseline(T=8192, H=96, budget_s=15.0):
+    """The oracle as it stands, on the host's cores, over a bounded sample of the headline
+    workload: a number of complete (batch, head) sequences of T tokens."""
+    import oracle
+
+    cores = oracle.default_threads()
+    n = max(1, min(cores, 8))
+    x = _cpu_sample(T, n)
+    t0 = time.perf_counter()
+    oracle.recurrent(*x, nthreads=cores)
+    dt = time.perf_counter() - t0
+    reps = max(1, min(64, int(budget_s / max(dt, 1e-3))))
+    n2 = n * reps
+    if n2 > n:
+        x = _cpu_sample(T, n2)
+        t0 = time.perf_counter()
+        oracle.recurrent(*x, nthreads=cores)
+        dt = time.perf_counter() - t0
+    else:
+        n2 = n
+    tokens = n2 * T / H  # token-heads -> tokens of the H-head layer
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n2} complete (batch, head) sequences of T={T} tokens "
+                      f"(fp64 token-by-token recurrence) in {dt:.2f} s; tokens = "
+                      f"token-heads / H={H}"}
+
+
+def run_reference(args):
+    world, rank, _ = _dist_setup(args)
+    if rank != 0:
+        return 0
+    import oracle
+
+    T, H = 8192, 96
+    cores = oracle.default_threads()
+    n = max(1, min(cores, 16))
+    x = _cpu_sample(T, n)
+    for _ in range(args.warmup):
+        oracle.recurrent(*x, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.recurrent(*x, nthreads=cores)
+    dt = time.perf_counter() - t0
+    tokens = args.steps * n * T / H
+    value = tokens / dt
+    line = {
+        "impl": "reference", "metric": "KDA fwd tokens/s (B=4,H=96,T=8192,d=128,C=64)",
+        "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "kda_bf16_B4_H96_T8192_d128_C64", "B": 4, "H": 96, "T": 8192,
+                   "d_k": 128, "d_v": 128, "C": 64, "parallelism": "none"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {n} complete (batch, head) sequences of "
+                                   f"T={T} tokens; tokens = token-heads / H={H}"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------------ GPU arm
+
+
+def bench_prefill(kda, args, world, rank, device, stream, peaks):
+    w = kda_synth.WORKLOADS[2]
+    B, T, H, C = w["B"], w["T"], w["H"], w["C"]
+    inp = kda_synth.make_prefill_inputs(B, T, H, D, D, "bf16", seed=w["seed"] + rank,
+                                        g_bias=True, device=device)
+    q, k, v, g, b = (inp[n] for n in ("q", "k", "v", "g", "beta"))
+    out = torch.empty(B, T, H, D, dtype=torch.bfloat16, device=device)
+    Sf = torch.empty(B, H, D, D, dtype=torch.float32, device=device)
+
+    def step():
+        kda.kda_chunk_fwd(q, k, v, g, b, None, out, Sf, C=C, stream=stream)
+
+    step()
+    kda.kda_sync_status(stream)
+    total_ms, clocks = _timed(step, args.steps, args.warmup, world, device, stream)
+    kda.kda_sync_status(stream)
+    ms = total_ms / args.steps
+    token_heads = B * T * H
+    alg_bytes = token_heads * BYTES_PER_TOKEN_HEAD + B * H * STATE_BYTES  # S0 = 0 is not read
+    flops = token_heads * useful_flops_per_token_head(C)
+    achieved_gbs = alg_bytes / (ms * 1e-3) / 1e9
+    traffic = _recorded_traffic("prefill_bf16_B4_H96_T8192_C64")
+    res = dict(ms=ms, clocks=clocks, tokens_per_s=world * B * T / (ms * 1e-3),
+               roofline={"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm"],
+                         "unit": "GB/s", "frac": achieved_gbs / peaks["hbm"],
+                         "traffic": traffic, "peak_source": peaks["source"],
+                         "algorithmic_bytes_per_launch": alg_bytes},
+               tflops=flops / (ms * 1e-3) / 1e12)
+    res["tensor_frac_of_bf16_peak"] = res["tflops"] / peaks["bf16"]
+
+    # end to end through the public API with host buffers (copies inside the timed region)
+    hin = {n: inp[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta")}
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    st_h = torch.empty(Sf.shape, dtype=Sf.dtype, pin_memory=True)
+
+    def e2e_step():
+        kda.chunk_fwd_host(hin["q"], hin["k"], hin["v"], hin["g"], hin["beta"], None, C=C,
+                           device=device, stream=stream, out_host=out_h, state_host=st_h)
+
+    e2e_steps = max(1, min(args.steps, 3))
+    e2e_ms, _ = _timed(e2e_step, e2e_steps, 1, world, device, stream)
+    res["e2e"] = {"value": world * B * T / (e2e_ms / e2e_steps * 1e-3), "unit": "tokens/s",
+                  "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin.values()),
+                  "d2h_bytes_per_step": out_h.numel() * 2 + st_h.numel() * 4,
+                  "steps": e2e_steps}
+    del inp, q, k, v, g, b, out, hin
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_decode(kda, args, world, rank, device, stream, peaks, steps=64):
+    w = kda_synth.WORKLOADS[4]
+    N, H = w["N"], w["H"]
+    dec = kda_synth.make_decode_inputs(N, H, D, D, "bf16", seed=w["seed"] + rank,
+                                       S0_std=w["S0_std"], steps=steps, device=device)
+    S = dec["S"]
+    outs = [torch.empty(N, H, D, dtype=torch.bfloat16, device=device) for _ in range(steps)]
+    seq = [[st[n] for n in ("q", "k", "v", "g", "beta")] for st in dec["steps"]]
+
+    def run64():
+        for i in range(steps):
+            kda.kda_recurrent_step(*seq[i], S, outs[i], stream=stream)
+
+    total_ms, clocks = _timed(run64, 1, 1, world, device, stream)
+    kda.kda_sync_status(stream)
+    ms_step = total_ms / steps
+    bytes_step = N * H * decode_bytes_per_head()
+    gbs = bytes_step / (ms_step * 1e-3) / 1e9
+    del dec, S, outs, seq
+    torch.cuda.empty_cache()
+    return {"workload": w["name"], "ms_per_step": ms_step, "steps_timed": steps,
+            "tokens_per_s": world * N / (ms_step * 1e-3), "clocks": clocks,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm"],
+                         "traffic": _recorded_traffic("decode_bf16_N256_H96"),
+                         "algorithmic_bytes_per_launch": bytes_step}}
+
+
+def bench_varlen(kda, args, world, rank, device, stream, peaks, steps=3):
+    w = kda_synth.WORKLOADS[3]
+    T, H, C = w["T"], w["H"], w["C"]
+    inp = kda_synth.make_varlen_inputs(T, H, D, D, w["n_seq"], "bf16", seed=w["seed"] + rank,
+                                       device=device)
+    cu = inp["cu_seqlens"].to(device)
+    q, k, v, g, b = (inp[n] for n in ("q", "k", "v", "g", "beta"))
+    N = cu.numel() - 1
+    out = torch.empty(1, T, H, D, dtype=torch.bfloat16, device=device)
+    Sf = torch.empty(N, H, D, D, dtype=torch.float32, device=device)
+
+    def step():
+        kda.kda_chunk_fwd_varlen(q, k, v, g, b, None, out, Sf, cu, C=C, stream=stream)
+
+    total_ms, clocks = _timed(step, steps, 1, world, device, stream)
+    kda.kda_sync_status(stream)
+    ms = total_ms / steps
+    alg = T * H * BYTES_PER_TOKEN_HEAD + N * H * STATE_BYTES
+    gbs = alg / (ms * 1e-3) / 1e9
+    lens = (inp["cu_seqlens"][1:] - inp["cu_seqlens"][:-1]).tolist()
+    del inp, q, k, v, g, b, out
+    torch.cuda.empty_cache()
+    return {"workload": w["name"], "ms_per_step": ms, "seq_lens": lens,
+            "tokens_per_s": world * T / (ms * 1e-3),
+            "tflops": T * H * useful_flops_per_token_head(C) / (ms * 1e-3) / 1e12,
+            "clocks": clocks,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm"], "traffic": None,
+                         "algorithmic_bytes_per_launch": alg}}
+
+
+def run_gpu(args):
+    import gated_delta_rule_167_b300 as kda
+
+    world, rank, local = _dist_setup(args)
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    kda.load_library()
+    stream = torch.cuda.current_stream(device)
+    peaks = _peaks()
+
+    pre = bench_prefill(kda, args, world, rank, device, stream, peaks)
+    secondary = {}
+    if not args.headline_only:
+        secondary["decode"] = bench_decode(kda, args, world, rank, device, stream, peaks)
+        secondary["varlen"] = bench_varlen(kda, args, world, rank, device, stream, peaks)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+
+    if rank == 0:
+        line = {
+            "metric": "KDA fwd tokens/s (B=4,H=96,T=8192,d=128,C=64)",
+            "value": pre["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": pre["ms"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "kda_bf16_B4_H96_T8192_d128_C64", "B": 4, "H": 96,
+                       "T": 8192, "d_k": 128, "d_v": 128, "C": 64, "state": "fp32",
+                       "global_batch": 4 * world, "seq_len": 8192,
+                       "parallelism": f"dp{world}" if world > 1 else "none",
+                       "l2": "inputs larger than L2 (3.2 GB per step)"},
+            "tflops": pre["tflops"], "tensor_frac_of_bf16_peak": pre["tensor_frac_of_bf16_peak"],
+            "roofline": pre["roofline"], "clocks": pre["clocks"], "e2e": pre["e2e"],
+            "gpu_launches": args.steps, "cpu_baseline": cpu,
+        }
+        line.update(secondary)
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,37 @@
+// Shared device helpers for the KDA kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+// Device-side status word of the library (one per device, in the library's own image; the
+// library is a single translation unit). Kernels record the first error they meet;
+// kda_sync_status() reads and clears it.
+__device__ unsigned int g_status = 0u;
+
+__device__ __forceinline__ void record_status(unsigned int code) {
+  atomicCAS(&g_status, 0u, code);
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+}  // namespace kda

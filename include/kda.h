@@ -1,0 +1,111 @@
+/*
+ * kda.h -- C ABI of the KDA (Kimi Delta Attention) forward library for NVIDIA B300 (sm_103a).
+ *
+ * What is computed (Kimi K3 wiki, "Notations mathématiques", table "Attention et KDA"):
+ *   alpha_t = exp(g_t)                      per key channel, g_t in (g_min = -5, 0)^{d_k}
+ *   S_t     = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *   o_t     = S_t^T q_t                     raw output, read from the updated state
+ * Prefill uses the exact chunkwise (block) form: serial across blocks of C tokens, parallel
+ * inside a block (Glossaire, entries "Chunkwise" and "UT"); decode applies one token of the
+ * recurrence to a resident state (Glossaire, entry "Decode").
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor pointer is a DEVICE pointer on the current CUDA device, 16-byte aligned,
+ *    contiguous row-major, in the layout given below. The caller owns every buffer; the
+ *    library allocates no device memory.
+ *  - Sequence tensors use [B, T, H, d]: q, k, g are [B, T, H, d_k]; v and out are
+ *    [B, T, H, d_v]; beta is [B, T, H]. Their element type is `dtype` (all the same).
+ *  - States S0, S_final, S are fp32 [B (or N), H, d_k, d_v] with d_v fastest.
+ *  - q and k are expected to be L2-normalised per token (a precondition of the method, not
+ *    re-checked). No 1/sqrt(d_k) scale is applied. Values of g and beta are not range-checked.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Calls are
+ *    asynchronous: a KDA_OK return means the arguments were valid and the work was enqueued.
+ *  - Errors: invalid pointers/sizes return KDA_ERR_INVALID_ARG and shapes outside the
+ *    supported set return KDA_ERR_UNSUPPORTED, both before anything is launched; a failed
+ *    launch returns KDA_ERR_CUDA. Conditions detected on the device (a bounded wait that ran
+ *    out, inconsistent cu_seqlens) are latched in a per-device status word that
+ *    kda_sync_status() returns and clears. kda_last_error() gives a message for the most
+ *    recent failure on the calling thread.
+ *  - Supported: d_k = d_v in {64, 128}; C in {16, 32, 64, 128}; T >= 0; B, H >= 1 (B = 0 or
+ *    T = 0 is a no-op apart from copying S0 to S_final).
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, negative or inconsistent size        */
+  KDA_ERR_UNSUPPORTED = 2, /* valid request outside the supported shapes/dtypes              */
+  KDA_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed                            */
+  KDA_ERR_TIMEOUT = 4      /* a bounded on-device wait gave up (reported by kda_sync_status) */
+} kda_status_t;
+
+typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype_t;
+
+/*
+ * Chunkwise prefill over a dense batch of B sequences of T tokens each.
+ *   q, k, g : [B, T, H, d_k]  dtype      v : [B, T, H, d_v]  dtype     beta : [B, T, H] dtype
+ *   S0      : [B, H, d_k, d_v] fp32, read only; NULL means a zero initial state
+ *   out     : [B, T, H, d_v]  dtype, written (o_t for every token)
+ *   S_final : [B, H, d_k, d_v] fp32, written with the state after token T; NULL = not written
+ *   C       : block size (16, 32, 64 or 128); the result does not depend on it beyond rounding
+ * fp32 inputs run on CUDA cores in fp32 throughout. bf16 inputs run on the tensor cores
+ * (bf16 operands, fp32 accumulation, fp32 state) when d_k = d_v = 128 and C is 64 or 128.
+ */
+kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g,
+                           const void* beta, const float* S0, void* out, float* S_final,
+                           int B, int H, int T, int d_k, int d_v, int C, kda_dtype_t dtype,
+                           void* stream);
+
+/*
+ * Chunkwise prefill over a packed batch of N variable-length sequences sharing one token
+ * axis of length T_total (the leading batch dimension is 1).
+ *   q, k, g : [1, T_total, H, d_k]   v, out : [1, T_total, H, d_v]   beta : [1, T_total, H]
+ *   cu_seqlens : DEVICE int32 [N + 1]; sequence s owns tokens [cu_seqlens[s], cu_seqlens[s+1]);
+ *                must satisfy cu_seqlens[0] = 0, non-decreasing, cu_seqlens[N] = T_total.
+ *                Violations are caught on the device: the affected sequences are skipped and
+ *                kda_sync_status() reports KDA_ERR_INVALID_ARG.
+ *   S0, S_final : [N, H, d_k, d_v] fp32 (per sequence; NULL as above). The state is reset at
+ *                 every sequence boundary. Blocks start at each sequence's first token; the
+ *                 last block of a sequence may be partial.
+ */
+kda_status_t kda_chunk_fwd_varlen(const void* q, const void* k, const void* v, const void* g,
+                                  const void* beta, const float* S0, void* out,
+                                  float* S_final, const int32_t* cu_seqlens, int N, int H,
+                                  int T_total, int d_k, int d_v, int C, kda_dtype_t dtype,
+                                  void* stream);
+
+/*
+ * One decode token for N sequences x H heads, updating the resident states in place.
+ *   q, k, g : [N, H, d_k] dtype   v, out : [N, H, d_v] dtype   beta : [N, H] dtype
+ *   S       : [N, H, d_k, d_v] fp32, read and overwritten with the updated state
+ * out receives o = S_new^T q. S must not alias any other argument.
+ */
+kda_status_t kda_recurrent_step(const void* q, const void* k, const void* v, const void* g,
+                                const void* beta, float* S, void* out, int N, int H, int d_k,
+                                int d_v, kda_dtype_t dtype, void* stream);
+
+/* Synchronises `stream`, then returns and clears the device-side status word of the current
+ * device (KDA_OK if nothing was latched), or KDA_ERR_CUDA if the synchronisation failed. */
+kda_status_t kda_sync_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* kda_status_string(kda_status_t status);
+
+/* Message describing the most recent failure on the calling thread ("" if none). */
+const char* kda_last_error(void);
+
+/* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
+int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */
