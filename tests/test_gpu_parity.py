@@ -184,12 +184,15 @@ def test_no_initial_state_and_no_final_state(kda, dtype):
     check(out, o_ref, dtype, "out")
 
 
-def test_beta_one_and_zero_edges(kda):
-    """beta = 1 (full replacement along k) and beta = 0 (pure decay) are exact edges."""
+@pytest.mark.parametrize("C", [16, 64])
+def test_beta_one_and_zero_edges(kda, C):
+    """beta = 1 (full replacement along k) and beta = 0 (pure decay) are exact edges. The decay
+    is scaled down so that the pure-decay state stays well inside the fp32 range."""
     inp = kda_synth.make_prefill_inputs(1, 130, 2, 128, 128, "f32", seed=9, S0_std=0.5)
+    inp["g"] = inp["g"] * 0.05
     for val in (0.0, 1.0):
         inp["beta"] = torch.full_like(inp["beta"], val)
-        out, Sf = run_dense(kda, inp, 64)
+        out, Sf = run_dense(kda, inp, C)
         o_ref, S_ref = oracle_dense(inp)
         check(out, o_ref, "f32", f"out beta={val}")
         check(Sf, S_ref, "f32", f"S_final beta={val}")
