@@ -79,38 +79,47 @@ def _recorded_traffic(kernel_key):
 
 
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML while the timed region runs."""
+    """Samples the SM clock and the clock-event (throttle) reasons while the timed region runs:
+    through NVML when it initialises, else through `nvidia-smi -lms`."""
 
     REASONS = {
-        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
-        0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+        0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+        0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
         0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
     }
 
-    def __init__(self, index, period=0.02):
-        self.index, self.period = index, period
+    def __init__(self, device, period=0.02):
+        self.index = _physical_gpu_id(device)
+        self.period = period
         self.samples, self.reasons = [], set()
         self._stop = threading.Event()
         self._thread = None
+        self._proc = None
         self.max_mhz = None
+        self.source = None
+        self.nv = None
         try:
             import pynvml
 
             pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            if str(self.index).startswith("GPU-"):
+                self.h = pynvml.nvmlDeviceGetHandleByUUID(self.index)
+            else:
+                self.h = pynvml.nvmlDeviceGetHandleByIndex(int(self.index))
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception:
-            self.nv = None
+            self.nv = pynvml
+            self.source = "nvml"
+        except Exception as e:  # fall back to nvidia-smi
+            self.source = f"nvidia-smi (nvml unavailable: {type(e).__name__})"
 
-    def _run(self):
+    def _run_nvml(self):
         nv = self.nv
         while not self._stop.is_set():
             try:
                 self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
                 mask = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
                 for bit, name in self.REASONS.items():
-                    if mask & bit and bit != 0x1:
+                    if mask & bit:
                         self.reasons.add(name)
             except Exception:
                 pass
@@ -118,21 +127,69 @@ class ClockSampler:
 
     def __enter__(self):
         if self.nv is not None:
-            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread = threading.Thread(target=self._run_nvml, daemon=True)
             self._thread.start()
+        else:
+            import subprocess
+
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index), "--query-gpu=clocks.sm,clocks.max.sm,"
+                     "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                     "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                time.sleep(0.3)  # let the first sample land before the timed region
+            except Exception:
+                self._proc = None
         return self
 
     def __exit__(self, *a):
         self._stop.set()
         if self._thread:
             self._thread.join()
+        if self._proc is not None:
+            time.sleep(0.25)
+            self._proc.terminate()
+            try:
+                out, _ = self._proc.communicate(timeout=5)
+            except Exception:
+                out = ""
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 6:
+                    continue
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except ValueError:
+                    continue
+                for name, val in zip(names, f[2:6]):
+                    if val.lower() == "active":
+                        self.reasons.add(name)
 
     def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                    "samples": 0}
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+        med = statistics.median(self.samples) if self.samples else None
+        return {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples), "source": self.source}
+
+
+def _physical_gpu_id(device):
+    """Identifier of the torch device for NVML / nvidia-smi: its UUID when torch exposes it,
+    else the first CUDA_VISIBLE_DEVICES entry, else the index."""
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+        if u and u != "None":
+            return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis:
+        first = vis.split(",")[device.index or 0].strip()
+        if first:
+            return first
+    return str(device.index or 0)
 
 
 def _dist_setup(args):
@@ -176,7 +233,7 @@ def _timed(fn, steps, warmup, world, device, stream):
     torch.cuda.synchronize(device)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(device.index) as cs:
+    with ClockSampler(device) as cs:
         e0.record(stream)
         for _ in range(steps):
             fn()
