@@ -9,33 +9,34 @@
 //   S' = Diag(e^{Gamma_L}) S + Khat^T U,  Khat_j = k_j e^{Gamma_L - Gamma_j}
 //
 // Bounded decay. Over a block of 64 tokens Gamma can fall to -320, so e^{-Gamma} overflows any
-// floating type and A, P cannot be formed as one product (K e^Gamma)(K e^{-Gamma})^T. With
-// g >= g_min = -5 every 16-token sub-block spans at most e^80, inside the bf16/fp32 range, so
-// A and P are built from four tensor-core products, one per 16-row block R with reference
-// B_R = Gamma at the row before the block (0 for the first block):
-//   rows r in block R:  X[r] = [k_r ; q_r] * e^{Gamma_r - B_R}          (factor in [e^-80, 1])
-//   columns j < 16(R+1): Y_R[j] = k_j * e^{B_R - Gamma_j}               (<= 1 before the block,
-//                                                                        <= e^80 inside it)
-//   D_R = X Y_R^T gives A (rows 0..63 of X, the k side) and P (rows 64..127, the q side) for
-// the rows of block R; the other rows of D_R are not used. Every factor is formed from one
-// exponential per element: e^{Gamma_r - B_R} and its inverse, times per-channel boundary
-// factors e^{B_R' - B_R} <= 1.
+// floating type and A, P cannot be one product (K e^Gamma)(K e^{-Gamma})^T. With
+// g >= g_min = -5 each 16-token sub-block spans at most e^80, inside the bf16/fp32 range, so A
+// and P come from one tensor-core product X Y^T in which every row block R = 0..3 has its own
+// reference B_R = Gamma at the last row of block R - 1 (B_0 = 0):
+//   X[r]     = [k_r ; q_r] e^{Gamma_r - B_R}   for r in block R           (factor in [e^-80, 1])
+//   Y_R[j]   = k_j e^{B_R - Gamma_j}           for j < 16(R + 1)          (<= 1 before block R,
+//                                                                          <= e^80 inside it)
+// Y stacks Y_0..Y_3 as N = 16 + 32 + 48 + 64 = 160 columns, so X is read once; the rows of
+// block R take their A and P entries from the Y_R columns. Every factor is formed from one
+// exponential per element, times per-channel factors e^{B_R' - B_R} <= 1.
 //
-// Layout and pipeline. One CTA (256 threads) owns one (sequence, head) problem. Per block:
-//   TMA (4 tensors x two 64-column, 128-byte-swizzled boxes) -> shared memory
-//   SIMT:   Gamma (registers), boundary factors, X and Y_R operands (bf16, swizzled)
-//   tcgen05: D_R = X Y_R^T                                 (M=128, N=16(R+1), K=128) x4
-//   SIMT:   A, P out of TMEM; T = (I + A)^{-1} by 16x16 block forward substitution;
-//           T Diag(beta), K e^Gamma, Q e^Gamma, Khat operands
-//   tcgen05: W^T = (K e^Gamma)^T (T Diag beta)^T,  U~^T = V^T (T Diag beta)^T   (M=128,N=64,K=64)
-//   (next block's TMA is issued here: its inputs are no longer read)
-//   tcgen05: U^T = U~^T - S^T W^T,  O^T = S^T (Q e^Gamma)^T                   (M=128,N=64,K=128)
-//   tcgen05: dS = Khat^T U (M=128,N=128,K=64),  O^T += U^T P^T                (M=128,N=64,K=64)
-//   SIMT:   O -> global (bf16); S <- e^{Gamma_L} S + dS kept in fp32 registers, bf16 copy to
-//           shared memory as the next block's operand.
-// The transposed forms keep every product at M = 128 (TMEM lane = row). The fp32 state lives
-// in registers for the whole sequence (64 values per thread); only its bf16 copy feeds the
-// tensor cores, so rounding does not accumulate in S itself.
+// One CTA (256 threads) owns one (sequence, head) problem and walks its blocks in order. In
+// the elementwise phases thread (c, h) owns channel c (= its TMEM lane) and rows / columns
+// 32h .. 32h + 31, so every operand it produces is a contiguous 64-byte run of one row of a
+// [channel][token] tile and is written with 16-byte stores. Per block:
+//   TMA: k, q (double-buffered), g, v tiles, two 64-channel boxes each, 128-byte swizzle
+//   SIMT: Gamma, X and Y operands                       tcgen05: D = X Y^T  (M 128, N 160, K 128)
+//   SIMT: (K e^Gamma)^T, Khat^T, (Q e^Gamma)^T; A and P out of TMEM; T = (I + A)^{-1} by
+//         16 x 16 blocks in fp32; T Diag(beta) in bf16
+//   tcgen05: W^T = (K e^Gamma)^T (T Diag beta)^T,  U~^T = V^T (T Diag beta)^T
+//   SIMT: -W^T to shared memory                        tcgen05: [U^T | O^T] += S^T [-W^T | (Q e^Gamma)^T]
+//   SIMT: U to shared memory                           tcgen05: dS = Khat^T U,  O^T += U^T P^T
+//   SIMT: O to global memory (bf16); S <- e^{Gamma_L} S + dS in fp32 registers, bf16 copy to
+//         shared memory as the next block's operand.
+// Transposed forms keep every product at M = 128 (TMEM lane = row). The fp32 state lives in
+// registers for the whole sequence; only its bf16 copy feeds the tensor cores, so rounding does
+// not accumulate in S itself. Every wait is bounded; a timeout latches KDA_ERR_TIMEOUT, lets
+// issued copies and products land, frees TMEM and returns.
 #pragma once
 
 #include <cuda.h>
@@ -53,42 +54,45 @@ namespace tc {
 constexpr int C = 64;
 constexpr int D = 128;
 constexpr int THREADS = 256;
+constexpr float LOG2E = 1.4426950408889634f;
 
 // ---- shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t IN_K = 0, IN_Q = 16384, IN_V = 32768, IN_G = 49152;  // TMA tiles, 16 KB each
-constexpr uint32_t RX = 65536;                 // 72 KB region, two uses per block:
-constexpr uint32_t XA = RX;                    //   [k e^(G-B); q e^(G-B)]  128 x 128, K-major
-constexpr uint32_t YB = RX + 32768;            //   Y_0..Y_3 (16,32,48,64 rows), K-major
-constexpr uint32_t KG = RX;                    //   K e^Gamma  (A of W^T, MN-major)
-constexpr uint32_t QG = RX + 16384;            //   Q e^Gamma  (B of O^T, K-major)
-constexpr uint32_t KH = RX + 32768;            //   Khat       (A of dS, MN-major)
-constexpr uint32_t WT = RX + 49152;            //   W^T        (B of U^T, MN-major)
-constexpr uint32_t TB = RX + 65536;            //   T Diag(beta) (B of W^T and U~^T, K-major)
-constexpr uint32_t SS = RX + 73728;            // bf16 S (A of U^T and O^T, MN-major), 32 KB
-constexpr uint32_t US = SS + 32768;            // bf16 U (B of dS / A of O^T, K-major), 16 KB
-constexpr uint32_t PS = US + 16384;            // bf16 P (B of O^T, K-major), 8 KB
-constexpr uint32_t AM = PS + 8192;             // fp32 A, then T in place: [64][65]
-constexpr uint32_t AM_LD = 65;
-constexpr uint32_t SMEM_BYTES = AM + 64 * AM_LD * 4;
+constexpr uint32_t IN_K = 0;          // k tiles, two buffers of 16 KB (block parity)
+constexpr uint32_t IN_Q = 32768;      // q tiles, two buffers of 16 KB
+constexpr uint32_t IN_G = 65536;      // g tile, 16 KB
+constexpr uint32_t IN_V = 81920;      // v tile, 16 KB (MN-major A of U~^T as loaded)
+constexpr uint32_t SS = 98304;        // bf16 S [k][v]: MN-major A of the U/O product, 2 panels
+constexpr uint32_t XY = 131072;       // 80 KB region with two lives per block:
+constexpr uint32_t XK = XY;           //   X rows 0..63 (k side), MN-major A panel 0
+constexpr uint32_t XQ = XY + 16384;   //   X rows 64..127 (q side), MN-major A panel 1
+constexpr uint32_t YP = XY + 32768;   //   Y, N = 160 columns in 3 MN-major B panels
+constexpr uint32_t KG = XY;           // after D: (K e^Gamma)^T [c][r], K-major A of W^T
+constexpr uint32_t KH = XY + 16384;   //   Khat^T [c][r], K-major A of dS
+constexpr uint32_t PT = XY + 32768;   //   P [r][j], K-major B of O^T += U^T P^T (8 KB)
+constexpr uint32_t WS = XY + 40960;   //   fp32 A then T (64 x 64, 16 KB); later -W^T, then U
+constexpr uint32_t NW = WS;           //   -W^T [c][r], MN-major B panel 0 of the U/O product
+constexpr uint32_t US = WS;           //   U [v][r], K-major B of dS and A of O^T += U^T P^T
+constexpr uint32_t QG = XY + 57344;   //   (Q e^Gamma)^T [c][r], MN-major B panel 1 of U/O
+constexpr uint32_t TB = XY + 73728;   //   fp32 M_R during the solve, then T Diag(beta) [r][j]
+constexpr uint32_t SMEM_BYTES = XY + 81920;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for aligning the base
-// Inside the G tile once Gamma is in registers (the tile is dead until the next TMA):
-constexpr uint32_t TAB = IN_G;                 // float [14][128] boundary factors
-constexpr uint32_t XM = IN_G + 14 * 128 * 4;   // float [16][48] block-solve scratch
-constexpr uint32_t TX_BYTES = 4 * 16384;       // bytes landed by one block's TMA
-
-__host__ __device__ constexpr uint32_t y_base(int R) { return YB + 4096u * (uint32_t)(R * (R + 1) / 2); }
-__host__ __device__ constexpr uint32_t y_panel(int R) { return 2048u * (uint32_t)(R + 1); }
+constexpr uint32_t BOX_BYTES = 8192;                // one 64-channel x 64-token TMA box
 
 // ---- TMEM columns (512 allocated)
-constexpr uint32_t TM_DS = 0, TM_U = 128, TM_O = 192, TM_WT = 256, TM_AP = 320;
-__host__ __device__ constexpr uint32_t ap_off(int R) { return 8u * (uint32_t)(R * (R + 1)); }  // 0,16,48,96
+constexpr uint32_t TD = 0;    // X Y^T, 160 columns
+constexpr uint32_t TW = 160;  // W^T, 64
+constexpr uint32_t TU = 224;  // U~^T, then U^T, 64
+constexpr uint32_t TO = 288;  // O^T, 64 (directly after TU: the U/O product writes both)
+constexpr uint32_t TS = 352;  // dS, 128
 
-// table rows inside TAB
-constexpr int TAB_EXPB = 0;   // e^{B_R}, R = 0..3
-constexpr int TAB_EXPL = 4;   // e^{B_4 - B_R}, R = 0..3   (B_4 = Gamma_L)
-constexpr int TAB_E = 8;      // e^{B_R' - B_R}, pairs (R, R') with R < R' <= 3
-__host__ __device__ constexpr int pair_index(int R, int Rp) {
-  return R == 0 ? Rp - 1 : (R == 1 ? Rp + 1 : 5);  // (0,1)0 (0,2)1 (0,3)2 (1,2)3 (1,3)4 (2,3)5
+// First column of Y_R inside the N = 160 stack.
+__host__ __device__ constexpr int y_ofs(int R) { return 8 * R * (R + 1); }  // 0, 16, 48, 96
+
+// fp32 64 x 64 workspace index with the 16-byte chunks of each row rotated by the row, so that
+// a warp storing the same chunk of 32 consecutive rows hits every bank group.
+__device__ __forceinline__ int wsi(int r, int j) {
+  const int ch = j >> 2;
+  return r * 64 + (((ch ^ r) & 7) | (ch & 8)) * 4 + (j & 3);
 }
 
 struct TmaMaps {
@@ -97,27 +101,8 @@ struct TmaMaps {
 
 using namespace sm100;
 
-__device__ __forceinline__ void st_bf16(uint8_t* base, uint32_t off, float x) {
-  *reinterpret_cast<__nv_bfloat16*>(base + off) = __float2bfloat16_rn(x);
-}
-
 __device__ __forceinline__ float ld_bf16(const uint8_t* base, uint32_t off) {
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + off));
-}
-
-// Packs 8 floats into 8 bf16 (round to nearest even) and stores them as one 16-byte chunk.
-__device__ __forceinline__ void st_chunk8(uint8_t* p, const float* x) {
-  __nv_bfloat162 h[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
-  *reinterpret_cast<uint4*>(p) = *reinterpret_cast<const uint4*>(h);
-}
-
-// Writes 32 consecutive values (columns col0..col0+31 of a 64-column swizzled panel row).
-__device__ __forceinline__ void st_row32(uint8_t* panel, uint32_t row, uint32_t col0,
-                                         const float* x) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) st_chunk8(panel + sw128_off(row, col0 + 8 * c), x + 8 * c);
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -125,29 +110,33 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t bar_tma, bar_mma;
+  const uint32_t sb = smem_u32(sm);
+  __shared__ uint64_t bar_kq[2], bar_g, bar_v, bar_mma;
   __shared__ uint32_t tmem_base_s;
   __shared__ float beta_s[C];
   __shared__ float xch[D];
-  __shared__ float bnd[5][D];  // B_0..B_4 per channel (B_4 = Gamma_L)
+  __shared__ float bnd[5][D];  // log2-domain Gamma at the block boundaries: B_0..B_3, B_4 = Gamma_L
 
   const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3;   // TMEM lane quarter this warp may address
-  const int colhalf = warp >> 2;  // which half of the columns this warp handles
-  const int c = tid & (D - 1);    // channel owned in the elementwise phases (= TMEM lane)
-  const int rhalf = tid >> 7;     // rows 32*rhalf .. +31 in the elementwise phases
+  const int warp = tid >> 5;
+  const int quarter = warp & 3;  // TMEM lane quarter this warp may address
+  const int c = tid & (D - 1);   // channel (= TMEM lane) owned in the elementwise phases
+  const int hh = tid >> 7;       // which half of the rows / columns this thread handles
 
   int h, len;
   size_t row0;
   const int p = blockIdx.x;
   if (!resolve_problem(P, p, h, row0, len)) return;
   const int H = P.H;
+  const int nblocks = (len + C - 1) / C;
   const __nv_bfloat16* __restrict__ beta_g = static_cast<const __nv_bfloat16*>(P.beta);
   __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(P.out);
 
   if (tid == 0) {
-    mbar_init(&bar_tma, 1);
+    mbar_init(&bar_kq[0], 1);
+    mbar_init(&bar_kq[1], 1);
+    mbar_init(&bar_g, 1);
+    mbar_init(&bar_v, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
     prefetch_tensormap(&maps.q);
@@ -160,71 +149,112 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  const uint32_t tlane = (uint32_t)(32 * quarter) << 16;
+  const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);  // this warp's lane quarter
 
-  auto issue_tma = [&](int t0) {
-    mbar_arrive_expect_tx(&bar_tma, TX_BYTES);
-    const int row = (int)(row0 + t0);
-#pragma unroll
-    for (int pnl = 0; pnl < 2; ++pnl) {
-      tma_load_3d(sm + IN_K + pnl * 8192, &maps.k, 64 * pnl, h, row, &bar_tma);
-      tma_load_3d(sm + IN_Q + pnl * 8192, &maps.q, 64 * pnl, h, row, &bar_tma);
-      tma_load_3d(sm + IN_V + pnl * 8192, &maps.v, 64 * pnl, h, row, &bar_tma);
-      tma_load_3d(sm + IN_G + pnl * 8192, &maps.g, 64 * pnl, h, row, &bar_tma);
-    }
+  // ---- TMA issue (thread 0 only)
+  auto load2 = [&](uint32_t dst, const CUtensorMap* m, int row, uint64_t* bar) {
+    tma_load_3d(sm + dst, m, 0, h, row, bar);
+    tma_load_3d(sm + dst + BOX_BYTES, m, 64, h, row, bar);
+  };
+  auto issue_kq = [&](int b) {
+    const int buf = b & 1;
+    mbar_arrive_expect_tx(&bar_kq[buf], 4 * BOX_BYTES);
+    load2(IN_K + 16384u * buf, &maps.k, (int)(row0 + (size_t)b * C), &bar_kq[buf]);
+    load2(IN_Q + 16384u * buf, &maps.q, (int)(row0 + (size_t)b * C), &bar_kq[buf]);
+  };
+  auto issue_g = [&](int b) {
+    mbar_arrive_expect_tx(&bar_g, 2 * BOX_BYTES);
+    load2(IN_G, &maps.g, (int)(row0 + (size_t)b * C), &bar_g);
+  };
+  auto issue_v = [&](int b) {
+    mbar_arrive_expect_tx(&bar_v, 2 * BOX_BYTES);
+    load2(IN_V, &maps.v, (int)(row0 + (size_t)b * C), &bar_v);
   };
 
-  // ---- initial state: fp32 in registers (lane c, columns 64*colhalf + j), bf16 copy in SS
+  // ---- initial state: fp32 in registers (row c, columns 64 hh ..), bf16 copy in SS
   float S[64];
   {
-    const float* s0 = P.S0 ? P.S0 + ((size_t)p * D + c) * D + 64 * colhalf : nullptr;
+    const float* s0 = P.S0 ? P.S0 + ((size_t)p * D + c) * D + 64 * hh : nullptr;
 #pragma unroll
     for (int j = 0; j < 64; j += 4) {
       float4 x = s0 ? *reinterpret_cast<const float4*>(s0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
       S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
     }
-    uint8_t* panel = sm + SS + 16384u * colhalf;
-    st_row32(panel, c, 0, S);
-    st_row32(panel, c, 32, S + 32);
+#pragma unroll
+    for (int k8 = 0; k8 < 8; ++k8)
+      st_shared_v4(sb + SS + 16384u * hh + sw128_off(c, 8 * k8), pack_bf16(S[8 * k8], S[8 * k8 + 1]),
+                   pack_bf16(S[8 * k8 + 2], S[8 * k8 + 3]), pack_bf16(S[8 * k8 + 4], S[8 * k8 + 5]),
+                   pack_bf16(S[8 * k8 + 6], S[8 * k8 + 7]));
+    uint32_t z[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) z[j] = 0u;
+    tmem_st32(tl + TO + 32 * hh, z);  // O^T starts each block at zero
+    tmem_st_wait();
   }
-  if (tid == 0 && len > 0) issue_tma(0);
+  // Phase parities and pending flags; bit b of the k/q words belongs to buffer b.
+  uint32_t ph_kq = 0u, ph_g = 0u, ph_v = 0u, ph_mma = 0u;
+  uint32_t pend_kq = 0u;
+  bool pend_g = false, pend_v = false, pend_mma = false;
+  if (tid == 0 && nblocks > 0) {
+    issue_kq(0);
+    issue_g(0);
+    issue_v(0);
+  }
+  if (nblocks > 0) {
+    pend_kq = 1u;
+    pend_g = pend_v = true;
+  }
+  tc_fence_before();
+  fence_proxy_async_smem();
+  __syncthreads();
 
-  uint32_t tma_phase = 0, mma_phase = 0;
-  bool tma_pending = len > 0;
   bool aborted = false;
-
   auto mma_done = [&]() -> bool {
-    const bool ok = mbar_wait(&bar_mma, mma_phase);
-    mma_phase ^= 1u;
+    const bool ok = mbar_wait(&bar_mma, ph_mma);
+    if (ok) ph_mma ^= 1u;  // a timed-out phase stays the one to drain
+    pend_mma = !ok;
     tc_fence_after();
     return ok;
   };
 
-  for (int t0 = 0; t0 < len && !aborted; t0 += C) {
+  for (int blk = 0; blk < nblocks; ++blk) {
+    const int t0 = blk * C;
     const int n = min(C, len - t0);
-    // ---------------- stage: beta, wait for the tiles
+    const int buf = blk & 1;
+    if (blk + 1 < nblocks) {  // the other k/q buffer was last read by block blk - 1
+      if (tid == 0) {
+        fence_proxy_async_smem();
+        issue_kq(blk + 1);
+      }
+      pend_kq |= 1u << (buf ^ 1);
+    }
     if (tid < C) beta_s[tid] = tid < n ? __bfloat162float(beta_g[(row0 + t0 + tid) * H + h]) : 0.f;
     {
-      const bool ok = mbar_wait(&bar_tma, tma_phase);
-      tma_phase ^= 1u;
-      if (__syncthreads_or(!ok)) { aborted = true; break; }
-      tma_pending = false;
+      const bool ok = mbar_wait(&bar_g, ph_g);
+      if (ok) ph_g ^= 1u;
+      pend_g = !ok;
+      const bool ok2 = mbar_wait(&bar_kq[buf], (ph_kq >> buf) & 1u);
+      if (ok2) {
+        ph_kq ^= 1u << buf;
+        pend_kq &= ~(1u << buf);
+      }
+      if (__syncthreads_or(!(ok && ok2))) { aborted = true; break; }
     }
-    // ---------------- Gamma (registers): thread owns channel c, rows 32*rhalf .. +31
+    // ---------------- Gamma (log2 domain), thread (c, hh) rows 32 hh .. 32 hh + 31
     float Gm[32];
     {
-      const uint8_t* gp = sm + IN_G + (c >> 6) * 8192;
+      const uint8_t* gp = sm + IN_G + (c >> 6) * BOX_BYTES;
       float acc = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const int r = 32 * rhalf + i;
-        acc += r < n ? ld_bf16(gp, sw128_off(r, c & 63)) : 0.f;
+        const int r = 32 * hh + i;
+        acc += r < n ? ld_bf16(gp, sw128_off(r, c & 63)) * LOG2E : 0.f;
         Gm[i] = acc;
       }
-      if (rhalf == 0) xch[c] = acc;
+      if (hh == 0) xch[c] = acc;
     }
     __syncthreads();
-    if (rhalf == 1) {
+    if (hh == 1) {
       const float base = xch[c];
 #pragma unroll
       for (int i = 0; i < 32; ++i) Gm[i] += base;
@@ -235,288 +265,341 @@ __global__ void __launch_bounds__(THREADS, 1)
       bnd[1][c] = Gm[15];
       bnd[2][c] = Gm[31];
     }
-    __syncthreads();
-    float* tab = reinterpret_cast<float*>(sm + TAB);
-    if (tid < D) {
-      float b[5];
+    __syncthreads();  // the g tile is dead
+    if (blk + 1 < nblocks) {
+      if (tid == 0) {
+        fence_proxy_async_smem();
+        issue_g(blk + 1);
+      }
+      pend_g = true;
+    }
+    // ---------------- X and Y operands; (K e^Gamma)^T, (Q e^Gamma)^T and Khat^T are kept
+    // packed in registers and written once the X Y^T product has released the region
+    uint32_t kgp[16], qgp[16], khp[16];
+    {
+      const uint8_t* kp = sm + IN_K + 16384u * buf + (c >> 6) * BOX_BYTES;
+      const uint8_t* qp = sm + IN_Q + 16384u * buf + (c >> 6) * BOX_BYTES;
+      float bR[2], eB[2], eL[2], eRR[2][4];
 #pragma unroll
-      for (int R = 0; R < 5; ++R) b[R] = bnd[R][c];
+      for (int a = 0; a < 2; ++a) {
+        const int R = 2 * hh + a;
+        bR[a] = bnd[R][c];
+        eB[a] = ex2(bR[a]);               // e^{B_R}
+        eL[a] = ex2(bnd[4][c] - bR[a]);   // e^{Gamma_L - B_R}
 #pragma unroll
-      for (int R = 0; R < 4; ++R) {
-        tab[(TAB_EXPB + R) * D + c] = __expf(b[R]);
-        tab[(TAB_EXPL + R) * D + c] = __expf(b[4] - b[R]);
+        for (int Rp = 0; Rp < 4; ++Rp) eRR[a][Rp] = Rp > R ? ex2(bnd[Rp][c] - bR[a]) : 1.f;
       }
 #pragma unroll
-      for (int R = 0; R < 3; ++R)
+      for (int gi = 0; gi < 4; ++gi) {
+        const int a = gi >> 1;
+        const int R = 2 * hh + a;
+        float xk[8], xq[8], y[8], kg[8], qg[8], kh[8];
 #pragma unroll
-        for (int Rp = R + 1; Rp < 4; ++Rp) tab[(TAB_E + pair_index(R, Rp)) * D + c] = __expf(b[Rp] - b[R]);
-    }
-    // F = e^{Gamma_r - B_R} and its inverse, kept for the second operand pass
-    float F[32], Fi[32];
+        for (int e = 0; e < 8; ++e) {
+          const int i = 8 * gi + e;
+          const int r = 32 * hh + i;
+          const uint32_t o = sw128_off(r, c & 63);
+          const float kk = r < n ? ld_bf16(kp, o) : 0.f;
+          const float qq = r < n ? ld_bf16(qp, o) : 0.f;
+          const float L = Gm[i] - bR[a];
+          const float F = ex2(L), Fi = ex2(-L);
+          xk[e] = kk * F;
+          xq[e] = qq * F;
+          y[e] = kk * Fi;
+          kg[e] = xk[e] * eB[a];
+          qg[e] = xq[e] * eB[a];
+          kh[e] = y[e] * eL[a];
+        }
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int R = (32 * rhalf + i) >> 4;
-      const float L = Gm[i] - bnd[R][c];
-      F[i] = __expf(L);
-      Fi[i] = __expf(-L);
-    }
-    __syncthreads();
-    // ---------------- X = [k F ; q F] and Y_R' = k Fi e^{B_R - B_R'}... (R' >= R)
-    {
-      const uint8_t* kp = sm + IN_K + (c >> 6) * 8192;
-      const uint8_t* qp = sm + IN_Q + (c >> 6) * 8192;
-      uint8_t* xa = sm + XA + (c >> 6) * 16384;
-      const int cc = c & 63;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int r = 32 * rhalf + i;
-        const int R = r >> 4;
-        const uint32_t o = sw128_off(r, cc);
-        const float kk = r < n ? ld_bf16(kp, o) : 0.f;
-        const float qq = r < n ? ld_bf16(qp, o) : 0.f;
-        st_bf16(xa, o, kk * F[i]);
-        st_bf16(xa, sw128_off(64 + r, cc), qq * F[i]);
-        const float kf = kk * Fi[i];
+        for (int e = 0; e < 4; ++e) {
+          kgp[4 * gi + e] = pack_bf16(kg[2 * e], kg[2 * e + 1]);
+          qgp[4 * gi + e] = pack_bf16(qg[2 * e], qg[2 * e + 1]);
+          khp[4 * gi + e] = pack_bf16(kh[2 * e], kh[2 * e + 1]);
+        }
+        const uint32_t col = 32 * hh + 8 * gi;
+        st_shared_v4(sb + XK + sw128_off(c, col), pack_bf16(xk[0], xk[1]), pack_bf16(xk[2], xk[3]),
+                     pack_bf16(xk[4], xk[5]), pack_bf16(xk[6], xk[7]));
+        st_shared_v4(sb + XQ + sw128_off(c, col), pack_bf16(xq[0], xq[1]), pack_bf16(xq[2], xq[3]),
+                     pack_bf16(xq[4], xq[5]), pack_bf16(xq[6], xq[7]));
 #pragma unroll
         for (int Rp = 0; Rp < 4; ++Rp) {
           if (Rp < R) continue;
-          const float e = Rp == R ? 1.f : tab[(TAB_E + pair_index(R, Rp)) * D + c];
-          st_bf16(sm + y_base(Rp) + (c >> 6) * y_panel(Rp), o, kf * e);
+          const float f = eRR[a][Rp];
+          const int nidx = y_ofs(Rp) + 16 * R + 8 * (gi & 1);
+          st_shared_v4(sb + YP + 16384u * (uint32_t)(nidx >> 6) + sw128_off(c, nidx & 63),
+                       pack_bf16(y[0] * f, y[1] * f), pack_bf16(y[2] * f, y[3] * f),
+                       pack_bf16(y[4] * f, y[5] * f), pack_bf16(y[6] * f, y[7] * f));
         }
       }
     }
     fence_proxy_async_smem();
     __syncthreads();
-    // ---------------- tcgen05: D_R = X Y_R^T
+    // ---------------- tcgen05: D = X Y^T (M 128, N 160, K 128)
     if (tid == 0) {
       tc_fence_after();
+      const uint32_t idesc = idesc_bf16(128, 160, 1, 1, 0);
 #pragma unroll
-      for (int R = 0; R < 4; ++R) {
-        const uint32_t idesc = idesc_bf16(128, 16 * (R + 1), 0, 0, 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = desc_sw128(smem_u32(sm + XA + (kk >> 2) * 16384 + (kk & 3) * 32), 16, 1024);
-          const uint64_t b = desc_sw128(
-              smem_u32(sm + y_base(R) + (kk >> 2) * y_panel(R) + (kk & 3) * 32), 16, 1024);
-          umma_bf16(tmem + TM_AP + ap_off(R), a, b, idesc, kk > 0);
-        }
-      }
+      for (int kk = 0; kk < 8; ++kk)
+        umma_bf16(tmem + TD, desc_sw128(sb + XK + 2048u * kk, 16384, 1024),
+                  desc_sw128(sb + YP + 2048u * kk, 16384, 1024), idesc, kk > 0);
       umma_commit(&bar_mma);
     }
+    pend_mma = true;
     if (__syncthreads_or(!mma_done())) { aborted = true; break; }
-    // ---------------- A and P out of TMEM
+
+    // ---------------- the X/Y region is free: (K e^Gamma)^T, Khat^T, (Q e^Gamma)^T
+#pragma unroll
+    for (int gi = 0; gi < 4; ++gi) {
+      const uint32_t o = sw128_off(c, 32 * hh + 8 * gi);
+      st_shared_v4(sb + KG + o, kgp[4 * gi], kgp[4 * gi + 1], kgp[4 * gi + 2], kgp[4 * gi + 3]);
+      st_shared_v4(sb + KH + o, khp[4 * gi], khp[4 * gi + 1], khp[4 * gi + 2], khp[4 * gi + 3]);
+      st_shared_v4(sb + QG + o, qgp[4 * gi], qgp[4 * gi + 1], qgp[4 * gi + 2], qgp[4 * gi + 3]);
+    }
+    // ---------------- A (fp32, into WS) and P (bf16, into PT) out of TMEM
+    // Lane m: rows 0..63 are the k side (A), 64..127 the q side (P); row r = m & 63 belongs to
+    // block R = r >> 4 and reads the Y_R columns. This thread covers columns j in [32 hh, +32).
     {
-      float* Am = reinterpret_cast<float*>(sm + AM);
-      const bool pside = quarter >= 2;
-      const int r = (quarter & 1) * 32 + lane;     // block row index of this lane
-      const int R = ((quarter & 1) << 1) + colhalf;  // block this warp reads
-      const bool valid = (r >> 4) == R;
-      const int NR = 16 * (R + 1);
-      for (int c0 = 0; c0 < NR; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + tlane + TM_AP + ap_off(R) + c0, v);
-        tmem_ld_wait();
-        if (valid) {
-          if (!pside) {
-            const float b = beta_s[r];
+      float* ws = reinterpret_cast<float*>(sm + WS);
+      const int r = c & 63;
+      const int Rme = r >> 4;
+      const bool pside = c >= 64;
+      const int R0 = 2 * (quarter & 1);  // the warp's two blocks: R0 and R0 + 1
+      float vals[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int jj = c0 + j;
-              Am[r * AM_LD + jj] = (jj < r) ? b * __uint_as_float(v[j]) : 0.f;
-            }
-          } else {
-            float x[32];
+      for (int j = 0; j < 32; ++j) vals[j] = 0.f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = (c0 + j <= r) ? __uint_as_float(v[j]) : 0.f;
-            st_row32(sm + PS, r, c0, x);
+      for (int a = 0; a < 2; ++a) {
+        const int Rx = R0 + a;
+        const int ncols = min(32, 16 * (Rx + 1) - 32 * hh);  // warp-uniform
+        const uint32_t col = tl + TD + (uint32_t)(y_ofs(Rx) + 32 * hh);
+        if (ncols >= 32) {
+          uint32_t v[32];
+          tmem_ld32(col, v);
+          tmem_ld_wait();
+          if (Rme == Rx) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(v[j]);
+          }
+        } else if (ncols == 16) {
+          uint32_t v[16];
+          tmem_ld16(col, v);
+          tmem_ld_wait();
+          if (Rme == Rx) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) vals[j] = __uint_as_float(v[j]);
           }
         }
       }
-      if (valid) {  // the rest of the row is the (zero) upper triangle
-        if (!pside) {
-          for (int jj = NR; jj < C; ++jj) Am[r * AM_LD + jj] = 0.f;
-        } else if (NR < C) {
-          float z[32];
+      if (!pside) {
+        const float b = beta_s[r];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) z[j] = 0.f;
-          for (int c0 = NR; c0 < C; c0 += 32) {
-            // NR is a multiple of 16; write whole 8-element chunks up to 64
-            for (int cc8 = c0; cc8 < c0 + 32 && cc8 < C; cc8 += 8)
-              st_chunk8(sm + PS + sw128_off(r, cc8), z);
+        for (int j4 = 0; j4 < 8; ++j4) {
+          float4 x;
+          const int j = 32 * hh + 4 * j4;
+          x.x = (j < r) ? b * vals[4 * j4] : 0.f;
+          x.y = (j + 1 < r) ? b * vals[4 * j4 + 1] : 0.f;
+          x.z = (j + 2 < r) ? b * vals[4 * j4 + 2] : 0.f;
+          x.w = (j + 3 < r) ? b * vals[4 * j4 + 3] : 0.f;
+          *reinterpret_cast<float4*>(ws + wsi(r, j)) = x;
+        }
+      } else {
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8) {
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int j = 32 * hh + 8 * j8 + e;
+            x[e] = (j <= r) ? vals[8 * j8 + e] : 0.f;
           }
+          st_shared_v4(sb + PT + sw128_off(r, 32 * hh + 8 * j8), pack_bf16(x[0], x[1]),
+                       pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
         }
       }
     }
     tc_fence_before();
-    fence_proxy_async_smem();
     __syncthreads();
-    // ---------------- T = (I + A)^{-1}, in place in Am (16x16 block forward substitution)
+    // ---------------- T = (I + A)^{-1} (unit lower triangular), in place in WS
     {
-      float* Am = reinterpret_cast<float*>(sm + AM);
-      float* Xm = reinterpret_cast<float*>(sm + XM);
-      float col[16];
+      float* ws = reinterpret_cast<float*>(sm + WS);
+      float* mb = reinterpret_cast<float*>(sm + TB);  // M_R = -T_RR A_{R,<R}: 16x16R at 256 R(R-1)/2
+      // (1) diagonal 16 x 16 blocks by forward substitution, one column per thread
+      float x[16];
       const int Rd = tid >> 4, jj = tid & 15;
       if (tid < 64) {
+        const int base = 16 * Rd;
 #pragma unroll
-        for (int r2 = 0; r2 < 16; ++r2) {
+        for (int i = 0; i < 16; ++i) {
           float acc = 0.f;
 #pragma unroll
-          for (int i = 0; i < r2; ++i) acc = fmaf(Am[(16 * Rd + r2) * AM_LD + 16 * Rd + i], col[i], acc);
-          col[r2] = (r2 == jj) ? 1.f : (r2 > jj ? -acc : 0.f);
+          for (int m = 0; m < i; ++m) acc = fmaf(ws[wsi(base + i, base + m)], x[m], acc);
+          x[i] = (i == jj) ? 1.f : (i > jj ? -acc : 0.f);
         }
       }
       __syncthreads();
       if (tid < 64) {
 #pragma unroll
-        for (int r2 = 0; r2 < 16; ++r2) Am[(16 * Rd + r2) * AM_LD + 16 * Rd + jj] = col[r2];
+        for (int i = 0; i < 16; ++i) ws[wsi(16 * Rd + i, 16 * Rd + jj)] = x[i];
       }
       __syncthreads();
+      // (2) M_R = -T_RR A_{R, <16R} for R = 1..3 (independent of each other)
+      const int ir = tid >> 4, cc = tid & 15;
+#pragma unroll
       for (int R = 1; R < 4; ++R) {
-        const int nJ = 16 * R;
-        for (int idx = tid; idx < 16 * nJ; idx += THREADS) {
-          const int rr = idx / nJ, j = idx % nJ;
-          const float* arow = Am + (16 * R + rr) * AM_LD;
+        float t[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) t[m] = ws[wsi(16 * R + ir, 16 * R + m)];
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+          const int col = cc + 16 * u;
           float acc = 0.f;
-          for (int i = j; i < nJ; ++i) acc = fmaf(arow[i], Am[i * AM_LD + j], acc);
-          Xm[rr * 48 + j] = -acc;
+#pragma unroll
+          for (int m = 0; m < 16; ++m) acc = fmaf(t[m], ws[wsi(16 * R + m, col)], acc);
+          mb[128 * R * (R - 1) + ir * 16 * R + col] = -acc;
         }
-        __syncthreads();
-        for (int idx = tid; idx < 16 * nJ; idx += THREADS) {
-          const int rr = idx / nJ, j = idx % nJ;
-          const float* trow = Am + (16 * R + rr) * AM_LD + 16 * R;
+      }
+      __syncthreads();
+      // (3) block rows in order: T_{R, <16R} = M_R T_{<16R, <16R}
+#pragma unroll
+      for (int R = 1; R < 4; ++R) {
+        const float* mrow = mb + 128 * R * (R - 1) + ir * 16 * R;
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+          const int col = cc + 16 * u;
           float acc = 0.f;
-          for (int i = 0; i <= rr; ++i) acc = fmaf(trow[i], Xm[i * 48 + j], acc);
-          Am[(16 * R + rr) * AM_LD + j] = acc;
+#pragma unroll
+          for (int m = 0; m < 16 * R; ++m) acc = fmaf(mrow[m], ws[wsi(m, col)], acc);
+          ws[wsi(16 * R + ir, col)] = acc;
         }
         __syncthreads();
       }
-      // T Diag(beta) -> bf16, K-major (row r, column j)
+      // (4) T Diag(beta) -> bf16, K-major [r][j]
       {
         const int r = tid >> 2, j0 = (tid & 3) * 16;
-        float x[16];
+        float y[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) x[j] = (j0 + j <= r) ? Am[r * AM_LD + j0 + j] * beta_s[j0 + j] : 0.f;
-        st_chunk8(sm + TB + sw128_off(r, j0), x);
-        st_chunk8(sm + TB + sw128_off(r, j0 + 8), x + 8);
-      }
-    }
-    // K e^Gamma, Q e^Gamma, Khat (same swizzled [row][channel] layout as the input tiles)
-    {
-      const uint8_t* kp = sm + IN_K + (c >> 6) * 8192;
-      const uint8_t* qp = sm + IN_Q + (c >> 6) * 8192;
-      const float* tab2 = reinterpret_cast<const float*>(sm + TAB);
-      const int cc = c & 63;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int r = 32 * rhalf + i;
-        const int R = r >> 4;
-        const uint32_t o = sw128_off(r, cc);
-        const float kk = r < n ? ld_bf16(kp, o) : 0.f;
-        const float qq = r < n ? ld_bf16(qp, o) : 0.f;
-        const float eg = F[i] * tab2[(TAB_EXPB + R) * D + c];
-        st_bf16(sm + KG + (c >> 6) * 8192, o, kk * eg);
-        st_bf16(sm + QG + (c >> 6) * 8192, o, qq * eg);
-        st_bf16(sm + KH + (c >> 6) * 8192, o, kk * Fi[i] * tab2[(TAB_EXPL + R) * D + c]);
+        for (int e = 0; e < 16; ++e) y[e] = ws[wsi(r, j0 + e)] * beta_s[j0 + e];
+        st_shared_v4(sb + TB + sw128_off(r, j0), pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
+                     pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+        st_shared_v4(sb + TB + sw128_off(r, j0 + 8), pack_bf16(y[8], y[9]), pack_bf16(y[10], y[11]),
+                     pack_bf16(y[12], y[13]), pack_bf16(y[14], y[15]));
       }
     }
     fence_proxy_async_smem();
-    __syncthreads();
-    // ---------------- tcgen05: W^T and U~^T
+    {
+      const bool ok = mbar_wait(&bar_v, ph_v);
+      if (ok) ph_v ^= 1u;
+      pend_v = !ok;
+      if (__syncthreads_or(!ok)) { aborted = true; break; }
+    }
+    // ---------------- tcgen05: W^T = (K e^Gamma)^T (T Diag beta)^T ; U~^T = V^T (T Diag beta)^T
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, 64, 1, 0, 0);
+      const uint32_t id_w = idesc_bf16(128, 64, 0, 0, 0);
+      const uint32_t id_u = idesc_bf16(128, 64, 1, 0, 0);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t b = desc_sw128(smem_u32(sm + TB + kk * 32), 16, 1024);
-        umma_bf16(tmem + TM_WT, desc_sw128(smem_u32(sm + KG + kk * 2048), 8192, 1024), b, idesc, kk > 0);
-        umma_bf16(tmem + TM_U, desc_sw128(smem_u32(sm + IN_V + kk * 2048), 8192, 1024), b, idesc, kk > 0);
+        const uint64_t b = desc_sw128(sb + TB + 32u * kk, 16, 1024);
+        umma_bf16(tmem + TW, desc_sw128(sb + KG + 32u * kk, 16, 1024), b, id_w, kk > 0);
+        umma_bf16(tmem + TU, desc_sw128(sb + IN_V + 2048u * kk, BOX_BYTES, 1024), b, id_u, kk > 0);
       }
       umma_commit(&bar_mma);
     }
+    pend_mma = true;
     if (__syncthreads_or(!mma_done())) { aborted = true; break; }
-    // the input tiles are free: fetch the next block while the serial part runs
-    if (tid == 0 && t0 + C < len) {
-      issue_tma(t0 + C);
-      tma_pending = true;
+    if (blk + 1 < nblocks) {  // the v tile is dead
+      if (tid == 0) {
+        fence_proxy_async_smem();
+        issue_v(blk + 1);
+      }
+      pend_v = true;
     }
-    // W^T -> bf16 (MN-major B: row = channel c, columns = r)
+    // ---------------- -W^T -> bf16, MN-major [c][r]
     {
       uint32_t v[32];
-      tmem_ld32(tmem + tlane + TM_WT + 32 * colhalf, v);
+      tmem_ld32(tl + TW + 32 * hh, v);
       tmem_ld_wait();
-      float x[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
-      st_row32(sm + WT, 32 * quarter + lane, 32 * colhalf, x);
+      for (int k8 = 0; k8 < 4; ++k8)
+        st_shared_v4(sb + NW + sw128_off(c, 32 * hh + 8 * k8),
+                     pack_bf16(-__uint_as_float(v[8 * k8]), -__uint_as_float(v[8 * k8 + 1])),
+                     pack_bf16(-__uint_as_float(v[8 * k8 + 2]), -__uint_as_float(v[8 * k8 + 3])),
+                     pack_bf16(-__uint_as_float(v[8 * k8 + 4]), -__uint_as_float(v[8 * k8 + 5])),
+                     pack_bf16(-__uint_as_float(v[8 * k8 + 6]), -__uint_as_float(v[8 * k8 + 7])));
     }
     tc_fence_before();
     fence_proxy_async_smem();
     __syncthreads();
-    // ---------------- tcgen05: U^T = U~^T - S^T W^T ; O^T = S^T (Q e^Gamma)^T
+    // ---------------- tcgen05: [U^T | O^T] += S^T [-W^T | (Q e^Gamma)^T]  (M 128, N 128, K 128)
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t id_u = idesc_bf16(128, 64, 1, 1, 1);
-      const uint32_t id_o = idesc_bf16(128, 64, 1, 0, 0);
+      const uint32_t idesc = idesc_bf16(128, 128, 1, 1, 0);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t a = desc_sw128(smem_u32(sm + SS + kk * 2048), 16384, 1024);
-        umma_bf16(tmem + TM_U, a, desc_sw128(smem_u32(sm + WT + kk * 2048), 16384, 1024), id_u, 1);
-        umma_bf16(tmem + TM_O, a,
-                  desc_sw128(smem_u32(sm + QG + (kk >> 2) * 8192 + (kk & 3) * 32), 16, 1024), id_o,
-                  kk > 0);
-      }
+      for (int kk = 0; kk < 8; ++kk)
+        umma_bf16(tmem + TU, desc_sw128(sb + SS + 2048u * kk, 16384, 1024),
+                  desc_sw128(sb + NW + 2048u * kk, QG - NW, 1024), idesc, 1);
       umma_commit(&bar_mma);
     }
+    pend_mma = true;
     if (__syncthreads_or(!mma_done())) { aborted = true; break; }
-    // U -> bf16, K-major (row = v, column = r)
+    // ---------------- U -> bf16, K-major [v][r]
     {
       uint32_t v[32];
-      tmem_ld32(tmem + tlane + TM_U + 32 * colhalf, v);
+      tmem_ld32(tl + TU + 32 * hh, v);
       tmem_ld_wait();
-      float x[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
-      st_row32(sm + US, 32 * quarter + lane, 32 * colhalf, x);
+      for (int k8 = 0; k8 < 4; ++k8)
+        st_shared_v4(sb + US + sw128_off(c, 32 * hh + 8 * k8),
+                     pack_bf16(__uint_as_float(v[8 * k8]), __uint_as_float(v[8 * k8 + 1])),
+                     pack_bf16(__uint_as_float(v[8 * k8 + 2]), __uint_as_float(v[8 * k8 + 3])),
+                     pack_bf16(__uint_as_float(v[8 * k8 + 4]), __uint_as_float(v[8 * k8 + 5])),
+                     pack_bf16(__uint_as_float(v[8 * k8 + 6]), __uint_as_float(v[8 * k8 + 7])));
     }
     tc_fence_before();
     fence_proxy_async_smem();
     __syncthreads();
-    // ---------------- tcgen05: dS = Khat^T U ; O^T += U^T P^T
+    // ---------------- tcgen05: dS = Khat^T U (M 128, N 128, K 64); O^T += U^T P^T (M 128, N 64, K 64)
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t id_s = idesc_bf16(128, 128, 1, 0, 0);
+      const uint32_t id_s = idesc_bf16(128, 128, 0, 0, 0);
       const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t u = desc_sw128(smem_u32(sm + US + kk * 32), 16, 1024);
-        umma_bf16(tmem + TM_DS, desc_sw128(smem_u32(sm + KH + kk * 2048), 8192, 1024), u, id_s, kk > 0);
-        umma_bf16(tmem + TM_O, u, desc_sw128(smem_u32(sm + PS + kk * 32), 16, 1024), id_o, 1);
+        const uint64_t u = desc_sw128(sb + US + 32u * kk, 16, 1024);
+        umma_bf16(tmem + TS, desc_sw128(sb + KH + 32u * kk, 16, 1024), u, id_s, kk > 0);
+        umma_bf16(tmem + TO, u, desc_sw128(sb + PT + 32u * kk, 16, 1024), id_o, 1);
       }
       umma_commit(&bar_mma);
     }
+    pend_mma = true;
     if (__syncthreads_or(!mma_done())) { aborted = true; break; }
-    // ---------------- outputs and the state update
+    // ---------------- outputs, then the state update
     {
       uint32_t v[32];
-      tmem_ld32(tmem + tlane + TM_O + 32 * colhalf, v);
+      tmem_ld32(tl + TO + 32 * hh, v);
       tmem_ld_wait();
-      const int vcol = 32 * quarter + lane;
+      __nv_bfloat16* op = out + ((row0 + t0) * H + h) * D + c;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const int r = 32 * colhalf + j;
-        if (r < n) out[((row0 + t0 + r) * H + h) * D + vcol] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        const int r = 32 * hh + j;
+        if (r < n) op[(size_t)r * H * D] = __float2bfloat16_rn(__uint_as_float(v[j]));
       }
-      const float gl = __expf(bnd[4][c]);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = 0u;
+      tmem_st32(tl + TO + 32 * hh, v);  // O^T restarts from zero in the next block
+      const float gl = ex2(bnd[4][c]);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        tmem_ld32(tmem + tlane + TM_DS + 64 * colhalf + 32 * half, v);
+        tmem_ld32(tl + TS + 64 * hh + 32 * half, v);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j) S[32 * half + j] = fmaf(gl, S[32 * half + j], __uint_as_float(v[j]));
       }
-      uint8_t* panel = sm + SS + 16384u * colhalf;
-      st_row32(panel, c, 0, S);
-      st_row32(panel, c, 32, S + 32);
+      tmem_st_wait();
+#pragma unroll
+      for (int k8 = 0; k8 < 8; ++k8)
+        st_shared_v4(sb + SS + 16384u * hh + sw128_off(c, 8 * k8), pack_bf16(S[8 * k8], S[8 * k8 + 1]),
+                     pack_bf16(S[8 * k8 + 2], S[8 * k8 + 3]), pack_bf16(S[8 * k8 + 4], S[8 * k8 + 5]),
+                     pack_bf16(S[8 * k8 + 6], S[8 * k8 + 7]));
     }
     tc_fence_before();
     fence_proxy_async_smem();
@@ -525,9 +608,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (aborted) {
     record_status(4u /* KDA_ERR_TIMEOUT */);
-    if (tma_pending) (void)mbar_wait(&bar_tma, tma_phase);  // let an issued copy land
+    if (tid == 0) {  // let anything already issued land before the CTA's memory goes away
+      if (pend_mma) (void)mbar_wait(&bar_mma, ph_mma);
+      if (pend_kq & 1u) (void)mbar_wait(&bar_kq[0], ph_kq & 1u);
+      if (pend_kq & 2u) (void)mbar_wait(&bar_kq[1], (ph_kq >> 1) & 1u);
+      if (pend_g) (void)mbar_wait(&bar_g, ph_g);
+      if (pend_v) (void)mbar_wait(&bar_v, ph_v);
+    }
   } else if (P.S_final) {
-    float* sf = P.S_final + ((size_t)p * D + c) * D + 64 * colhalf;
+    float* sf = P.S_final + ((size_t)p * D + c) * D + 64 * hh;
 #pragma unroll
     for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4*>(sf + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
   }
