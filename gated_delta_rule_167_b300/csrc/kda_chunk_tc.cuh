@@ -69,12 +69,14 @@ constexpr uint32_t YP = XY + 32768;   //   Y, N = 160 columns in 3 MN-major B pa
 constexpr uint32_t KG = XY;           // after D: (K e^Gamma)^T [c][r], K-major A of W^T
 constexpr uint32_t KH = XY + 16384;   //   Khat^T [c][r], K-major A of dS
 constexpr uint32_t PT = XY + 32768;   //   P [r][j], K-major B of O^T += U^T P^T (8 KB)
-constexpr uint32_t WS = XY + 40960;   //   fp32 A then T (64 x 64, 16 KB); later -W^T, then U
+constexpr uint32_t WS = XY + 40960;   //   fp32 A then T ([64][WLD], 18 KB); later -W^T, then U
 constexpr uint32_t NW = WS;           //   -W^T [c][r], MN-major B panel 0 of the U/O product
 constexpr uint32_t US = WS;           //   U [v][r], K-major B of dS and A of O^T += U^T P^T
-constexpr uint32_t QG = XY + 57344;   //   (Q e^Gamma)^T [c][r], MN-major B panel 1 of U/O
-constexpr uint32_t TB = XY + 73728;   //   fp32 M_R during the solve, then T Diag(beta) [r][j]
-constexpr uint32_t SMEM_BYTES = XY + 81920;
+constexpr uint32_t QG = XY + 59392;   //   (Q e^Gamma)^T [c][r], MN-major B panel 1 of U/O
+constexpr uint32_t TB = XY + 75776;   //   fp32 M_R during the solve, then T Diag(beta) [r][j]
+constexpr uint32_t OS = KG;           // O staging for the TMA store (two [64][64] boxes), once
+                                      // the W^T product has released (K e^Gamma)^T
+constexpr uint32_t SMEM_BYTES = XY + 83968;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for aligning the base
 constexpr uint32_t BOX_BYTES = 8192;                // one 64-channel x 64-token TMA box
 
@@ -88,15 +90,14 @@ constexpr uint32_t TS = 352;  // dS, 128
 // First column of Y_R inside the N = 160 stack.
 __host__ __device__ constexpr int y_ofs(int R) { return 8 * R * (R + 1); }  // 0, 16, 48, 96
 
-// fp32 64 x 64 workspace index with the 16-byte chunks of each row rotated by the row, so that
-// a warp storing the same chunk of 32 consecutive rows hits every bank group.
-__device__ __forceinline__ int wsi(int r, int j) {
-  const int ch = j >> 2;
-  return r * 64 + (((ch ^ r) & 7) | (ch & 8)) * 4 + (j & 3);
-}
+// Row stride (floats) of the fp32 64 x 64 solve workspace: 72 makes the tf32 B-fragment loads
+// (rows t, columns g) conflict-free.
+constexpr int WLD = 72;
+// M_R = -T_RR A_{R,<16R} (16 x 16R, row stride 16R + 4) inside the TB region.
+__host__ __device__ constexpr int mb_off(int R) { return R == 1 ? 0 : (R == 2 ? 320 : 896); }
 
 struct TmaMaps {
-  CUtensorMap q, k, v, g;
+  CUtensorMap q, k, v, g, o;
 };
 
 using namespace sm100;
@@ -208,6 +209,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   fence_proxy_async_smem();
   __syncthreads();
 
+  // beta of the next block is loaded one block ahead (a strided global read)
+  float beta_next = 0.f;
+  if (tid < C && tid < len) beta_next = __bfloat162float(beta_g[(row0 + tid) * H + h]);
   bool aborted = false;
   auto mma_done = [&]() -> bool {
     const bool ok = mbar_wait(&bar_mma, ph_mma);
@@ -228,7 +232,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       pend_kq |= 1u << (buf ^ 1);
     }
-    if (tid < C) beta_s[tid] = tid < n ? __bfloat162float(beta_g[(row0 + t0 + tid) * H + h]) : 0.f;
+    if (tid < C) {
+      beta_s[tid] = beta_next;  // zero past the end of the sequence
+      beta_next = 0.f;
+      if (tid < len - t0 - C) beta_next = __bfloat162float(beta_g[(row0 + t0 + C + tid) * H + h]);
+    }
     {
       const bool ok = mbar_wait(&bar_g, ph_g);
       if (ok) ph_g ^= 1u;
@@ -253,6 +261,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (hh == 0) xch[c] = acc;
     }
+    if (tid == 0) bulk_wait_read();  // the previous block's O store has left the staging tiles
     __syncthreads();
     if (hh == 1) {
       const float base = xch[c];
@@ -400,7 +409,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           x.y = (j + 1 < r) ? b * vals[4 * j4 + 1] : 0.f;
           x.z = (j + 2 < r) ? b * vals[4 * j4 + 2] : 0.f;
           x.w = (j + 3 < r) ? b * vals[4 * j4 + 3] : 0.f;
-          *reinterpret_cast<float4*>(ws + wsi(r, j)) = x;
+          *reinterpret_cast<float4*>(ws + r * WLD + j) = x;
         }
       } else {
 #pragma unroll
@@ -421,54 +430,67 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- T = (I + A)^{-1} (unit lower triangular), in place in WS
     {
       float* ws = reinterpret_cast<float*>(sm + WS);
-      float* mb = reinterpret_cast<float*>(sm + TB);  // M_R = -T_RR A_{R,<R}: 16x16R at 256 R(R-1)/2
-      // (1) diagonal 16 x 16 blocks by forward substitution, one column per thread
+      float* mb = reinterpret_cast<float*>(sm + TB);
+      const int lane = tid & 31;
+      const int g = lane >> 2, t = lane & 3;
+      // (1) diagonal 16 x 16 blocks T_RR by forward substitution, one column per thread
       float x[16];
       const int Rd = tid >> 4, jj = tid & 15;
       if (tid < 64) {
-        const int base = 16 * Rd;
+        const float* bp = ws + 16 * Rd * (WLD + 1);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           float acc = 0.f;
 #pragma unroll
-          for (int m = 0; m < i; ++m) acc = fmaf(ws[wsi(base + i, base + m)], x[m], acc);
+          for (int m = 0; m < i; ++m) acc = fmaf(bp[i * WLD + m], x[m], acc);
           x[i] = (i == jj) ? 1.f : (i > jj ? -acc : 0.f);
         }
       }
       __syncthreads();
       if (tid < 64) {
+        float* cp = ws + 16 * Rd * (WLD + 1) + jj;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) ws[wsi(16 * Rd + i, 16 * Rd + jj)] = x[i];
+        for (int i = 0; i < 16; ++i) cp[i * WLD] = x[i];
       }
       __syncthreads();
-      // (2) M_R = -T_RR A_{R, <16R} for R = 1..3 (independent of each other)
-      const int ir = tid >> 4, cc = tid & 15;
+      // (2) M_R = -T_RR A_{R,<16R} for R = 1..3 (independent): 12 tiles of 16 x 8, two k steps
+      for (int tile = warp; tile < 12; tile += THREADS / 32) {
+        const int R = tile < 2 ? 1 : (tile < 6 ? 2 : 3);
+        const int nt = tile - (R == 1 ? 0 : (R == 2 ? 2 : 6));
+        const float* tr = ws + 16 * R * (WLD + 1);
+        const float* ar = ws + 16 * R * WLD + 8 * nt;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int R = 1; R < 4; ++R) {
-        float t[16];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) t[m] = ws[wsi(16 * R + ir, 16 * R + m)];
-#pragma unroll
-        for (int u = 0; u < R; ++u) {
-          const int col = cc + 16 * u;
-          float acc = 0.f;
-#pragma unroll
-          for (int m = 0; m < 16; ++m) acc = fmaf(t[m], ws[wsi(16 * R + m, col)], acc);
-          mb[128 * R * (R - 1) + ir * 16 * R + col] = -acc;
+        for (int ks = 0; ks < 2; ++ks) {
+          const float a[4] = {tr[g * WLD + 8 * ks + t], tr[(g + 8) * WLD + 8 * ks + t],
+                              tr[g * WLD + 8 * ks + t + 4], tr[(g + 8) * WLD + 8 * ks + t + 4]};
+          const float b[2] = {ar[(8 * ks + t) * WLD + g], ar[(8 * ks + t + 4) * WLD + g]};
+          mma_3xtf32(d, a, b);
         }
+        const int ld = 16 * R + 4;
+        float* mo = mb + mb_off(R) + 8 * nt;
+        *reinterpret_cast<float2*>(mo + g * ld + 2 * t) = make_float2(-d[0], -d[1]);
+        *reinterpret_cast<float2*>(mo + (g + 8) * ld + 2 * t) = make_float2(-d[2], -d[3]);
       }
       __syncthreads();
-      // (3) block rows in order: T_{R, <16R} = M_R T_{<16R, <16R}
+      // (3) block rows in order: T_{R,<16R} = M_R T_{<16R,<16R}; T is zero above its diagonal,
+      // so k steps above the output tile's columns are skipped
 #pragma unroll
       for (int R = 1; R < 4; ++R) {
-        const float* mrow = mb + 128 * R * (R - 1) + ir * 16 * R;
-#pragma unroll
-        for (int u = 0; u < R; ++u) {
-          const int col = cc + 16 * u;
-          float acc = 0.f;
-#pragma unroll
-          for (int m = 0; m < 16 * R; ++m) acc = fmaf(mrow[m], ws[wsi(m, col)], acc);
-          ws[wsi(16 * R + ir, col)] = acc;
+        const int ld = 16 * R + 4;
+        const float* mr = mb + mb_off(R);
+        for (int nt = warp; nt < 2 * R; nt += THREADS / 32) {
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int ks = nt; ks < 2 * R; ++ks) {
+            const float a[4] = {mr[g * ld + 8 * ks + t], mr[(g + 8) * ld + 8 * ks + t],
+                                mr[g * ld + 8 * ks + t + 4], mr[(g + 8) * ld + 8 * ks + t + 4]};
+            const float b[2] = {ws[(8 * ks + t) * WLD + 8 * nt + g],
+                                ws[(8 * ks + t + 4) * WLD + 8 * nt + g]};
+            mma_3xtf32(d, a, b);
+          }
+          float* to = ws + 16 * R * WLD + 8 * nt;
+          *reinterpret_cast<float2*>(to + g * WLD + 2 * t) = make_float2(d[0], d[1]);
+          *reinterpret_cast<float2*>(to + (g + 8) * WLD + 2 * t) = make_float2(d[2], d[3]);
         }
         __syncthreads();
       }
@@ -477,7 +499,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int r = tid >> 2, j0 = (tid & 3) * 16;
         float y[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) y[e] = ws[wsi(r, j0 + e)] * beta_s[j0 + e];
+        for (int e = 0; e < 16; ++e) y[e] = ws[r * WLD + j0 + e] * beta_s[j0 + e];
         st_shared_v4(sb + TB + sw128_off(r, j0), pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
                      pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
         st_shared_v4(sb + TB + sw128_off(r, j0 + 8), pack_bf16(y[8], y[9]), pack_bf16(y[10], y[11]),
@@ -577,11 +599,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t v[32];
       tmem_ld32(tl + TO + 32 * hh, v);
       tmem_ld_wait();
-      __nv_bfloat16* op = out + ((row0 + t0) * H + h) * D + c;
+      if (n == C) {  // full block: stage [token][channel] boxes for one TMA store
+        uint8_t* ob = sm + OS + (c >> 6) * BOX_BYTES;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int r = 32 * hh + j;
-        if (r < n) op[(size_t)r * H * D] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        for (int j = 0; j < 32; ++j)
+          *reinterpret_cast<__nv_bfloat16*>(ob + sw128_off(32 * hh + j, c & 63)) =
+              __float2bfloat16_rn(__uint_as_float(v[j]));
+      } else {  // partial last block: plain stores of the valid rows only
+        __nv_bfloat16* op = out + ((row0 + t0) * H + h) * D + c;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int r = 32 * hh + j;
+          if (r < n) op[(size_t)r * H * D] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        }
       }
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = 0u;
@@ -604,7 +634,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_before();
     fence_proxy_async_smem();
     __syncthreads();
+    if (n == C && tid == 0) {
+      tma_store_3d(&maps.o, sm + OS, 0, h, (int)(row0 + t0));
+      tma_store_3d(&maps.o, sm + OS + BOX_BYTES, 64, h, (int)(row0 + t0));
+      bulk_commit();
+    }
   }
+  if (tid == 0) bulk_wait_all();
 
   if (aborted) {
     record_status(4u /* KDA_ERR_TIMEOUT */);
@@ -665,7 +701,8 @@ inline kda_status_t launch_chunk_tc(const SeqParams& P, int n_problems, int C, c
   tc::TmaMaps maps;
   const long long rows = P.cu_seqlens ? (long long)P.T : (long long)P.n_seq * P.T;
   if (!tc::encode_token_map(&maps.q, P.q, rows, P.H) || !tc::encode_token_map(&maps.k, P.k, rows, P.H) ||
-      !tc::encode_token_map(&maps.v, P.v, rows, P.H) || !tc::encode_token_map(&maps.g, P.g, rows, P.H)) {
+      !tc::encode_token_map(&maps.v, P.v, rows, P.H) || !tc::encode_token_map(&maps.g, P.g, rows, P.H) ||
+      !tc::encode_token_map(&maps.o, P.out, rows, P.H)) {
     err = "cuTensorMapEncodeTiled failed";
     return KDA_ERR_CUDA;
   }
