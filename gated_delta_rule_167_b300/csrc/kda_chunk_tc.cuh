@@ -30,12 +30,13 @@
 //         16 x 16 blocks in fp32; T Diag(beta) in bf16
 //   tcgen05: W^T = (K e^Gamma)^T (T Diag beta)^T,  U~^T = V^T (T Diag beta)^T
 //   SIMT: -W^T to shared memory                        tcgen05: [U^T | O^T] += S^T [-W^T | (Q e^Gamma)^T]
-//   SIMT: U to shared memory                           tcgen05: dS = Khat^T U,  O^T += U^T P^T
-//   SIMT: O to global memory (bf16); S <- e^{Gamma_L} S + dS in fp32 registers, bf16 copy to
-//         shared memory as the next block's operand.
+//   SIMT: U to shared memory                           tcgen05: S += Khat^T U,  O^T += U^T P^T
+//   SIMT: O to global memory (bf16, TMA store); bf16 copy of S to shared memory as the next
+//         block's operand.
 // Transposed forms keep every product at M = 128 (TMEM lane = row). The fp32 state lives in
-// registers for the whole sequence; only its bf16 copy feeds the tensor cores, so rounding does
-// not accumulate in S itself. Every wait is bounded; a timeout latches KDA_ERR_TIMEOUT, lets
+// TMEM for the whole sequence: while X Y^T runs it is scaled by e^{Gamma_L} in place, and the
+// Khat^T U product accumulates onto it. Only its bf16 copy feeds the tensor cores, so rounding
+// does not accumulate in S itself. Every wait is bounded; a timeout latches KDA_ERR_TIMEOUT, lets
 // issued copies and products land, frees TMEM and returns.
 #pragma once
 
@@ -74,8 +75,8 @@ constexpr uint32_t NW = WS;           //   -W^T [c][r], MN-major B panel 0 of th
 constexpr uint32_t US = WS;           //   U [v][r], K-major B of dS and A of O^T += U^T P^T
 constexpr uint32_t QG = XY + 59392;   //   (Q e^Gamma)^T [c][r], MN-major B panel 1 of U/O
 constexpr uint32_t TB = XY + 75776;   //   fp32 M_R during the solve, then T Diag(beta) [r][j]
-constexpr uint32_t OS = KG;           // O staging for the TMA store (two [64][64] boxes), once
-                                      // the W^T product has released (K e^Gamma)^T
+constexpr uint32_t OS = WS;           // O staging for the TMA store (two [64][64] boxes) once
+                                      // the dS / O products have released U
 constexpr uint32_t SMEM_BYTES = XY + 83968;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for aligning the base
 constexpr uint32_t BOX_BYTES = 8192;                // one 64-channel x 64-token TMA box
@@ -85,7 +86,7 @@ constexpr uint32_t TD = 0;    // X Y^T, 160 columns
 constexpr uint32_t TW = 160;  // W^T, 64
 constexpr uint32_t TU = 224;  // U~^T, then U^T, 64
 constexpr uint32_t TO = 288;  // O^T, 64 (directly after TU: the U/O product writes both)
-constexpr uint32_t TS = 352;  // dS, 128
+constexpr uint32_t TS = 352;  // fp32 state S [k][v], 128 (the S += Khat^T U product accumulates here)
 
 // First column of Y_R inside the N = 160 stack.
 __host__ __device__ constexpr int y_ofs(int R) { return 8 * R * (R + 1); }  // 0, 16, 48, 96
@@ -114,15 +115,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t sb = smem_u32(sm);
   __shared__ uint64_t bar_kq[2], bar_g, bar_v, bar_mma;
   __shared__ uint32_t tmem_base_s;
-  __shared__ float beta_s[C];
+  __shared__ __align__(16) float beta_s[C];
   __shared__ float xch[D];
   __shared__ float bnd[5][D];  // log2-domain Gamma at the block boundaries: B_0..B_3, B_4 = Gamma_L
+  __shared__ float trr[4][16][17];  // diagonal blocks T_RR of the solve
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int quarter = warp & 3;  // TMEM lane quarter this warp may address
   const int c = tid & (D - 1);   // channel (= TMEM lane) owned in the elementwise phases
   const int hh = tid >> 7;       // which half of the rows / columns this thread handles
+  const int g = (tid & 31) >> 2, t = tid & 3;  // m16n8k8 fragment coordinates
 
   int h, len;
   size_t row0;
@@ -173,19 +176,27 @@ __global__ void __launch_bounds__(THREADS, 1)
   };
 
   // ---- initial state: fp32 in registers (row c, columns 64 hh ..), bf16 copy in SS
-  float S[64];
   {
     const float* s0 = P.S0 ? P.S0 + ((size_t)p * D + c) * D + 64 * hh : nullptr;
 #pragma unroll
-    for (int j = 0; j < 64; j += 4) {
-      float4 x = s0 ? *reinterpret_cast<const float4*>(s0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-      S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
-    }
+    for (int half = 0; half < 2; ++half) {
+      uint32_t sv[32];
 #pragma unroll
-    for (int k8 = 0; k8 < 8; ++k8)
-      st_shared_v4(sb + SS + 16384u * hh + sw128_off(c, 8 * k8), pack_bf16(S[8 * k8], S[8 * k8 + 1]),
-                   pack_bf16(S[8 * k8 + 2], S[8 * k8 + 3]), pack_bf16(S[8 * k8 + 4], S[8 * k8 + 5]),
-                   pack_bf16(S[8 * k8 + 6], S[8 * k8 + 7]));
+      for (int j = 0; j < 32; j += 4) {
+        const float4 x = s0 ? *reinterpret_cast<const float4*>(s0 + 32 * half + j)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        sv[j] = __float_as_uint(x.x); sv[j + 1] = __float_as_uint(x.y);
+        sv[j + 2] = __float_as_uint(x.z); sv[j + 3] = __float_as_uint(x.w);
+      }
+      tmem_st32(tl + TS + 64 * hh + 32 * half, sv);
+#pragma unroll
+      for (int k8 = 0; k8 < 4; ++k8)
+        st_shared_v4(sb + SS + 16384u * hh + sw128_off(c, 32 * half + 8 * k8),
+                     pack_bf16(__uint_as_float(sv[8 * k8]), __uint_as_float(sv[8 * k8 + 1])),
+                     pack_bf16(__uint_as_float(sv[8 * k8 + 2]), __uint_as_float(sv[8 * k8 + 3])),
+                     pack_bf16(__uint_as_float(sv[8 * k8 + 4]), __uint_as_float(sv[8 * k8 + 5])),
+                     pack_bf16(__uint_as_float(sv[8 * k8 + 6]), __uint_as_float(sv[8 * k8 + 7])));
+    }
     uint32_t z[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) z[j] = 0u;
@@ -210,8 +221,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
 
   // beta of the next block is loaded one block ahead (a strided global read)
-  float beta_next = 0.f;
-  if (tid < C && tid < len) beta_next = __bfloat162float(beta_g[(row0 + tid) * H + h]);
+  // (kept as raw bits so that nothing waits on the load until the block that needs it)
+  unsigned short beta_next = 0;
+  const unsigned short* __restrict__ beta_u = reinterpret_cast<const unsigned short*>(beta_g);
+  if (tid < C && tid < len) beta_next = beta_u[(row0 + tid) * H + h];
   bool aborted = false;
   auto mma_done = [&]() -> bool {
     const bool ok = mbar_wait(&bar_mma, ph_mma);
@@ -233,9 +246,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       pend_kq |= 1u << (buf ^ 1);
     }
     if (tid < C) {
-      beta_s[tid] = beta_next;  // zero past the end of the sequence
-      beta_next = 0.f;
-      if (tid < len - t0 - C) beta_next = __bfloat162float(beta_g[(row0 + t0 + C + tid) * H + h]);
+      beta_s[tid] = __uint_as_float((uint32_t)beta_next << 16);  // zero past the end
+      beta_next = 0;
+      if (tid < len - t0 - C) beta_next = beta_u[(row0 + t0 + C + tid) * H + h];
     }
     {
       const bool ok = mbar_wait(&bar_g, ph_g);
@@ -252,16 +265,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     float Gm[32];
     {
       const uint8_t* gp = sm + IN_G + (c >> 6) * BOX_BYTES;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) Gm[i] = ld_bf16(gp, sw128_off(32 * hh + i, c & 63));
       float acc = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const int r = 32 * hh + i;
-        acc += r < n ? ld_bf16(gp, sw128_off(r, c & 63)) * LOG2E : 0.f;
+        acc = fmaf(32 * hh + i < n ? Gm[i] : 0.f, LOG2E, acc);
         Gm[i] = acc;
       }
       if (hh == 0) xch[c] = acc;
     }
-    if (tid == 0) bulk_wait_read();  // the previous block's O store has left the staging tiles
     __syncthreads();
     if (hh == 1) {
       const float base = xch[c];
@@ -274,6 +287,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       bnd[1][c] = Gm[15];
       bnd[2][c] = Gm[31];
     }
+    if (tid == 0) bulk_wait_read();  // the previous block's O store has left the staging tiles
     __syncthreads();  // the g tile is dead
     if (blk + 1 < nblocks) {
       if (tid == 0) {
@@ -298,18 +312,31 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int Rp = 0; Rp < 4; ++Rp) eRR[a][Rp] = Rp > R ? ex2(bnd[Rp][c] - bR[a]) : 1.f;
       }
+      float kv[16], qv[16];
 #pragma unroll
       for (int gi = 0; gi < 4; ++gi) {
         const int a = gi >> 1;
         const int R = 2 * hh + a;
+        if ((gi & 1) == 0) {  // the next 16 rows of k and q, loaded before any use
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const uint32_t o = sw128_off(32 * hh + 8 * gi + e, c & 63);
+            kv[e] = ld_bf16(kp, o);
+            qv[e] = ld_bf16(qp, o);
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const bool live = 32 * hh + 8 * gi + e < n;
+            kv[e] = live ? kv[e] : 0.f;
+            qv[e] = live ? qv[e] : 0.f;
+          }
+        }
         float xk[8], xq[8], y[8], kg[8], qg[8], kh[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int i = 8 * gi + e;
-          const int r = 32 * hh + i;
-          const uint32_t o = sw128_off(r, c & 63);
-          const float kk = r < n ? ld_bf16(kp, o) : 0.f;
-          const float qq = r < n ? ld_bf16(qp, o) : 0.f;
+          const float kk = kv[8 * (gi & 1) + e];
+          const float qq = qv[8 * (gi & 1) + e];
           const float L = Gm[i] - bR[a];
           const float F = ex2(L), Fi = ex2(-L);
           xk[e] = kk * F;
@@ -354,6 +381,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       umma_commit(&bar_mma);
     }
     pend_mma = true;
+    // ---------------- while X Y^T runs: S <- e^{Gamma_L} S in TMEM (dS accumulates onto it)
+    {
+      const float gl = ex2(bnd[4][c]);
+      uint32_t v[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        tmem_ld32(tl + TS + 64 * hh + 32 * half, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(gl * __uint_as_float(v[j]));
+        tmem_st32(tl + TS + 64 * hh + 32 * half, v);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+    }
     if (__syncthreads_or(!mma_done())) { aborted = true; break; }
 
     // ---------------- the X/Y region is free: (K e^Gamma)^T, Khat^T, (Q e^Gamma)^T
@@ -431,46 +473,57 @@ __global__ void __launch_bounds__(THREADS, 1)
     {
       float* ws = reinterpret_cast<float*>(sm + WS);
       float* mb = reinterpret_cast<float*>(sm + TB);
-      const int lane = tid & 31;
-      const int g = lane >> 2, t = lane & 3;
-      // (1) diagonal 16 x 16 blocks T_RR by forward substitution, one column per thread
+      // (1) diagonal 16 x 16 blocks T_RR by forward substitution, one column per thread; the
+      // result goes to trr so that A_RR stays readable until every column is done
       float x[16];
       const int Rd = tid >> 4, jj = tid & 15;
       if (tid < 64) {
         const float* bp = ws + 16 * Rd * (WLD + 1);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          float acc = 0.f;
+          float arow[16];
 #pragma unroll
-          for (int m = 0; m < i; ++m) acc = fmaf(bp[i * WLD + m], x[m], acc);
-          x[i] = (i == jj) ? 1.f : (i > jj ? -acc : 0.f);
+          for (int m4 = 0; m4 < 4; ++m4) {
+            const float4 v4 = *reinterpret_cast<const float4*>(bp + i * WLD + 4 * m4);
+            arow[4 * m4] = v4.x; arow[4 * m4 + 1] = v4.y; arow[4 * m4 + 2] = v4.z; arow[4 * m4 + 3] = v4.w;
+          }
+          float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+          for (int m = 0; m < i; ++m) {
+            if (m & 1) acc1 = fmaf(arow[m], x[m], acc1);
+            else acc0 = fmaf(arow[m], x[m], acc0);
+          }
+          x[i] = (i == jj) ? 1.f : (i > jj ? -(acc0 + acc1) : 0.f);
         }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) trr[Rd][i][jj] = x[i];
       }
       __syncthreads();
+      // (2) M_R = -T_RR A_{R,<16R} for R = 1..3 (independent): 12 tiles of 16 x 8, two k steps.
+      // Meanwhile the diagonal blocks of WS receive T_RR.
       if (tid < 64) {
         float* cp = ws + 16 * Rd * (WLD + 1) + jj;
 #pragma unroll
         for (int i = 0; i < 16; ++i) cp[i * WLD] = x[i];
       }
-      __syncthreads();
-      // (2) M_R = -T_RR A_{R,<16R} for R = 1..3 (independent): 12 tiles of 16 x 8, two k steps
       for (int tile = warp; tile < 12; tile += THREADS / 32) {
         const int R = tile < 2 ? 1 : (tile < 6 ? 2 : 3);
         const int nt = tile - (R == 1 ? 0 : (R == 2 ? 2 : 6));
-        const float* tr = ws + 16 * R * (WLD + 1);
         const float* ar = ws + 16 * R * WLD + 8 * nt;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc[3][4] = {};
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
-          const float a[4] = {tr[g * WLD + 8 * ks + t], tr[(g + 8) * WLD + 8 * ks + t],
-                              tr[g * WLD + 8 * ks + t + 4], tr[(g + 8) * WLD + 8 * ks + t + 4]};
+          const float a[4] = {trr[R][g][8 * ks + t], trr[R][g + 8][8 * ks + t],
+                              trr[R][g][8 * ks + t + 4], trr[R][g + 8][8 * ks + t + 4]};
           const float b[2] = {ar[(8 * ks + t) * WLD + g], ar[(8 * ks + t + 4) * WLD + g]};
-          mma_3xtf32(d, a, b);
+          mma_3xtf32_split(acc, a, b);
         }
         const int ld = 16 * R + 4;
         float* mo = mb + mb_off(R) + 8 * nt;
-        *reinterpret_cast<float2*>(mo + g * ld + 2 * t) = make_float2(-d[0], -d[1]);
-        *reinterpret_cast<float2*>(mo + (g + 8) * ld + 2 * t) = make_float2(-d[2], -d[3]);
+        *reinterpret_cast<float2*>(mo + g * ld + 2 * t) =
+            make_float2(-(acc[0][0] + acc[1][0] + acc[2][0]), -(acc[0][1] + acc[1][1] + acc[2][1]));
+        *reinterpret_cast<float2*>(mo + (g + 8) * ld + 2 * t) =
+            make_float2(-(acc[0][2] + acc[1][2] + acc[2][2]), -(acc[0][3] + acc[1][3] + acc[2][3]));
       }
       __syncthreads();
       // (3) block rows in order: T_{R,<16R} = M_R T_{<16R,<16R}; T is zero above its diagonal,
@@ -479,18 +532,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int R = 1; R < 4; ++R) {
         const int ld = 16 * R + 4;
         const float* mr = mb + mb_off(R);
-        for (int nt = warp; nt < 2 * R; nt += THREADS / 32) {
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
-          for (int ks = nt; ks < 2 * R; ++ks) {
+        if (warp < 2 * R) {
+          const int nt = warp;
+          float acc[3][4] = {};
+#pragma unroll
+          for (int ks = 0; ks < 2 * R; ++ks) {
+            if (ks < nt) continue;
             const float a[4] = {mr[g * ld + 8 * ks + t], mr[(g + 8) * ld + 8 * ks + t],
                                 mr[g * ld + 8 * ks + t + 4], mr[(g + 8) * ld + 8 * ks + t + 4]};
             const float b[2] = {ws[(8 * ks + t) * WLD + 8 * nt + g],
                                 ws[(8 * ks + t + 4) * WLD + 8 * nt + g]};
-            mma_3xtf32(d, a, b);
+            mma_3xtf32_split(acc, a, b);
           }
           float* to = ws + 16 * R * WLD + 8 * nt;
-          *reinterpret_cast<float2*>(to + g * WLD + 2 * t) = make_float2(d[0], d[1]);
-          *reinterpret_cast<float2*>(to + (g + 8) * WLD + 2 * t) = make_float2(d[2], d[3]);
+          *reinterpret_cast<float2*>(to + g * WLD + 2 * t) =
+              make_float2(acc[0][0] + acc[1][0] + acc[2][0], acc[0][1] + acc[1][1] + acc[2][1]);
+          *reinterpret_cast<float2*>(to + (g + 8) * WLD + 2 * t) =
+              make_float2(acc[0][2] + acc[1][2] + acc[2][2], acc[0][3] + acc[1][3] + acc[2][3]);
         }
         __syncthreads();
       }
@@ -499,7 +557,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int r = tid >> 2, j0 = (tid & 3) * 16;
         float y[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) y[e] = ws[r * WLD + j0 + e] * beta_s[j0 + e];
+        for (int e4 = 0; e4 < 4; ++e4) {
+          const float4 v4 = *reinterpret_cast<const float4*>(ws + r * WLD + j0 + 4 * e4);
+          const float4 b4 = *reinterpret_cast<const float4*>(beta_s + j0 + 4 * e4);
+          y[4 * e4] = v4.x * b4.x; y[4 * e4 + 1] = v4.y * b4.y;
+          y[4 * e4 + 2] = v4.z * b4.z; y[4 * e4 + 3] = v4.w * b4.w;
+        }
         st_shared_v4(sb + TB + sw128_off(r, j0), pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
                      pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
         st_shared_v4(sb + TB + sw128_off(r, j0 + 8), pack_bf16(y[8], y[9]), pack_bf16(y[10], y[11]),
@@ -579,7 +642,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_before();
     fence_proxy_async_smem();
     __syncthreads();
-    // ---------------- tcgen05: dS = Khat^T U (M 128, N 128, K 64); O^T += U^T P^T (M 128, N 64, K 64)
+    // ---------------- tcgen05: S += Khat^T U (M 128, N 128, K 64); O^T += U^T P^T (M 128, N 64, K 64)
     if (tid == 0) {
       tc_fence_after();
       const uint32_t id_s = idesc_bf16(128, 128, 0, 0, 0);
@@ -587,7 +650,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t u = desc_sw128(sb + US + 32u * kk, 16, 1024);
-        umma_bf16(tmem + TS, desc_sw128(sb + KH + 32u * kk, 16, 1024), u, id_s, kk > 0);
+        umma_bf16(tmem + TS, desc_sw128(sb + KH + 32u * kk, 16, 1024), u, id_s, 1);
         umma_bf16(tmem + TO, u, desc_sw128(sb + PT + 32u * kk, 16, 1024), id_o, 1);
       }
       umma_commit(&bar_mma);
@@ -616,20 +679,19 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = 0u;
       tmem_st32(tl + TO + 32 * hh, v);  // O^T restarts from zero in the next block
-      const float gl = ex2(bnd[4][c]);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int half = 0; half < 2; ++half) {  // bf16 copy of the new state for the next block
         tmem_ld32(tl + TS + 64 * hh + 32 * half, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) S[32 * half + j] = fmaf(gl, S[32 * half + j], __uint_as_float(v[j]));
+        for (int k8 = 0; k8 < 4; ++k8)
+          st_shared_v4(sb + SS + 16384u * hh + sw128_off(c, 32 * half + 8 * k8),
+                       pack_bf16(__uint_as_float(v[8 * k8]), __uint_as_float(v[8 * k8 + 1])),
+                       pack_bf16(__uint_as_float(v[8 * k8 + 2]), __uint_as_float(v[8 * k8 + 3])),
+                       pack_bf16(__uint_as_float(v[8 * k8 + 4]), __uint_as_float(v[8 * k8 + 5])),
+                       pack_bf16(__uint_as_float(v[8 * k8 + 6]), __uint_as_float(v[8 * k8 + 7])));
       }
       tmem_st_wait();
-#pragma unroll
-      for (int k8 = 0; k8 < 8; ++k8)
-        st_shared_v4(sb + SS + 16384u * hh + sw128_off(c, 8 * k8), pack_bf16(S[8 * k8], S[8 * k8 + 1]),
-                     pack_bf16(S[8 * k8 + 2], S[8 * k8 + 3]), pack_bf16(S[8 * k8 + 4], S[8 * k8 + 5]),
-                     pack_bf16(S[8 * k8 + 6], S[8 * k8 + 7]));
     }
     tc_fence_before();
     fence_proxy_async_smem();
@@ -653,8 +715,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (P.S_final) {
     float* sf = P.S_final + ((size_t)p * D + c) * D + 64 * hh;
+    uint32_t v[32];
 #pragma unroll
-    for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4*>(sf + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    for (int half = 0; half < 2; ++half) {
+      tmem_ld32(tl + TS + 64 * hh + 32 * half, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(sf + 32 * half + j) =
+            make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                        __uint_as_float(v[j + 3]));
+    }
   }
   tc_fence_before();
   __syncthreads();
