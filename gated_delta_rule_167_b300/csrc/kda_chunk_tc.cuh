@@ -2,11 +2,13 @@
 //
 // Mathematics (Kimi K3 wiki: "Notations mathématiques", table "Attention et KDA" for the
 // recurrence; "Glossaire", entries "Chunkwise", "UT" and "Décroissance bornée"). For one block
-// of C tokens, with Gamma the inclusive cumulative sum of g inside the block:
+// of C tokens with incoming state S, Gamma the inclusive cumulative sum of g inside the block:
 //   A_rj = beta_r sum_c k_rc k_jc e^{Gamma_rc - Gamma_jc} (j < r),  T = (I + A)^{-1}
-//   W = T Diag(beta) (K e^Gamma),  U~ = T Diag(beta) V,  U = U~ - W S
+//   U = T Diag(beta) (V - (K e^Gamma) S)          (the UT transform applied to the residual)
 //   P_rj = sum_c q_rc k_jc e^{Gamma_rc - Gamma_jc} (j <= r),  O = (Q e^Gamma) S + P U
 //   S' = Diag(e^{Gamma_L}) S + Khat^T U,  Khat_j = k_j e^{Gamma_L - Gamma_j}
+// (U equals U~ - W S with U~ = T Diag(beta) V and W = T Diag(beta) K e^Gamma; forming the
+// residual V - (K e^Gamma) S first needs no W and lets that product start before the solve.)
 //
 // Bounded decay. Over a block of 64 tokens Gamma can fall to -320, so e^{-Gamma} overflows any
 // floating type and A, P cannot be one product (K e^Gamma)(K e^{-Gamma})^T. With
@@ -20,24 +22,24 @@
 // block R take their A and P entries from the Y_R columns. Every factor is formed from one
 // exponential per element, times per-channel factors e^{B_R' - B_R} <= 1.
 //
-// One CTA (256 threads) owns one (sequence, head) problem and walks its blocks in order. In
-// the elementwise phases thread (c, h) owns channel c (= its TMEM lane) and rows / columns
-// 32h .. 32h + 31, so every operand it produces is a contiguous 64-byte run of one row of a
-// [channel][token] tile and is written with 16-byte stores. Per block:
-//   TMA: k, q (double-buffered), g, v tiles, two 64-channel boxes each, 128-byte swizzle
-//   SIMT: Gamma, X and Y operands                       tcgen05: D = X Y^T  (M 128, N 160, K 128)
-//   SIMT: (K e^Gamma)^T, Khat^T, (Q e^Gamma)^T; A and P out of TMEM; T = (I + A)^{-1} by
-//         16 x 16 blocks in fp32; T Diag(beta) in bf16
-//   tcgen05: W^T = (K e^Gamma)^T (T Diag beta)^T,  U~^T = V^T (T Diag beta)^T
-//   SIMT: -W^T to shared memory                        tcgen05: [U^T | O^T] += S^T [-W^T | (Q e^Gamma)^T]
-//   SIMT: U to shared memory                           tcgen05: S += Khat^T U,  O^T += U^T P^T
-//   SIMT: O to global memory (bf16, TMA store); bf16 copy of S to shared memory as the next
-//         block's operand.
-// Transposed forms keep every product at M = 128 (TMEM lane = row). The fp32 state lives in
-// TMEM for the whole sequence: while X Y^T runs it is scaled by e^{Gamma_L} in place, and the
-// Khat^T U product accumulates onto it. Only its bf16 copy feeds the tensor cores, so rounding
-// does not accumulate in S itself. Every wait is bounded; a timeout latches KDA_ERR_TIMEOUT, lets
-// issued copies and products land, frees TMEM and returns.
+// Layout. One CTA (256 threads) owns one (sequence, head) problem and walks its blocks in
+// order. The state is kept transposed in TMEM: S^T in fp32 (lane = value channel v, column =
+// key channel c) and its bf16 copy, which is the A operand of the products with S. Every
+// intermediate of the state update (the residual Z = (K e^Gamma) S, U, the bf16 copies) goes
+// TMEM -> registers -> TMEM, so only operands built from the inputs pass through shared memory
+// (and need a proxy fence). Per block:
+//   TMA: k, q, g, v tiles (two 64-channel boxes each, 128-byte swizzle)
+//   SIMT: Gamma; X, Y, (K e^Gamma)^T, (Q e^Gamma)^T, Khat^T operands ([channel][token] rows)
+//   tcgen05: D = X Y^T (M 128, N 160);  [Z^T | O^T] = S^T [(K e^Gamma)^T | (Q e^Gamma)^T]
+//   SIMT (meanwhile): S^T <- S^T Diag(e^{Gamma_L}) in TMEM
+//   SIMT: A and P out of TMEM; T = (I + A)^{-1} (16 x 16 blocks, fp32 / 3xTF32); T Diag(beta)
+//   tcgen05: U^T = V^T (T Diag beta)^T - Z^T (T Diag beta)^T
+//   tcgen05: O^T += U^T P^T;  S^T += U^T Khat
+//   SIMT: O to global memory (TMA store of full blocks); bf16 copy of S^T for the next block.
+// Transposed forms keep every product at M = 128 (TMEM lane = row). Only the bf16 copy of the
+// state feeds the tensor cores; the fp32 state accumulates in TMEM, so rounding does not
+// accumulate in S itself. Every wait is bounded; a timeout latches KDA_ERR_TIMEOUT, lets issued
+// copies and products land, frees TMEM and returns.
 #pragma once
 
 #include <cuda.h>
@@ -58,35 +60,34 @@ constexpr int THREADS = 256;
 constexpr float LOG2E = 1.4426950408889634f;
 
 // ---- shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t IN_K = 0;          // k tiles, two buffers of 16 KB (block parity)
-constexpr uint32_t IN_Q = 32768;      // q tiles, two buffers of 16 KB
-constexpr uint32_t IN_G = 65536;      // g tile, 16 KB
-constexpr uint32_t IN_V = 81920;      // v tile, 16 KB (MN-major A of U~^T as loaded)
-constexpr uint32_t SS = 98304;        // bf16 S [k][v]: MN-major A of the U/O product, 2 panels
-constexpr uint32_t XY = 131072;       // 80 KB region with two lives per block:
+constexpr uint32_t IN_K = 0;          // k tile (two 64-channel boxes of [64 tokens][64])
+constexpr uint32_t IN_Q = 16384;      // q tile
+constexpr uint32_t IN_G = 32768;      // g tile
+constexpr uint32_t IN_V = 49152;      // v tile (MN-major A of V^T (T Diag beta)^T as loaded)
+constexpr uint32_t XY = 65536;        // 80 KB region with two lives per block:
 constexpr uint32_t XK = XY;           //   X rows 0..63 (k side), MN-major A panel 0
 constexpr uint32_t XQ = XY + 16384;   //   X rows 64..127 (q side), MN-major A panel 1
 constexpr uint32_t YP = XY + 32768;   //   Y, N = 160 columns in 3 MN-major B panels
-constexpr uint32_t KG = XY;           // after D: (K e^Gamma)^T [c][r], K-major A of W^T
-constexpr uint32_t KH = XY + 16384;   //   Khat^T [c][r], K-major A of dS
-constexpr uint32_t PT = XY + 32768;   //   P [r][j], K-major B of O^T += U^T P^T (8 KB)
-constexpr uint32_t WS = XY + 40960;   //   fp32 A then T ([64][WLD], 18 KB); later -W^T, then U
-constexpr uint32_t NW = WS;           //   -W^T [c][r], MN-major B panel 0 of the U/O product
-constexpr uint32_t US = WS;           //   U [v][r], K-major B of dS and A of O^T += U^T P^T
-constexpr uint32_t QG = XY + 59392;   //   (Q e^Gamma)^T [c][r], MN-major B panel 1 of U/O
-constexpr uint32_t TB = XY + 75776;   //   fp32 M_R during the solve, then T Diag(beta) [r][j]
-constexpr uint32_t OS = WS;           // O staging for the TMA store (two [64][64] boxes) once
-                                      // the dS / O products have released U
-constexpr uint32_t SMEM_BYTES = XY + 83968;
+constexpr uint32_t WS = XY;           // after D: fp32 A then T ([64][WLD], 18 KB)
+constexpr uint32_t PT = XY + 18432;   //   P [r][j], K-major B of O^T += U^T P^T (8 KB)
+constexpr uint32_t TB = XY + 26624;   //   fp32 M_R during the solve, then T Diag(beta) [r][j]
+constexpr uint32_t KG = XY + 81920;   // (K e^Gamma)^T [c][r]: MN-major B panel 0 of [Z^T | O^T]
+constexpr uint32_t QG = KG + 16384;   // (Q e^Gamma)^T [c][r]: MN-major B panel 1 of [Z^T | O^T]
+constexpr uint32_t KH = QG + 16384;   // Khat^T [c][r]: K-major B of S^T += U^T Khat
+constexpr uint32_t OS = KH + 16384;   // O staging for the TMA store: two [64 tokens][64] boxes
+constexpr uint32_t SMEM_BYTES = OS + 16384;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for aligning the base
 constexpr uint32_t BOX_BYTES = 8192;                // one 64-channel x 64-token TMA box
 
 // ---- TMEM columns (512 allocated)
-constexpr uint32_t TD = 0;    // X Y^T, 160 columns
-constexpr uint32_t TW = 160;  // W^T, 64
-constexpr uint32_t TU = 224;  // U~^T, then U^T, 64
-constexpr uint32_t TO = 288;  // O^T, 64 (directly after TU: the U/O product writes both)
-constexpr uint32_t TS = 352;  // fp32 state S [k][v], 128 (the S += Khat^T U product accumulates here)
+constexpr uint32_t T_ST = 0;    // S^T fp32 [v][c], 128
+constexpr uint32_t T_SB = 128;  // S^T bf16 (A operand), 64
+constexpr uint32_t T_D = 192;   // X Y^T, 160; once read: U^T fp32 (64) and U^T bf16 (32)
+constexpr uint32_t T_UT = 192;
+constexpr uint32_t T_UB = 256;
+constexpr uint32_t T_ZT = 352;  // Z^T fp32, 64
+constexpr uint32_t T_OT = 416;  // O^T fp32, 64 (directly after Z^T: one product writes both)
+constexpr uint32_t T_ZB = 480;  // Z^T bf16 (A operand), 32
 
 // First column of Y_R inside the N = 160 stack.
 __host__ __device__ constexpr int y_ofs(int R) { return 8 * R * (R + 1); }  // 0, 16, 48, 96
@@ -107,18 +108,30 @@ __device__ __forceinline__ float ld_bf16(const uint8_t* base, uint32_t off) {
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + off));
 }
 
+// Row of local index i (0..31) of thread half hh: half 0 holds blocks 0 and 3, half 1 holds
+// blocks 1 and 2, which balances the Y work (block R feeds 4 - R sub-stacks of Y).
+__device__ __forceinline__ int prep_row(int hh, int i) {
+  return hh == 0 ? (i < 16 ? i : 32 + i) : 16 + i;
+}
+
+__device__ __forceinline__ void st_pack8(uint32_t saddr, const float (&x)[8]) {
+  st_shared_v4(saddr, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+               pack_bf16(x[6], x[7]));
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
     chunk_tc_kernel(const __grid_constant__ TmaMaps maps, SeqParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(sm);
-  __shared__ uint64_t bar_kq[2], bar_g, bar_v, bar_mma;
+  __shared__ uint64_t bar_in, bar_v, bar_mma;
   __shared__ uint32_t tmem_base_s;
   __shared__ __align__(16) float beta_s[C];
-  __shared__ float xch[D];
+  __shared__ float xch[2][D];
   __shared__ float bnd[5][D];  // log2-domain Gamma at the block boundaries: B_0..B_3, B_4 = Gamma_L
-  __shared__ float trr[4][16][17];  // diagonal blocks T_RR of the solve
+  __shared__ __align__(16) float gl_s[D];  // e^{Gamma_L} per key channel
+  __shared__ float trr[4][16][17];         // diagonal blocks T_RR of the solve
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -133,13 +146,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (!resolve_problem(P, p, h, row0, len)) return;
   const int H = P.H;
   const int nblocks = (len + C - 1) / C;
-  const __nv_bfloat16* __restrict__ beta_g = static_cast<const __nv_bfloat16*>(P.beta);
   __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(P.out);
 
   if (tid == 0) {
-    mbar_init(&bar_kq[0], 1);
-    mbar_init(&bar_kq[1], 1);
-    mbar_init(&bar_g, 1);
+    mbar_init(&bar_in, 1);
     mbar_init(&bar_v, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
@@ -147,6 +157,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     prefetch_tensormap(&maps.k);
     prefetch_tensormap(&maps.v);
     prefetch_tensormap(&maps.g);
+    prefetch_tensormap(&maps.o);
   }
   if (warp == 0) tmem_alloc(&tmem_base_s, 512);
   tc_fence_before();
@@ -160,71 +171,51 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_load_3d(sm + dst, m, 0, h, row, bar);
     tma_load_3d(sm + dst + BOX_BYTES, m, 64, h, row, bar);
   };
-  auto issue_kq = [&](int b) {
-    const int buf = b & 1;
-    mbar_arrive_expect_tx(&bar_kq[buf], 4 * BOX_BYTES);
-    load2(IN_K + 16384u * buf, &maps.k, (int)(row0 + (size_t)b * C), &bar_kq[buf]);
-    load2(IN_Q + 16384u * buf, &maps.q, (int)(row0 + (size_t)b * C), &bar_kq[buf]);
-  };
-  auto issue_g = [&](int b) {
-    mbar_arrive_expect_tx(&bar_g, 2 * BOX_BYTES);
-    load2(IN_G, &maps.g, (int)(row0 + (size_t)b * C), &bar_g);
+  auto issue_in = [&](int b) {
+    const int row = (int)(row0 + (size_t)b * C);
+    mbar_arrive_expect_tx(&bar_in, 6 * BOX_BYTES);
+    load2(IN_K, &maps.k, row, &bar_in);
+    load2(IN_Q, &maps.q, row, &bar_in);
+    load2(IN_G, &maps.g, row, &bar_in);
   };
   auto issue_v = [&](int b) {
     mbar_arrive_expect_tx(&bar_v, 2 * BOX_BYTES);
     load2(IN_V, &maps.v, (int)(row0 + (size_t)b * C), &bar_v);
   };
 
-  // ---- initial state: fp32 in registers (row c, columns 64 hh ..), bf16 copy in SS
+  // ---- initial state S^T: lane v = c, key channels 64 hh .. 64 hh + 63 (coalesced over v)
   {
-    const float* s0 = P.S0 ? P.S0 + ((size_t)p * D + c) * D + 64 * hh : nullptr;
+    const float* s0 = P.S0 ? P.S0 + (size_t)p * D * D + c : nullptr;
+    uint32_t sbf[32];
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       uint32_t sv[32];
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        const float4 x = s0 ? *reinterpret_cast<const float4*>(s0 + 32 * half + j)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-        sv[j] = __float_as_uint(x.x); sv[j + 1] = __float_as_uint(x.y);
-        sv[j + 2] = __float_as_uint(x.z); sv[j + 3] = __float_as_uint(x.w);
-      }
-      tmem_st32(tl + TS + 64 * hh + 32 * half, sv);
+      for (int j = 0; j < 32; ++j)
+        sv[j] = s0 ? __float_as_uint(s0[(size_t)(64 * hh + 32 * half + j) * D]) : 0u;
+      tmem_st32(tl + T_ST + 64 * hh + 32 * half, sv);
 #pragma unroll
-      for (int k8 = 0; k8 < 4; ++k8)
-        st_shared_v4(sb + SS + 16384u * hh + sw128_off(c, 32 * half + 8 * k8),
-                     pack_bf16(__uint_as_float(sv[8 * k8]), __uint_as_float(sv[8 * k8 + 1])),
-                     pack_bf16(__uint_as_float(sv[8 * k8 + 2]), __uint_as_float(sv[8 * k8 + 3])),
-                     pack_bf16(__uint_as_float(sv[8 * k8 + 4]), __uint_as_float(sv[8 * k8 + 5])),
-                     pack_bf16(__uint_as_float(sv[8 * k8 + 6]), __uint_as_float(sv[8 * k8 + 7])));
+      for (int j = 0; j < 16; ++j)
+        sbf[16 * half + j] = pack_bf16(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]));
     }
-    uint32_t z[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) z[j] = 0u;
-    tmem_st32(tl + TO + 32 * hh, z);  // O^T starts each block at zero
+    tmem_st32(tl + T_SB + 32 * hh, sbf);
     tmem_st_wait();
   }
-  // Phase parities and pending flags; bit b of the k/q words belongs to buffer b.
-  uint32_t ph_kq = 0u, ph_g = 0u, ph_v = 0u, ph_mma = 0u;
-  uint32_t pend_kq = 0u;
-  bool pend_g = false, pend_v = false, pend_mma = false;
+  uint32_t ph_in = 0u, ph_v = 0u, ph_mma = 0u;
+  bool pend_in = false, pend_v = false, pend_mma = false;
   if (tid == 0 && nblocks > 0) {
-    issue_kq(0);
-    issue_g(0);
+    issue_in(0);
     issue_v(0);
   }
-  if (nblocks > 0) {
-    pend_kq = 1u;
-    pend_g = pend_v = true;
-  }
+  if (nblocks > 0) pend_in = pend_v = true;
+  // beta of the next block is loaded one block ahead (a strided global read), kept as raw bits
+  // so that nothing waits on the load until the block that needs it
+  const unsigned short* __restrict__ beta_u = static_cast<const unsigned short*>(P.beta);
+  unsigned short beta_next = 0;
+  if (tid < C && tid < len) beta_next = beta_u[(row0 + tid) * H + h];
   tc_fence_before();
-  fence_proxy_async_smem();
   __syncthreads();
 
-  // beta of the next block is loaded one block ahead (a strided global read)
-  // (kept as raw bits so that nothing waits on the load until the block that needs it)
-  unsigned short beta_next = 0;
-  const unsigned short* __restrict__ beta_u = reinterpret_cast<const unsigned short*>(beta_g);
-  if (tid < C && tid < len) beta_next = beta_u[(row0 + tid) * H + h];
   bool aborted = false;
   auto mma_done = [&]() -> bool {
     const bool ok = mbar_wait(&bar_mma, ph_mma);
@@ -237,176 +228,170 @@ __global__ void __launch_bounds__(THREADS, 1)
   for (int blk = 0; blk < nblocks; ++blk) {
     const int t0 = blk * C;
     const int n = min(C, len - t0);
-    const int buf = blk & 1;
-    if (blk + 1 < nblocks) {  // the other k/q buffer was last read by block blk - 1
-      if (tid == 0) {
-        fence_proxy_async_smem();
-        issue_kq(blk + 1);
-      }
-      pend_kq |= 1u << (buf ^ 1);
-    }
     if (tid < C) {
       beta_s[tid] = __uint_as_float((uint32_t)beta_next << 16);  // zero past the end
       beta_next = 0;
       if (tid < len - t0 - C) beta_next = beta_u[(row0 + t0 + C + tid) * H + h];
     }
     {
-      const bool ok = mbar_wait(&bar_g, ph_g);
-      if (ok) ph_g ^= 1u;
-      pend_g = !ok;
-      const bool ok2 = mbar_wait(&bar_kq[buf], (ph_kq >> buf) & 1u);
-      if (ok2) {
-        ph_kq ^= 1u << buf;
-        pend_kq &= ~(1u << buf);
-      }
-      if (__syncthreads_or(!(ok && ok2))) { aborted = true; break; }
+      const bool ok = mbar_wait(&bar_in, ph_in);
+      if (ok) ph_in ^= 1u;
+      pend_in = !ok;
+      if (__syncthreads_or(!ok)) { aborted = true; break; }
     }
-    // ---------------- Gamma (log2 domain), thread (c, hh) rows 32 hh .. 32 hh + 31
+    // ---------------- Gamma (log2 domain): local cumulative sums, then the block offsets
     float Gm[32];
     {
       const uint8_t* gp = sm + IN_G + (c >> 6) * BOX_BYTES;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) Gm[i] = ld_bf16(gp, sw128_off(32 * hh + i, c & 63));
+      for (int i = 0; i < 32; ++i) Gm[i] = ld_bf16(gp, sw128_off(prep_row(hh, i), c & 63));
       float acc = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        acc = fmaf(32 * hh + i < n ? Gm[i] : 0.f, LOG2E, acc);
+        if (hh == 0 && i == 16) acc = 0.f;  // rows 48..63 restart; Gamma_47 is added below
+        acc = fmaf(prep_row(hh, i) < n ? Gm[i] : 0.f, LOG2E, acc);
         Gm[i] = acc;
       }
-      if (hh == 0) xch[c] = acc;
+      xch[hh][c] = hh == 0 ? Gm[15] : Gm[31];  // Gamma_15, and Gamma_47 - Gamma_15
     }
     __syncthreads();
-    if (hh == 1) {
-      const float base = xch[c];
+    if (hh == 0) {
+      const float b3 = Gm[15] + xch[1][c];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) Gm[i] += base;
-      bnd[3][c] = Gm[15];
-      bnd[4][c] = Gm[31];
-    } else {
+      for (int i = 16; i < 32; ++i) Gm[i] += b3;
       bnd[0][c] = 0.f;
       bnd[1][c] = Gm[15];
-      bnd[2][c] = Gm[31];
+      bnd[3][c] = b3;
+      bnd[4][c] = Gm[31];
+      gl_s[c] = ex2(Gm[31]);
+    } else {
+      const float b1 = xch[0][c];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) Gm[i] += b1;
+      bnd[2][c] = Gm[15];
     }
-    if (tid == 0) bulk_wait_read();  // the previous block's O store has left the staging tiles
-    __syncthreads();  // the g tile is dead
-    if (blk + 1 < nblocks) {
-      if (tid == 0) {
-        fence_proxy_async_smem();
-        issue_g(blk + 1);
-      }
-      pend_g = true;
-    }
-    // ---------------- X and Y operands; (K e^Gamma)^T, (Q e^Gamma)^T and Khat^T are kept
-    // packed in registers and written once the X Y^T product has released the region
-    uint32_t kgp[16], qgp[16], khp[16];
+    __syncthreads();
+    // ---------------- operands: X, Y, (K e^Gamma)^T, (Q e^Gamma)^T, Khat^T
     {
-      const uint8_t* kp = sm + IN_K + 16384u * buf + (c >> 6) * BOX_BYTES;
-      const uint8_t* qp = sm + IN_Q + 16384u * buf + (c >> 6) * BOX_BYTES;
-      float bR[2], eB[2], eL[2], eRR[2][4];
+      const uint8_t* kp = sm + IN_K + (c >> 6) * BOX_BYTES;
+      const uint8_t* qp = sm + IN_Q + (c >> 6) * BOX_BYTES;
+      float bv[5];
+#pragma unroll
+      for (int R = 0; R < 5; ++R) bv[R] = bnd[R][c];
 #pragma unroll
       for (int a = 0; a < 2; ++a) {
-        const int R = 2 * hh + a;
-        bR[a] = bnd[R][c];
-        eB[a] = ex2(bR[a]);               // e^{B_R}
-        eL[a] = ex2(bnd[4][c] - bR[a]);   // e^{Gamma_L - B_R}
+        const int R = hh == 0 ? 3 * a : 1 + a;  // this thread's block for rows 16a .. 16a + 15
+        const float bR = hh == 0 ? (a == 0 ? bv[0] : bv[3]) : (a == 0 ? bv[1] : bv[2]);
+        const float eB = ex2(bR);           // e^{B_R}
+        const float eL = ex2(bv[4] - bR);   // e^{Gamma_L - B_R}
+        float eRR[4];
 #pragma unroll
-        for (int Rp = 0; Rp < 4; ++Rp) eRR[a][Rp] = Rp > R ? ex2(bnd[Rp][c] - bR[a]) : 1.f;
-      }
-      float kv[16], qv[16];
+        for (int Rp = 0; Rp < 4; ++Rp) eRR[Rp] = Rp > R ? ex2(bv[Rp] - bR) : 1.f;
+        float kv[16], qv[16];
 #pragma unroll
-      for (int gi = 0; gi < 4; ++gi) {
-        const int a = gi >> 1;
-        const int R = 2 * hh + a;
-        if ((gi & 1) == 0) {  // the next 16 rows of k and q, loaded before any use
+        for (int e = 0; e < 16; ++e) {
+          const uint32_t o = sw128_off(16 * R + e, c & 63);
+          kv[e] = ld_bf16(kp, o);
+          qv[e] = ld_bf16(qp, o);
+        }
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const uint32_t o = sw128_off(32 * hh + 8 * gi + e, c & 63);
-            kv[e] = ld_bf16(kp, o);
-            qv[e] = ld_bf16(qp, o);
+        for (int e = 0; e < 16; ++e) {
+          const bool live = 16 * R + e < n;
+          kv[e] = live ? kv[e] : 0.f;
+          qv[e] = live ? qv[e] : 0.f;
+        }
+#pragma unroll
+        for (int gi = 0; gi < 2; ++gi) {
+          float xk[8], xq[8], y[8], kg[8], qg[8], kh[8];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const int i = 16 * a + 8 * gi + e;
+            const float L0 = Gm[i] - bR, L1 = Gm[i + 1] - bR;
+            const float2 F = make_float2(ex2(L0), ex2(L1));
+            const float2 Fi = make_float2(ex2(-L0), ex2(-L1));
+            const float2 k2 = make_float2(kv[8 * gi + e], kv[8 * gi + e + 1]);
+            const float2 q2 = make_float2(qv[8 * gi + e], qv[8 * gi + e + 1]);
+            const float2 xk2 = mul2(k2, F), xq2 = mul2(q2, F), y2 = mul2(k2, Fi);
+            const float2 kg2 = mul2(xk2, make_float2(eB, eB));
+            const float2 qg2 = mul2(xq2, make_float2(eB, eB));
+            const float2 kh2 = mul2(y2, make_float2(eL, eL));
+            xk[e] = xk2.x; xk[e + 1] = xk2.y;
+            xq[e] = xq2.x; xq[e + 1] = xq2.y;
+            y[e] = y2.x; y[e + 1] = y2.y;
+            kg[e] = kg2.x; kg[e + 1] = kg2.y;
+            qg[e] = qg2.x; qg[e + 1] = qg2.y;
+            kh[e] = kh2.x; kh[e + 1] = kh2.y;
           }
+          const uint32_t r0 = 16 * R + 8 * gi;  // first token of these 8 rows
+          const uint32_t o = sw128_off(c, r0);
+          st_pack8(sb + XK + o, xk);
+          st_pack8(sb + XQ + o, xq);
+          st_pack8(sb + KG + o, kg);
+          st_pack8(sb + QG + o, qg);
+          st_pack8(sb + KH + o, kh);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const bool live = 32 * hh + 8 * gi + e < n;
-            kv[e] = live ? kv[e] : 0.f;
-            qv[e] = live ? qv[e] : 0.f;
+          for (int Rp = 0; Rp < 4; ++Rp) {
+            if (Rp < R) continue;
+            const float f = eRR[Rp];
+            const int nidx = y_ofs(Rp) + (int)r0;
+            float yf[8];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const float2 v2 = mul2(make_float2(y[e], y[e + 1]), make_float2(f, f));
+              yf[e] = v2.x; yf[e + 1] = v2.y;
+            }
+            st_pack8(sb + YP + 16384u * (uint32_t)(nidx >> 6) + sw128_off(c, nidx & 63), yf);
           }
-        }
-        float xk[8], xq[8], y[8], kg[8], qg[8], kh[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int i = 8 * gi + e;
-          const float kk = kv[8 * (gi & 1) + e];
-          const float qq = qv[8 * (gi & 1) + e];
-          const float L = Gm[i] - bR[a];
-          const float F = ex2(L), Fi = ex2(-L);
-          xk[e] = kk * F;
-          xq[e] = qq * F;
-          y[e] = kk * Fi;
-          kg[e] = xk[e] * eB[a];
-          qg[e] = xq[e] * eB[a];
-          kh[e] = y[e] * eL[a];
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          kgp[4 * gi + e] = pack_bf16(kg[2 * e], kg[2 * e + 1]);
-          qgp[4 * gi + e] = pack_bf16(qg[2 * e], qg[2 * e + 1]);
-          khp[4 * gi + e] = pack_bf16(kh[2 * e], kh[2 * e + 1]);
-        }
-        const uint32_t col = 32 * hh + 8 * gi;
-        st_shared_v4(sb + XK + sw128_off(c, col), pack_bf16(xk[0], xk[1]), pack_bf16(xk[2], xk[3]),
-                     pack_bf16(xk[4], xk[5]), pack_bf16(xk[6], xk[7]));
-        st_shared_v4(sb + XQ + sw128_off(c, col), pack_bf16(xq[0], xq[1]), pack_bf16(xq[2], xq[3]),
-                     pack_bf16(xq[4], xq[5]), pack_bf16(xq[6], xq[7]));
-#pragma unroll
-        for (int Rp = 0; Rp < 4; ++Rp) {
-          if (Rp < R) continue;
-          const float f = eRR[a][Rp];
-          const int nidx = y_ofs(Rp) + 16 * R + 8 * (gi & 1);
-          st_shared_v4(sb + YP + 16384u * (uint32_t)(nidx >> 6) + sw128_off(c, nidx & 63),
-                       pack_bf16(y[0] * f, y[1] * f), pack_bf16(y[2] * f, y[3] * f),
-                       pack_bf16(y[4] * f, y[5] * f), pack_bf16(y[6] * f, y[7] * f));
         }
       }
     }
     fence_proxy_async_smem();
     __syncthreads();
-    // ---------------- tcgen05: D = X Y^T (M 128, N 160, K 128)
+    if (blk + 1 < nblocks) {  // the k, q and g tiles are dead
+      if (tid == 0) issue_in(blk + 1);
+      pend_in = true;
+    }
+    // ---------------- tcgen05: D = X Y^T ; [Z^T | O^T] = S^T [(K e^Gamma)^T | (Q e^Gamma)^T]
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, 160, 1, 1, 0);
+      const uint32_t id_d = idesc_bf16(128, 160, 1, 1, 0);
+      const uint32_t id_z = idesc_bf16(128, 128, 0, 1, 0);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        umma_bf16(tmem + TD, desc_sw128(sb + XK + 2048u * kk, 16384, 1024),
-                  desc_sw128(sb + YP + 2048u * kk, 16384, 1024), idesc, kk > 0);
+      for (int kk = 0; kk < 8; ++kk) {
+        umma_bf16(tmem + T_D, desc_sw128(sb + XK + 2048u * kk, 16384, 1024),
+                  desc_sw128(sb + YP + 2048u * kk, 16384, 1024), id_d, kk > 0);
+        umma_bf16_tmem_a(tmem + T_ZT, tmem + T_SB + 8u * kk,
+                         desc_sw128(sb + KG + 2048u * kk, QG - KG, 1024), id_z, kk > 0);
+      }
       umma_commit(&bar_mma);
     }
     pend_mma = true;
-    // ---------------- while X Y^T runs: S <- e^{Gamma_L} S in TMEM (dS accumulates onto it)
+    // ---------------- meanwhile: S^T <- S^T Diag(e^{Gamma_L}) (the products above read the
+    // bf16 copy; Khat^T U accumulates onto this one)
     {
-      const float gl = ex2(bnd[4][c]);
       uint32_t v[32];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        tmem_ld32(tl + TS + 64 * hh + 32 * half, v);
+        const int c0 = 64 * hh + 32 * half;
+        tmem_ld32(tl + T_ST + c0, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(gl * __uint_as_float(v[j]));
-        tmem_st32(tl + TS + 64 * hh + 32 * half, v);
+        for (int j = 0; j < 32; j += 4) {
+          const float4 gv = *reinterpret_cast<const float4*>(gl_s + c0 + j);
+          const float2 a0 = mul2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])),
+                                 make_float2(gv.x, gv.y));
+          const float2 a1 = mul2(make_float2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])),
+                                 make_float2(gv.z, gv.w));
+          v[j] = __float_as_uint(a0.x); v[j + 1] = __float_as_uint(a0.y);
+          v[j + 2] = __float_as_uint(a1.x); v[j + 3] = __float_as_uint(a1.y);
+        }
+        tmem_st32(tl + T_ST + c0, v);
       }
       tmem_st_wait();
       tc_fence_before();
     }
     if (__syncthreads_or(!mma_done())) { aborted = true; break; }
-
-    // ---------------- the X/Y region is free: (K e^Gamma)^T, Khat^T, (Q e^Gamma)^T
-#pragma unroll
-    for (int gi = 0; gi < 4; ++gi) {
-      const uint32_t o = sw128_off(c, 32 * hh + 8 * gi);
-      st_shared_v4(sb + KG + o, kgp[4 * gi], kgp[4 * gi + 1], kgp[4 * gi + 2], kgp[4 * gi + 3]);
-      st_shared_v4(sb + KH + o, khp[4 * gi], khp[4 * gi + 1], khp[4 * gi + 2], khp[4 * gi + 3]);
-      st_shared_v4(sb + QG + o, qgp[4 * gi], qgp[4 * gi + 1], qgp[4 * gi + 2], qgp[4 * gi + 3]);
-    }
-    // ---------------- A (fp32, into WS) and P (bf16, into PT) out of TMEM
+    // ---------------- A (fp32, into WS) and P (bf16, into PT) out of TMEM; Z^T -> bf16
     // Lane m: rows 0..63 are the k side (A), 64..127 the q side (P); row r = m & 63 belongs to
     // block R = r >> 4 and reads the Y_R columns. This thread covers columns j in [32 hh, +32).
     {
@@ -422,7 +407,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int a = 0; a < 2; ++a) {
         const int Rx = R0 + a;
         const int ncols = min(32, 16 * (Rx + 1) - 32 * hh);  // warp-uniform
-        const uint32_t col = tl + TD + (uint32_t)(y_ofs(Rx) + 32 * hh);
+        const uint32_t col = tl + T_D + (uint32_t)(y_ofs(Rx) + 32 * hh);
         if (ncols >= 32) {
           uint32_t v[32];
           tmem_ld32(col, v);
@@ -462,12 +447,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int j = 32 * hh + 8 * j8 + e;
             x[e] = (j <= r) ? vals[8 * j8 + e] : 0.f;
           }
-          st_shared_v4(sb + PT + sw128_off(r, 32 * hh + 8 * j8), pack_bf16(x[0], x[1]),
-                       pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+          st_pack8(sb + PT + sw128_off(r, 32 * hh + 8 * j8), x);
         }
       }
+      // Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand
+      uint32_t v[32], zb[16];
+      tmem_ld32(tl + T_ZT + 32 * hh, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) zb[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+      tmem_st16(tl + T_ZB + 16 * hh, zb);
     }
-    tc_fence_before();
     __syncthreads();
     // ---------------- T = (I + A)^{-1} (unit lower triangular), in place in WS
     {
@@ -570,97 +560,66 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     fence_proxy_async_smem();
+    tmem_st_wait();
+    tc_fence_before();
     {
       const bool ok = mbar_wait(&bar_v, ph_v);
       if (ok) ph_v ^= 1u;
       pend_v = !ok;
       if (__syncthreads_or(!ok)) { aborted = true; break; }
     }
-    // ---------------- tcgen05: W^T = (K e^Gamma)^T (T Diag beta)^T ; U~^T = V^T (T Diag beta)^T
+    // ---------------- tcgen05: U^T = V^T (T Diag beta)^T - Z^T (T Diag beta)^T  (M 128, N 64, K 64)
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t id_w = idesc_bf16(128, 64, 0, 0, 0);
-      const uint32_t id_u = idesc_bf16(128, 64, 1, 0, 0);
+      const uint32_t id_v = idesc_bf16(128, 64, 1, 0, 0);
+      const uint32_t id_z = idesc_bf16(128, 64, 0, 0, 1);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t b = desc_sw128(sb + TB + 32u * kk, 16, 1024);
-        umma_bf16(tmem + TW, desc_sw128(sb + KG + 32u * kk, 16, 1024), b, id_w, kk > 0);
-        umma_bf16(tmem + TU, desc_sw128(sb + IN_V + 2048u * kk, BOX_BYTES, 1024), b, id_u, kk > 0);
+        umma_bf16(tmem + T_UT, desc_sw128(sb + IN_V + 2048u * kk, BOX_BYTES, 1024), b, id_v, kk > 0);
+        umma_bf16_tmem_a(tmem + T_UT, tmem + T_ZB + 8u * kk, b, id_z, 1);
       }
       umma_commit(&bar_mma);
     }
     pend_mma = true;
+    if (tid == 0) bulk_wait_read();  // the previous block's O store has left the staging tiles
     if (__syncthreads_or(!mma_done())) { aborted = true; break; }
     if (blk + 1 < nblocks) {  // the v tile is dead
-      if (tid == 0) {
-        fence_proxy_async_smem();
-        issue_v(blk + 1);
-      }
+      if (tid == 0) issue_v(blk + 1);
       pend_v = true;
     }
-    // ---------------- -W^T -> bf16, MN-major [c][r]
+    // ---------------- U^T -> bf16 A operand
     {
-      uint32_t v[32];
-      tmem_ld32(tl + TW + 32 * hh, v);
+      uint32_t v[32], ub[16];
+      tmem_ld32(tl + T_UT + 32 * hh, v);
       tmem_ld_wait();
 #pragma unroll
-      for (int k8 = 0; k8 < 4; ++k8)
-        st_shared_v4(sb + NW + sw128_off(c, 32 * hh + 8 * k8),
-                     pack_bf16(-__uint_as_float(v[8 * k8]), -__uint_as_float(v[8 * k8 + 1])),
-                     pack_bf16(-__uint_as_float(v[8 * k8 + 2]), -__uint_as_float(v[8 * k8 + 3])),
-                     pack_bf16(-__uint_as_float(v[8 * k8 + 4]), -__uint_as_float(v[8 * k8 + 5])),
-                     pack_bf16(-__uint_as_float(v[8 * k8 + 6]), -__uint_as_float(v[8 * k8 + 7])));
+      for (int j = 0; j < 16; ++j) ub[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+      tmem_st16(tl + T_UB + 16 * hh, ub);
+      tmem_st_wait();
     }
     tc_fence_before();
-    fence_proxy_async_smem();
     __syncthreads();
-    // ---------------- tcgen05: [U^T | O^T] += S^T [-W^T | (Q e^Gamma)^T]  (M 128, N 128, K 128)
+    // ---------------- tcgen05: O^T += U^T P^T (N 64) ; S^T += U^T Khat (N 128), K 64
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, 128, 1, 1, 0);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        umma_bf16(tmem + TU, desc_sw128(sb + SS + 2048u * kk, 16384, 1024),
-                  desc_sw128(sb + NW + 2048u * kk, QG - NW, 1024), idesc, 1);
-      umma_commit(&bar_mma);
-    }
-    pend_mma = true;
-    if (__syncthreads_or(!mma_done())) { aborted = true; break; }
-    // ---------------- U -> bf16, K-major [v][r]
-    {
-      uint32_t v[32];
-      tmem_ld32(tl + TU + 32 * hh, v);
-      tmem_ld_wait();
-#pragma unroll
-      for (int k8 = 0; k8 < 4; ++k8)
-        st_shared_v4(sb + US + sw128_off(c, 32 * hh + 8 * k8),
-                     pack_bf16(__uint_as_float(v[8 * k8]), __uint_as_float(v[8 * k8 + 1])),
-                     pack_bf16(__uint_as_float(v[8 * k8 + 2]), __uint_as_float(v[8 * k8 + 3])),
-                     pack_bf16(__uint_as_float(v[8 * k8 + 4]), __uint_as_float(v[8 * k8 + 5])),
-                     pack_bf16(__uint_as_float(v[8 * k8 + 6]), __uint_as_float(v[8 * k8 + 7])));
-    }
-    tc_fence_before();
-    fence_proxy_async_smem();
-    __syncthreads();
-    // ---------------- tcgen05: S += Khat^T U (M 128, N 128, K 64); O^T += U^T P^T (M 128, N 64, K 64)
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t id_s = idesc_bf16(128, 128, 0, 0, 0);
       const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
+      const uint32_t id_s = idesc_bf16(128, 128, 0, 0, 0);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t u = desc_sw128(sb + US + 32u * kk, 16, 1024);
-        umma_bf16(tmem + TS, desc_sw128(sb + KH + 32u * kk, 16, 1024), u, id_s, 1);
-        umma_bf16(tmem + TO, u, desc_sw128(sb + PT + 32u * kk, 16, 1024), id_o, 1);
+        umma_bf16_tmem_a(tmem + T_OT, tmem + T_UB + 8u * kk, desc_sw128(sb + PT + 32u * kk, 16, 1024),
+                         id_o, 1);
+        umma_bf16_tmem_a(tmem + T_ST, tmem + T_UB + 8u * kk, desc_sw128(sb + KH + 32u * kk, 16, 1024),
+                         id_s, 1);
       }
       umma_commit(&bar_mma);
     }
     pend_mma = true;
     if (__syncthreads_or(!mma_done())) { aborted = true; break; }
-    // ---------------- outputs, then the state update
+    // ---------------- outputs; bf16 copy of the new state for the next block
     {
       uint32_t v[32];
-      tmem_ld32(tl + TO + 32 * hh, v);
+      tmem_ld32(tl + T_OT + 32 * hh, v);
       tmem_ld_wait();
       if (n == C) {  // full block: stage [token][channel] boxes for one TMA store
         uint8_t* ob = sm + OS + (c >> 6) * BOX_BYTES;
@@ -676,25 +635,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (r < n) op[(size_t)r * H * D] = __float2bfloat16_rn(__uint_as_float(v[j]));
         }
       }
+      uint32_t sbf[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = 0u;
-      tmem_st32(tl + TO + 32 * hh, v);  // O^T restarts from zero in the next block
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {  // bf16 copy of the new state for the next block
-        tmem_ld32(tl + TS + 64 * hh + 32 * half, v);
+      for (int half = 0; half < 2; ++half) {
+        tmem_ld32(tl + T_ST + 64 * hh + 32 * half, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int k8 = 0; k8 < 4; ++k8)
-          st_shared_v4(sb + SS + 16384u * hh + sw128_off(c, 32 * half + 8 * k8),
-                       pack_bf16(__uint_as_float(v[8 * k8]), __uint_as_float(v[8 * k8 + 1])),
-                       pack_bf16(__uint_as_float(v[8 * k8 + 2]), __uint_as_float(v[8 * k8 + 3])),
-                       pack_bf16(__uint_as_float(v[8 * k8 + 4]), __uint_as_float(v[8 * k8 + 5])),
-                       pack_bf16(__uint_as_float(v[8 * k8 + 6]), __uint_as_float(v[8 * k8 + 7])));
+        for (int j = 0; j < 16; ++j)
+          sbf[16 * half + j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
       }
+      tmem_st32(tl + T_SB + 32 * hh, sbf);
       tmem_st_wait();
     }
-    tc_fence_before();
     fence_proxy_async_smem();
+    tc_fence_before();
     __syncthreads();
     if (n == C && tid == 0) {
       tma_store_3d(&maps.o, sm + OS, 0, h, (int)(row0 + t0));
@@ -708,23 +662,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     record_status(4u /* KDA_ERR_TIMEOUT */);
     if (tid == 0) {  // let anything already issued land before the CTA's memory goes away
       if (pend_mma) (void)mbar_wait(&bar_mma, ph_mma);
-      if (pend_kq & 1u) (void)mbar_wait(&bar_kq[0], ph_kq & 1u);
-      if (pend_kq & 2u) (void)mbar_wait(&bar_kq[1], (ph_kq >> 1) & 1u);
-      if (pend_g) (void)mbar_wait(&bar_g, ph_g);
+      if (pend_in) (void)mbar_wait(&bar_in, ph_in);
       if (pend_v) (void)mbar_wait(&bar_v, ph_v);
     }
-  } else if (P.S_final) {
-    float* sf = P.S_final + ((size_t)p * D + c) * D + 64 * hh;
+  } else if (P.S_final) {  // S_final[c'][v] from S^T (lane v): coalesced over v
+    float* sf = P.S_final + (size_t)p * D * D + c;
     uint32_t v[32];
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      tmem_ld32(tl + TS + 64 * hh + 32 * half, v);
+      tmem_ld32(tl + T_ST + 64 * hh + 32 * half, v);
       tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(sf + 32 * half + j) =
-            make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
-                        __uint_as_float(v[j + 3]));
+      for (int j = 0; j < 32; ++j) sf[(size_t)(64 * hh + 32 * half + j) * D] = __uint_as_float(v[j]);
     }
   }
   tc_fence_before();
