@@ -22,8 +22,10 @@
 // block R take their A and P entries from the Y_R columns. Every factor is formed from one
 // exponential per element, times per-channel factors e^{B_R' - B_R} <= 1.
 //
-// Layout. One CTA (256 threads) owns one (sequence, head) problem and walks its blocks in
-// order. The state is kept transposed in TMEM: S^T in fp32 (lane = value channel v, column =
+// Layout. One CTA (512 threads) owns one (sequence, head) problem and walks its blocks in
+// order. In the elementwise phases thread (c, q) owns channel / TMEM lane c and the q-th
+// 16-token quarter of the block (the q-th sub-block R = q), so every operand it produces is a
+// contiguous 32-byte run of one row of a [channel][token] tile. The state is kept transposed in TMEM: S^T in fp32 (lane = value channel v, column =
 // key channel c) and its bf16 copy, which is the A operand of the products with S. Every
 // intermediate of the state update (the residual Z = (K e^Gamma) S, U, the bf16 copies) goes
 // TMEM -> registers -> TMEM, so only operands built from the inputs pass through shared memory
@@ -56,7 +58,7 @@ namespace tc {
 
 constexpr int C = 64;
 constexpr int D = 128;
-constexpr int THREADS = 256;
+constexpr int THREADS = 512;
 constexpr float LOG2E = 1.4426950408889634f;
 
 // ---- shared memory map (bytes from a 1024-aligned base)
@@ -108,12 +110,6 @@ __device__ __forceinline__ float ld_bf16(const uint8_t* base, uint32_t off) {
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + off));
 }
 
-// Row of local index i (0..31) of thread half hh: half 0 holds blocks 0 and 3, half 1 holds
-// blocks 1 and 2, which balances the Y work (block R feeds 4 - R sub-stacks of Y).
-__device__ __forceinline__ int prep_row(int hh, int i) {
-  return hh == 0 ? (i < 16 ? i : 32 + i) : 16 + i;
-}
-
 __device__ __forceinline__ void st_pack8(uint32_t saddr, const float (&x)[8]) {
   st_shared_v4(saddr, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
                pack_bf16(x[6], x[7]));
@@ -128,7 +124,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __shared__ uint64_t bar_in, bar_v, bar_mma;
   __shared__ uint32_t tmem_base_s;
   __shared__ __align__(16) float beta_s[C];
-  __shared__ float xch[2][D];
+  __shared__ float xch[4][D];
   __shared__ float bnd[5][D];  // log2-domain Gamma at the block boundaries: B_0..B_3, B_4 = Gamma_L
   __shared__ __align__(16) float gl_s[D];  // e^{Gamma_L} per key channel
   __shared__ float trr[4][16][17];         // diagonal blocks T_RR of the solve
@@ -137,7 +133,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = tid >> 5;
   const int quarter = warp & 3;  // TMEM lane quarter this warp may address
   const int c = tid & (D - 1);   // channel (= TMEM lane) owned in the elementwise phases
-  const int hh = tid >> 7;       // which half of the rows / columns this thread handles
+  const int qq = tid >> 7;       // which 16-token quarter (and 32-column quarter) it handles
   const int g = (tid & 31) >> 2, t = tid & 3;  // m16n8k8 fragment coordinates
 
   int h, len;
@@ -183,22 +179,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     load2(IN_V, &maps.v, (int)(row0 + (size_t)b * C), &bar_v);
   };
 
-  // ---- initial state S^T: lane v = c, key channels 64 hh .. 64 hh + 63 (coalesced over v)
+  // ---- initial state S^T: lane v = c, key channels 32 q .. 32 q + 31 (coalesced over v)
   {
     const float* s0 = P.S0 ? P.S0 + (size_t)p * D * D + c : nullptr;
-    uint32_t sbf[32];
+    uint32_t sv[32], sbf[16];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint32_t sv[32];
+    for (int j = 0; j < 32; ++j) sv[j] = s0 ? __float_as_uint(s0[(size_t)(32 * qq + j) * D]) : 0u;
+    tmem_st32(tl + T_ST + 32 * qq, sv);
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        sv[j] = s0 ? __float_as_uint(s0[(size_t)(64 * hh + 32 * half + j) * D]) : 0u;
-      tmem_st32(tl + T_ST + 64 * hh + 32 * half, sv);
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        sbf[16 * half + j] = pack_bf16(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]));
-    }
-    tmem_st32(tl + T_SB + 32 * hh, sbf);
+    for (int j = 0; j < 16; ++j) sbf[j] = pack_bf16(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]));
+    tmem_st16(tl + T_SB + 16 * qq, sbf);
     tmem_st_wait();
   }
   uint32_t ph_in = 0u, ph_v = 0u, ph_mma = 0u;
@@ -239,109 +229,100 @@ __global__ void __launch_bounds__(THREADS, 1)
       pend_in = !ok;
       if (__syncthreads_or(!ok)) { aborted = true; break; }
     }
-    // ---------------- Gamma (log2 domain): local cumulative sums, then the block offsets
-    float Gm[32];
+    // ---------------- Gamma (log2 domain): cumulative sum of this quarter, then its offset
+    float Gm[16];
     {
       const uint8_t* gp = sm + IN_G + (c >> 6) * BOX_BYTES;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) Gm[i] = ld_bf16(gp, sw128_off(prep_row(hh, i), c & 63));
+      for (int i = 0; i < 16; ++i) Gm[i] = ld_bf16(gp, sw128_off(16 * qq + i, c & 63));
       float acc = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        if (hh == 0 && i == 16) acc = 0.f;  // rows 48..63 restart; Gamma_47 is added below
-        acc = fmaf(prep_row(hh, i) < n ? Gm[i] : 0.f, LOG2E, acc);
+      for (int i = 0; i < 16; ++i) {
+        acc = fmaf(16 * qq + i < n ? Gm[i] : 0.f, LOG2E, acc);
         Gm[i] = acc;
       }
-      xch[hh][c] = hh == 0 ? Gm[15] : Gm[31];  // Gamma_15, and Gamma_47 - Gamma_15
+      xch[qq][c] = acc;
     }
     __syncthreads();
-    if (hh == 0) {
-      const float b3 = Gm[15] + xch[1][c];
-#pragma unroll
-      for (int i = 16; i < 32; ++i) Gm[i] += b3;
-      bnd[0][c] = 0.f;
-      bnd[1][c] = Gm[15];
-      bnd[3][c] = b3;
-      bnd[4][c] = Gm[31];
-      gl_s[c] = ex2(Gm[31]);
-    } else {
-      const float b1 = xch[0][c];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) Gm[i] += b1;
-      bnd[2][c] = Gm[15];
-    }
-    __syncthreads();
-    // ---------------- operands: X, Y, (K e^Gamma)^T, (Q e^Gamma)^T, Khat^T
     {
+      float base = 0.f;
+#pragma unroll
+      for (int q2 = 0; q2 < 3; ++q2) base += q2 < qq ? xch[q2][c] : 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) Gm[i] += base;
+      bnd[qq][c] = base;  // B_q = Gamma at the last row of quarter q - 1
+      if (qq == 3) {
+        bnd[4][c] = Gm[15];
+        gl_s[c] = ex2(Gm[15]);
+      }
+    }
+    __syncthreads();
+    // ---------------- operands: X, Y, (K e^Gamma)^T, (Q e^Gamma)^T, Khat^T (block R = q)
+    {
+      const int R = qq;
       const uint8_t* kp = sm + IN_K + (c >> 6) * BOX_BYTES;
       const uint8_t* qp = sm + IN_Q + (c >> 6) * BOX_BYTES;
-      float bv[5];
+      const float bR = bnd[R][c];
+      const float eB = ex2(bR);               // e^{B_R}
+      const float eL = ex2(bnd[4][c] - bR);   // e^{Gamma_L - B_R}
+      float eRR[4];
 #pragma unroll
-      for (int R = 0; R < 5; ++R) bv[R] = bnd[R][c];
+      for (int Rp = 1; Rp < 4; ++Rp) eRR[Rp] = Rp > R ? ex2(bnd[Rp][c] - bR) : 1.f;
+      eRR[0] = 1.f;
+      float kv[16], qv[16];
 #pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        const int R = hh == 0 ? 3 * a : 1 + a;  // this thread's block for rows 16a .. 16a + 15
-        const float bR = hh == 0 ? (a == 0 ? bv[0] : bv[3]) : (a == 0 ? bv[1] : bv[2]);
-        const float eB = ex2(bR);           // e^{B_R}
-        const float eL = ex2(bv[4] - bR);   // e^{Gamma_L - B_R}
-        float eRR[4];
+      for (int e = 0; e < 16; ++e) {
+        const uint32_t o = sw128_off(16 * R + e, c & 63);
+        kv[e] = ld_bf16(kp, o);
+        qv[e] = ld_bf16(qp, o);
+      }
 #pragma unroll
-        for (int Rp = 0; Rp < 4; ++Rp) eRR[Rp] = Rp > R ? ex2(bv[Rp] - bR) : 1.f;
-        float kv[16], qv[16];
+      for (int e = 0; e < 16; ++e) {
+        const bool live = 16 * R + e < n;
+        kv[e] = live ? kv[e] : 0.f;
+        qv[e] = live ? qv[e] : 0.f;
+      }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint32_t o = sw128_off(16 * R + e, c & 63);
-          kv[e] = ld_bf16(kp, o);
-          qv[e] = ld_bf16(qp, o);
+      for (int gi = 0; gi < 2; ++gi) {
+        float xk[8], xq[8], y[8], kg[8], qg[8], kh[8];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const int i = 8 * gi + e;
+          const float L0 = Gm[i] - bR, L1 = Gm[i + 1] - bR;
+          const float2 F = make_float2(ex2(L0), ex2(L1));
+          const float2 Fi = make_float2(ex2(-L0), ex2(-L1));
+          const float2 k2 = make_float2(kv[i], kv[i + 1]);
+          const float2 q2 = make_float2(qv[i], qv[i + 1]);
+          const float2 xk2 = mul2(k2, F), xq2 = mul2(q2, F), y2 = mul2(k2, Fi);
+          const float2 kg2 = mul2(xk2, make_float2(eB, eB));
+          const float2 qg2 = mul2(xq2, make_float2(eB, eB));
+          const float2 kh2 = mul2(y2, make_float2(eL, eL));
+          xk[e] = xk2.x; xk[e + 1] = xk2.y;
+          xq[e] = xq2.x; xq[e + 1] = xq2.y;
+          y[e] = y2.x; y[e + 1] = y2.y;
+          kg[e] = kg2.x; kg[e + 1] = kg2.y;
+          qg[e] = qg2.x; qg[e + 1] = qg2.y;
+          kh[e] = kh2.x; kh[e + 1] = kh2.y;
         }
+        const uint32_t r0 = 16 * R + 8 * gi;  // first token of these 8 rows
+        const uint32_t o = sw128_off(c, r0);
+        st_pack8(sb + XK + o, xk);
+        st_pack8(sb + XQ + o, xq);
+        st_pack8(sb + KG + o, kg);
+        st_pack8(sb + QG + o, qg);
+        st_pack8(sb + KH + o, kh);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const bool live = 16 * R + e < n;
-          kv[e] = live ? kv[e] : 0.f;
-          qv[e] = live ? qv[e] : 0.f;
-        }
-#pragma unroll
-        for (int gi = 0; gi < 2; ++gi) {
-          float xk[8], xq[8], y[8], kg[8], qg[8], kh[8];
+        for (int Rp = 0; Rp < 4; ++Rp) {
+          if (Rp < R) continue;
+          const float f = eRR[Rp];
+          const int nidx = y_ofs(Rp) + (int)r0;
+          float yf[8];
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
-            const int i = 16 * a + 8 * gi + e;
-            const float L0 = Gm[i] - bR, L1 = Gm[i + 1] - bR;
-            const float2 F = make_float2(ex2(L0), ex2(L1));
-            const float2 Fi = make_float2(ex2(-L0), ex2(-L1));
-            const float2 k2 = make_float2(kv[8 * gi + e], kv[8 * gi + e + 1]);
-            const float2 q2 = make_float2(qv[8 * gi + e], qv[8 * gi + e + 1]);
-            const float2 xk2 = mul2(k2, F), xq2 = mul2(q2, F), y2 = mul2(k2, Fi);
-            const float2 kg2 = mul2(xk2, make_float2(eB, eB));
-            const float2 qg2 = mul2(xq2, make_float2(eB, eB));
-            const float2 kh2 = mul2(y2, make_float2(eL, eL));
-            xk[e] = xk2.x; xk[e + 1] = xk2.y;
-            xq[e] = xq2.x; xq[e + 1] = xq2.y;
-            y[e] = y2.x; y[e + 1] = y2.y;
-            kg[e] = kg2.x; kg[e + 1] = kg2.y;
-            qg[e] = qg2.x; qg[e + 1] = qg2.y;
-            kh[e] = kh2.x; kh[e + 1] = kh2.y;
+            const float2 v2 = mul2(make_float2(y[e], y[e + 1]), make_float2(f, f));
+            yf[e] = v2.x; yf[e + 1] = v2.y;
           }
-          const uint32_t r0 = 16 * R + 8 * gi;  // first token of these 8 rows
-          const uint32_t o = sw128_off(c, r0);
-          st_pack8(sb + XK + o, xk);
-          st_pack8(sb + XQ + o, xq);
-          st_pack8(sb + KG + o, kg);
-          st_pack8(sb + QG + o, qg);
-          st_pack8(sb + KH + o, kh);
-#pragma unroll
-          for (int Rp = 0; Rp < 4; ++Rp) {
-            if (Rp < R) continue;
-            const float f = eRR[Rp];
-            const int nidx = y_ofs(Rp) + (int)r0;
-            float yf[8];
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-              const float2 v2 = mul2(make_float2(y[e], y[e + 1]), make_float2(f, f));
-              yf[e] = v2.x; yf[e + 1] = v2.y;
-            }
-            st_pack8(sb + YP + 16384u * (uint32_t)(nidx >> 6) + sw128_off(c, nidx & 63), yf);
-          }
+          st_pack8(sb + YP + 16384u * (uint32_t)(nidx >> 6) + sw128_off(c, nidx & 63), yf);
         }
       }
     }
@@ -370,9 +351,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // bf16 copy; Khat^T U accumulates onto this one)
     {
       uint32_t v[32];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int c0 = 64 * hh + 32 * half;
+      {
+        const int c0 = 32 * qq;
         tmem_ld32(tl + T_ST + c0, v);
         tmem_ld_wait();
 #pragma unroll
@@ -393,32 +373,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (__syncthreads_or(!mma_done())) { aborted = true; break; }
     // ---------------- A (fp32, into WS) and P (bf16, into PT) out of TMEM; Z^T -> bf16
     // Lane m: rows 0..63 are the k side (A), 64..127 the q side (P); row r = m & 63 belongs to
-    // block R = r >> 4 and reads the Y_R columns. This thread covers columns j in [32 hh, +32).
+    // block R = r >> 4 and reads the Y_R columns. This thread covers columns j in [16 q, +16).
     {
       float* ws = reinterpret_cast<float*>(sm + WS);
       const int r = c & 63;
       const int Rme = r >> 4;
       const bool pside = c >= 64;
       const int R0 = 2 * (quarter & 1);  // the warp's two blocks: R0 and R0 + 1
-      float vals[32];
+      float vals[16];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) vals[j] = 0.f;
+      for (int j = 0; j < 16; ++j) vals[j] = 0.f;
 #pragma unroll
       for (int a = 0; a < 2; ++a) {
         const int Rx = R0 + a;
-        const int ncols = min(32, 16 * (Rx + 1) - 32 * hh);  // warp-uniform
-        const uint32_t col = tl + T_D + (uint32_t)(y_ofs(Rx) + 32 * hh);
-        if (ncols >= 32) {
-          uint32_t v[32];
-          tmem_ld32(col, v);
-          tmem_ld_wait();
-          if (Rme == Rx) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(v[j]);
-          }
-        } else if (ncols == 16) {
+        if (qq <= Rx) {  // warp-uniform: columns 16 q .. 16 q + 15 exist in Y_Rx
           uint32_t v[16];
-          tmem_ld16(col, v);
+          tmem_ld16(tl + T_D + (uint32_t)(y_ofs(Rx) + 16 * qq), v);
           tmem_ld_wait();
           if (Rme == Rx) {
 #pragma unroll
@@ -429,9 +399,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!pside) {
         const float b = beta_s[r];
 #pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
+        for (int j4 = 0; j4 < 4; ++j4) {
           float4 x;
-          const int j = 32 * hh + 4 * j4;
+          const int j = 16 * qq + 4 * j4;
           x.x = (j < r) ? b * vals[4 * j4] : 0.f;
           x.y = (j + 1 < r) ? b * vals[4 * j4 + 1] : 0.f;
           x.z = (j + 2 < r) ? b * vals[4 * j4 + 2] : 0.f;
@@ -440,23 +410,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else {
 #pragma unroll
-        for (int j8 = 0; j8 < 4; ++j8) {
+        for (int j8 = 0; j8 < 2; ++j8) {
           float x[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const int j = 32 * hh + 8 * j8 + e;
+            const int j = 16 * qq + 8 * j8 + e;
             x[e] = (j <= r) ? vals[8 * j8 + e] : 0.f;
           }
-          st_pack8(sb + PT + sw128_off(r, 32 * hh + 8 * j8), x);
+          st_pack8(sb + PT + sw128_off(r, 16 * qq + 8 * j8), x);
         }
       }
-      // Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand
-      uint32_t v[32], zb[16];
-      tmem_ld32(tl + T_ZT + 32 * hh, v);
+      // Z^T (lane v = c, tokens 16 q ..) -> bf16 A operand
+      uint32_t v[16], zb[8];
+      tmem_ld16(tl + T_ZT + 16 * qq, v);
       tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) zb[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-      tmem_st16(tl + T_ZB + 16 * hh, zb);
+      for (int j = 0; j < 8; ++j) zb[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+      tmem_st8(tl + T_ZB + 8 * qq, zb);
     }
     __syncthreads();
     // ---------------- T = (I + A)^{-1} (unit lower triangular), in place in WS
@@ -544,19 +514,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       // (4) T Diag(beta) -> bf16, K-major [r][j]
       {
-        const int r = tid >> 2, j0 = (tid & 3) * 16;
-        float y[16];
+        const int r = tid >> 3, j0 = (tid & 7) * 8;
+        float y[8];
 #pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) {
+        for (int e4 = 0; e4 < 2; ++e4) {
           const float4 v4 = *reinterpret_cast<const float4*>(ws + r * WLD + j0 + 4 * e4);
           const float4 b4 = *reinterpret_cast<const float4*>(beta_s + j0 + 4 * e4);
           y[4 * e4] = v4.x * b4.x; y[4 * e4 + 1] = v4.y * b4.y;
           y[4 * e4 + 2] = v4.z * b4.z; y[4 * e4 + 3] = v4.w * b4.w;
         }
-        st_shared_v4(sb + TB + sw128_off(r, j0), pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
-                     pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
-        st_shared_v4(sb + TB + sw128_off(r, j0 + 8), pack_bf16(y[8], y[9]), pack_bf16(y[10], y[11]),
-                     pack_bf16(y[12], y[13]), pack_bf16(y[14], y[15]));
+        st_pack8(sb + TB + sw128_off(r, j0), y);
       }
     }
     fence_proxy_async_smem();
@@ -590,12 +557,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     // ---------------- U^T -> bf16 A operand
     {
-      uint32_t v[32], ub[16];
-      tmem_ld32(tl + T_UT + 32 * hh, v);
+      uint32_t v[16], ub[8];
+      tmem_ld16(tl + T_UT + 16 * qq, v);
       tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) ub[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-      tmem_st16(tl + T_UB + 16 * hh, ub);
+      for (int j = 0; j < 8; ++j) ub[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+      tmem_st8(tl + T_UB + 8 * qq, ub);
       tmem_st_wait();
     }
     tc_fence_before();
@@ -619,32 +586,28 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- outputs; bf16 copy of the new state for the next block
     {
       uint32_t v[32];
-      tmem_ld32(tl + T_OT + 32 * hh, v);
+      tmem_ld16(tl + T_OT + 16 * qq, *reinterpret_cast<uint32_t(*)[16]>(v));
       tmem_ld_wait();
       if (n == C) {  // full block: stage [token][channel] boxes for one TMA store
         uint8_t* ob = sm + OS + (c >> 6) * BOX_BYTES;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          *reinterpret_cast<__nv_bfloat16*>(ob + sw128_off(32 * hh + j, c & 63)) =
+        for (int j = 0; j < 16; ++j)
+          *reinterpret_cast<__nv_bfloat16*>(ob + sw128_off(16 * qq + j, c & 63)) =
               __float2bfloat16_rn(__uint_as_float(v[j]));
       } else {  // partial last block: plain stores of the valid rows only
         __nv_bfloat16* op = out + ((row0 + t0) * H + h) * D + c;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int r = 32 * hh + j;
+        for (int j = 0; j < 16; ++j) {
+          const int r = 16 * qq + j;
           if (r < n) op[(size_t)r * H * D] = __float2bfloat16_rn(__uint_as_float(v[j]));
         }
       }
-      uint32_t sbf[32];
+      uint32_t sbf[16];
+      tmem_ld32(tl + T_ST + 32 * qq, v);
+      tmem_ld_wait();
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        tmem_ld32(tl + T_ST + 64 * hh + 32 * half, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          sbf[16 * half + j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-      }
-      tmem_st32(tl + T_SB + 32 * hh, sbf);
+      for (int j = 0; j < 16; ++j) sbf[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+      tmem_st16(tl + T_SB + 16 * qq, sbf);
       tmem_st_wait();
     }
     fence_proxy_async_smem();
@@ -668,13 +631,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (P.S_final) {  // S_final[c'][v] from S^T (lane v): coalesced over v
     float* sf = P.S_final + (size_t)p * D * D + c;
     uint32_t v[32];
+    tmem_ld32(tl + T_ST + 32 * qq, v);
+    tmem_ld_wait();
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      tmem_ld32(tl + T_ST + 64 * hh + 32 * half, v);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) sf[(size_t)(64 * hh + 32 * half + j) * D] = __uint_as_float(v[j]);
-    }
+    for (int j = 0; j < 32; ++j) sf[(size_t)(32 * qq + j) * D] = __uint_as_float(v[j]);
   }
   tc_fence_before();
   __syncthreads();
