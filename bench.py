@@ -418,9 +418,11 @@ def bench_varlen(kda, args, world, rank, device, stream, peaks, steps=3):
     lens = (inp["cu_seqlens"][1:] - inp["cu_seqlens"][:-1]).tolist()
     del inp, q, k, v, g, b, out
     torch.cuda.empty_cache()
-    return {"workload": w["name"], "ms_per_step": ms, "seq_lens": lens,
-            "tokens_per_s": world * T / (ms * 1e-3),
-            "tflops": T * H * useful_flops_per_token_head(C) / (ms * 1e-3) / 1e12,
+    # the tensor-core kernel serves a 128-token chunk as two 64-token blocks: count that work
+    block = 64 if C in (64, 128) else C
+    return {"workload": w["name"], "ms_per_step": ms, "seq_lens": lens, "C": C,
+            "block_tokens": block, "tokens_per_s": world * T / (ms * 1e-3),
+            "tflops": T * H * useful_flops_per_token_head(block) / (ms * 1e-3) / 1e12,
             "clocks": clocks,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm"], "traffic": None,

@@ -643,7 +643,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 
-inline bool tc_supports(int C_) { return C_ == C; }
+// The kernel works in 64-token blocks. A request for 128-token chunks is served by the same
+// kernel: each chunk is two consecutive 64-token blocks, which is the same mathematics (the
+// block form is exact for any block size) with fewer intra-block products.
+inline bool tc_supports(int C_) { return C_ == C || C_ == 2 * C; }
 
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;

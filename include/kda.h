@@ -54,9 +54,11 @@ typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype_t;
  *   S0      : [B, H, d_k, d_v] fp32, read only; NULL means a zero initial state
  *   out     : [B, T, H, d_v]  dtype, written (o_t for every token)
  *   S_final : [B, H, d_k, d_v] fp32, written with the state after token T; NULL = not written
- *   C       : block size (16, 32, 64 or 128); the result does not depend on it beyond rounding
- * fp32 inputs run on CUDA cores in fp32 throughout. bf16 inputs run on the tensor cores
- * (bf16 operands, fp32 accumulation, fp32 state) when d_k = d_v = 128 and C is 64 or 128.
+ *   C       : chunk size (16, 32, 64 or 128); the result does not depend on it beyond rounding
+ * fp32 inputs run on CUDA cores in fp32 throughout, in 16- or 32-token blocks. bf16 inputs run
+ * on the tensor cores (bf16 operands, fp32 accumulation, fp32 state) when d_k = d_v = 128 and
+ * C is 64 or 128; that kernel works in 64-token blocks, so a 128-token chunk is processed as
+ * two consecutive 64-token blocks (the same mathematics).
  */
 kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g,
                            const void* beta, const float* S0, void* out, float* S_final,
