@@ -12,15 +12,20 @@
 //
 // Bounded decay. Over a block of 64 tokens Gamma can fall to -320, so e^{-Gamma} overflows any
 // floating type and A, P cannot be one product (K e^Gamma)(K e^{-Gamma})^T. With
-// g >= g_min = -5 each 16-token sub-block spans at most e^80, inside the bf16/fp32 range, so A
-// and P come from one tensor-core product X Y^T in which every row block R = 0..3 has its own
-// reference B_R = Gamma at the last row of block R - 1 (B_0 = 0):
-//   X[r]     = [k_r ; q_r] e^{Gamma_r - B_R}   for r in block R           (factor in [e^-80, 1])
-//   Y_R[j]   = k_j e^{B_R - Gamma_j}           for j < 16(R + 1)          (<= 1 before block R,
-//                                                                          <= e^80 inside it)
-// Y stacks Y_0..Y_3 as N = 16 + 32 + 48 + 64 = 160 columns, so X is read once; the rows of
-// block R take their A and P entries from the Y_R columns. Every factor is formed from one
-// exponential per element, times per-channel factors e^{B_R' - B_R} <= 1.
+// g >= g_min = -5 every 16-token sub-block spans at most e^80, inside the bf16/fp32 range. The
+// block is split into two 32-token halves, each with its own reference point rho placed on the
+// boundary between its two 16-token sub-blocks (rho_A = Gamma_15, rho_B = Gamma_47):
+//   X[r]   = [k_r ; q_r] e^{Gamma_r - rho(r)}     for every row r        (factor in [e^-80, e^75])
+//   Y_A[j] = k_j e^{rho_A - Gamma_j}              for j < 32             (in [e^-75, e^80])
+//   Y_B[j] = k_j e^{rho_B - Gamma_j}              for j < 64             (<= e^80; for j < 32 it
+//                                                                         may underflow, only where
+//                                                                         every product it enters
+//                                                                         is below e^-12)
+// so that one tensor-core product X [Y_B ; Y_A]^T (N = 96) holds every A_rj and P_rj with
+// j <= r: rows of the first half read the Y_A columns, rows of the second half the Y_B columns.
+// Entries above the diagonal may overflow in that product; they are discarded by selection.
+// Every factor is one exponential of its own exponent, so nothing overflows and anything that
+// underflows is below that bound.
 //
 // Layout. One CTA (512 threads) owns one (sequence, head) problem and walks its blocks in
 // order. In the elementwise phases thread (c, q) owns channel / TMEM lane c and the q-th
@@ -66,14 +71,14 @@ constexpr uint32_t IN_K = 0;          // k tile (two 64-channel boxes of [64 tok
 constexpr uint32_t IN_Q = 16384;      // q tile
 constexpr uint32_t IN_G = 32768;      // g tile
 constexpr uint32_t IN_V = 49152;      // v tile (MN-major A of V^T (T Diag beta)^T as loaded)
-constexpr uint32_t XY = 65536;        // 80 KB region with two lives per block:
+constexpr uint32_t XY = 65536;        // 64 KB region with two lives per block:
 constexpr uint32_t XK = XY;           //   X rows 0..63 (k side), MN-major A panel 0
 constexpr uint32_t XQ = XY + 16384;   //   X rows 64..127 (q side), MN-major A panel 1
-constexpr uint32_t YP = XY + 32768;   //   Y, N = 160 columns in 3 MN-major B panels
+constexpr uint32_t YP = XY + 32768;   //   [Y_B | Y_A], N = 96 columns in 2 MN-major B panels
 constexpr uint32_t WS = XY;           // after D: fp32 A then T ([64][WLD], 18 KB)
 constexpr uint32_t PT = XY + 18432;   //   P [r][j], K-major B of O^T += U^T P^T (8 KB)
 constexpr uint32_t TB = XY + 26624;   //   fp32 M_R during the solve, then T Diag(beta) [r][j]
-constexpr uint32_t KG = XY + 81920;   // (K e^Gamma)^T [c][r]: MN-major B panel 0 of [Z^T | O^T]
+constexpr uint32_t KG = XY + 65536;   // (K e^Gamma)^T [c][r]: MN-major B panel 0 of [Z^T | O^T]
 constexpr uint32_t QG = KG + 16384;   // (Q e^Gamma)^T [c][r]: MN-major B panel 1 of [Z^T | O^T]
 constexpr uint32_t KH = QG + 16384;   // Khat^T [c][r]: K-major B of S^T += U^T Khat
 constexpr uint32_t OS = KH + 16384;   // O staging for the TMA store: two [64 tokens][64] boxes
@@ -84,15 +89,15 @@ constexpr uint32_t BOX_BYTES = 8192;                // one 64-channel x 64-token
 // ---- TMEM columns (512 allocated)
 constexpr uint32_t T_ST = 0;    // S^T fp32 [v][c], 128
 constexpr uint32_t T_SB = 128;  // S^T bf16 (A operand), 64
-constexpr uint32_t T_D = 192;   // X Y^T, 160; once read: U^T fp32 (64) and U^T bf16 (32)
+constexpr uint32_t T_D = 192;   // X Y^T, 96; once read: U^T fp32 (64) and U^T bf16 (32)
 constexpr uint32_t T_UT = 192;
 constexpr uint32_t T_UB = 256;
 constexpr uint32_t T_ZT = 352;  // Z^T fp32, 64
 constexpr uint32_t T_OT = 416;  // O^T fp32, 64 (directly after Z^T: one product writes both)
 constexpr uint32_t T_ZB = 480;  // Z^T bf16 (A operand), 32
 
-// First column of Y_R inside the N = 160 stack.
-__host__ __device__ constexpr int y_ofs(int R) { return 8 * R * (R + 1); }  // 0, 16, 48, 96
+// Columns of the X Y^T product: Y_B (reference rho_B) at 0..63, Y_A (rho_A) at 64..95.
+constexpr int Y_A = 64;
 
 // Row stride (floats) of the fp32 64 x 64 solve workspace: 72 makes the tf32 B-fragment loads
 // (rows t, columns g) conflict-free.
@@ -260,15 +265,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- operands: X, Y, (K e^Gamma)^T, (Q e^Gamma)^T, Khat^T (block R = q)
     {
       const int R = qq;
+      const bool first = R < 2;  // first half: reference rho_A, else rho_B
       const uint8_t* kp = sm + IN_K + (c >> 6) * BOX_BYTES;
       const uint8_t* qp = sm + IN_Q + (c >> 6) * BOX_BYTES;
-      const float bR = bnd[R][c];
-      const float eB = ex2(bR);               // e^{B_R}
-      const float eL = ex2(bnd[4][c] - bR);   // e^{Gamma_L - B_R}
-      float eRR[4];
-#pragma unroll
-      for (int Rp = 1; Rp < 4; ++Rp) eRR[Rp] = Rp > R ? ex2(bnd[Rp][c] - bR) : 1.f;
-      eRR[0] = 1.f;
+      const float rhoB = bnd[3][c];
+      const float rho = first ? bnd[1][c] : rhoB;
+      const float gL = bnd[4][c];
       float kv[16], qv[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
@@ -284,22 +286,26 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
 #pragma unroll
       for (int gi = 0; gi < 2; ++gi) {
-        float xk[8], xq[8], y[8], kg[8], qg[8], kh[8];
+        float xk[8], xq[8], y[8], yb[8], kg[8], qg[8], kh[8];
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
           const int i = 8 * gi + e;
-          const float L0 = Gm[i] - bR, L1 = Gm[i + 1] - bR;
-          const float2 F = make_float2(ex2(L0), ex2(L1));
-          const float2 Fi = make_float2(ex2(-L0), ex2(-L1));
+          const float L0 = Gm[i] - rho, L1 = Gm[i + 1] - rho;
+          const float2 F = make_float2(ex2(L0), ex2(L1));                  // e^{Gamma - rho}
+          const float2 Fi = make_float2(ex2(-L0), ex2(-L1));               // e^{rho - Gamma}
+          const float2 eG = make_float2(ex2(Gm[i]), ex2(Gm[i + 1]));       // e^{Gamma}
+          const float2 eH = make_float2(ex2(gL - Gm[i]), ex2(gL - Gm[i + 1]));  // e^{Gamma_L - Gamma}
           const float2 k2 = make_float2(kv[i], kv[i + 1]);
           const float2 q2 = make_float2(qv[i], qv[i + 1]);
           const float2 xk2 = mul2(k2, F), xq2 = mul2(q2, F), y2 = mul2(k2, Fi);
-          const float2 kg2 = mul2(xk2, make_float2(eB, eB));
-          const float2 qg2 = mul2(xq2, make_float2(eB, eB));
-          const float2 kh2 = mul2(y2, make_float2(eL, eL));
+          const float2 kg2 = mul2(k2, eG), qg2 = mul2(q2, eG), kh2 = mul2(k2, eH);
+          float2 yb2 = y2;
+          if (first)  // e^{rho_B - Gamma}
+            yb2 = mul2(k2, make_float2(ex2(rhoB - Gm[i]), ex2(rhoB - Gm[i + 1])));
           xk[e] = xk2.x; xk[e + 1] = xk2.y;
           xq[e] = xq2.x; xq[e + 1] = xq2.y;
           y[e] = y2.x; y[e + 1] = y2.y;
+          yb[e] = yb2.x; yb[e + 1] = yb2.y;
           kg[e] = kg2.x; kg[e + 1] = kg2.y;
           qg[e] = qg2.x; qg[e + 1] = qg2.y;
           kh[e] = kh2.x; kh[e + 1] = kh2.y;
@@ -311,18 +317,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         st_pack8(sb + KG + o, kg);
         st_pack8(sb + QG + o, qg);
         st_pack8(sb + KH + o, kh);
-#pragma unroll
-        for (int Rp = 0; Rp < 4; ++Rp) {
-          if (Rp < R) continue;
-          const float f = eRR[Rp];
-          const int nidx = y_ofs(Rp) + (int)r0;
-          float yf[8];
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const float2 v2 = mul2(make_float2(y[e], y[e + 1]), make_float2(f, f));
-            yf[e] = v2.x; yf[e + 1] = v2.y;
-          }
-          st_pack8(sb + YP + 16384u * (uint32_t)(nidx >> 6) + sw128_off(c, nidx & 63), yf);
+        if (first) {
+          st_pack8(sb + YP + 16384u + o, y);  // Y_A (panel 1, columns 64 + r)
+          st_pack8(sb + YP + o, yb);           // Y_B (panel 0)
+        } else {
+          st_pack8(sb + YP + o, y);            // Y_B
         }
       }
     }
@@ -332,10 +331,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (tid == 0) issue_in(blk + 1);
       pend_in = true;
     }
-    // ---------------- tcgen05: D = X Y^T ; [Z^T | O^T] = S^T [(K e^Gamma)^T | (Q e^Gamma)^T]
+    // ---------------- tcgen05: D = X [Y_B | Y_A]^T ; [Z^T | O^T] = S^T [(K e^Gamma)^T | (Q e^Gamma)^T]
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t id_d = idesc_bf16(128, 160, 1, 1, 0);
+      const uint32_t id_d = idesc_bf16(128, 96, 1, 1, 0);
       const uint32_t id_z = idesc_bf16(128, 128, 0, 1, 0);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
@@ -372,29 +371,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (__syncthreads_or(!mma_done())) { aborted = true; break; }
     // ---------------- A (fp32, into WS) and P (bf16, into PT) out of TMEM; Z^T -> bf16
-    // Lane m: rows 0..63 are the k side (A), 64..127 the q side (P); row r = m & 63 belongs to
-    // block R = r >> 4 and reads the Y_R columns. This thread covers columns j in [16 q, +16).
+    // Lane m: rows 0..63 are the k side (A), 64..127 the q side (P); row r = m & 63 reads the
+    // Y_A columns in the first half of the block, the Y_B columns in the second (warp-uniform).
+    // This thread covers columns j in [16 q, +16).
     {
       float* ws = reinterpret_cast<float*>(sm + WS);
       const int r = c & 63;
-      const int Rme = r >> 4;
       const bool pside = c >= 64;
-      const int R0 = 2 * (quarter & 1);  // the warp's two blocks: R0 and R0 + 1
+      const bool firsthalf = (quarter & 1) == 0;
       float vals[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) vals[j] = 0.f;
+      if (!firsthalf || qq < 2) {  // the first half has columns j < 32 only
+        uint32_t v[16];
+        tmem_ld16(tl + T_D + (uint32_t)((firsthalf ? Y_A : 0) + 16 * qq), v);
+        tmem_ld_wait();
 #pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        const int Rx = R0 + a;
-        if (qq <= Rx) {  // warp-uniform: columns 16 q .. 16 q + 15 exist in Y_Rx
-          uint32_t v[16];
-          tmem_ld16(tl + T_D + (uint32_t)(y_ofs(Rx) + 16 * qq), v);
-          tmem_ld_wait();
-          if (Rme == Rx) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) vals[j] = __uint_as_float(v[j]);
-          }
-        }
+        for (int j = 0; j < 16; ++j) vals[j] = __uint_as_float(v[j]);
       }
       if (!pside) {
         const float b = beta_s[r];

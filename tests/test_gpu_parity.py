@@ -208,6 +208,28 @@ def test_strong_decay_floor(kda):
     check(Sf, S_ref, "bf16", "S_final")
 
 
+@pytest.mark.parametrize("pattern", ["bursty", "gap"])
+def test_uneven_decay(kda, pattern):
+    """Decay concentrated on a few tokens: the within-block factors reach the ends of their
+    range while some products across sub-blocks stay O(1). "gap" puts g = -5 on tokens 16..20
+    and 34..47 of every block and 0 elsewhere; "bursty" draws g = -5 with probability 0.3 per
+    token and channel, else 0."""
+    inp = kda_synth.make_prefill_inputs(1, 256, 2, 128, 128, "bf16", seed=31, S0_std=0.05)
+    g = torch.zeros_like(inp["g"], dtype=torch.float32)
+    if pattern == "gap":
+        pos = torch.arange(256) % 64
+        mask = ((pos >= 16) & (pos <= 20)) | ((pos >= 34) & (pos <= 47))
+        g[:, mask] = -5.0
+    else:
+        gen = torch.Generator().manual_seed(5)
+        g = torch.where(torch.rand(g.shape, generator=gen) < 0.3, -5.0, 0.0)
+    inp["g"] = g.to(inp["g"].dtype)
+    out, Sf = run_dense(kda, inp, 64)
+    o_ref, S_ref = oracle_dense(inp)
+    check(out, o_ref, "bf16", "out")
+    check(Sf, S_ref, "bf16", "S_final")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("C", [64, 128])
 def test_varlen_small_edges(kda, dtype, C):
