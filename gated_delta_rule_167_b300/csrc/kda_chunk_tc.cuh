@@ -28,25 +28,27 @@
 // underflows is below that bound.
 //
 // Layout. One CTA (512 threads) owns one (sequence, head) problem and walks its blocks in
-// order. In the elementwise phases thread (c, q) owns channel / TMEM lane c and the q-th
-// 16-token quarter of the block (the q-th sub-block R = q), so every operand it produces is a
-// contiguous 32-byte run of one row of a [channel][token] tile. The state is kept transposed in TMEM: S^T in fp32 (lane = value channel v, column =
+// order. The state is kept transposed in TMEM: S^T in fp32 (lane = value channel v, column =
 // key channel c) and its bf16 copy, which is the A operand of the products with S. Every
 // intermediate of the state update (the residual Z = (K e^Gamma) S, U, the bf16 copies) goes
-// TMEM -> registers -> TMEM, so only operands built from the inputs pass through shared memory
-// (and need a proxy fence). Per block:
-//   TMA: k, q, g, v tiles (two 64-channel boxes each, 128-byte swizzle)
-//   SIMT: Gamma; X, Y, (K e^Gamma)^T, (Q e^Gamma)^T, Khat^T operands ([channel][token] rows)
-//   tcgen05: D = X Y^T (M 128, N 160);  [Z^T | O^T] = S^T [(K e^Gamma)^T | (Q e^Gamma)^T]
-//   SIMT (meanwhile): S^T <- S^T Diag(e^{Gamma_L}) in TMEM
-//   SIMT: A and P out of TMEM; T = (I + A)^{-1} (16 x 16 blocks, fp32 / 3xTF32); T Diag(beta)
-//   tcgen05: U^T = V^T (T Diag beta)^T - Z^T (T Diag beta)^T
-//   tcgen05: O^T += U^T P^T;  S^T += U^T Khat
-//   SIMT: O to global memory (TMA store of full blocks); bf16 copy of S^T for the next block.
-// Transposed forms keep every product at M = 128 (TMEM lane = row). Only the bf16 copy of the
-// state feeds the tensor cores; the fp32 state accumulates in TMEM, so rounding does not
-// accumulate in S itself. Every wait is bounded; a timeout latches KDA_ERR_TIMEOUT, lets issued
-// copies and products land, frees TMEM and returns.
+// TMEM -> registers -> TMEM, so only operands built from the inputs pass through shared memory.
+//
+// Two warp groups work on consecutive blocks at the same time:
+//   group P (warps 0-7), block n + 1: Gamma; X, Y, (K e^Gamma)^T, (Q e^Gamma)^T, Khat^T
+//     ([channel][token] rows, 16-byte stores); then the A/P product D = X [Y_B | Y_A]^T.
+//   group S (warps 8-15), block n:
+//     tcgen05: [Z^T | O^T] = S^T [(K e^Gamma)^T | (Q e^Gamma)^T]; meanwhile S^T <- S^T e^{Gamma_L}
+//     SIMT: A and P out of TMEM; Z^T -> bf16; T = (I + A)^{-1} (16 x 16 blocks, fp32 with
+//           3xTF32 warp MMAs); T Diag(beta) -> bf16
+//     tcgen05: U^T = V^T (T Diag beta)^T - Z^T (T Diag beta)^T;  SIMT: U^T -> bf16
+//     tcgen05: O^T += U^T P^T;  S^T += U^T Khat;  SIMT: O out, bf16 copy of S^T
+// Shared buffers pass between the groups through mbarriers: P may rewrite X and Y once the A/P
+// product of the previous block has completed, (K/Q e^Gamma)^T once S's first product has, and
+// Khat^T (held in registers until then) once S's last product has; S starts a block once its
+// A/P product is complete. Transposed forms keep every product at M = 128 (TMEM lane = row).
+// Only the bf16 copy of the state feeds the tensor cores; the fp32 state accumulates in TMEM,
+// so rounding does not accumulate in S itself. Every wait is bounded; a timeout latches
+// KDA_ERR_TIMEOUT, lets issued copies and products land, frees TMEM and returns.
 #pragma once
 
 #include <cuda.h>
@@ -63,40 +65,40 @@ namespace tc {
 
 constexpr int C = 64;
 constexpr int D = 128;
-constexpr int THREADS = 512;
+constexpr int THREADS = 512;  // two groups of 256
+constexpr int GROUP = 256;
+constexpr int BAR_P = 1, BAR_S = 2;  // hardware barrier ids of the groups
 constexpr float LOG2E = 1.4426950408889634f;
 
 // ---- shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t IN_K = 0;          // k tile (two 64-channel boxes of [64 tokens][64])
-constexpr uint32_t IN_Q = 16384;      // q tile
-constexpr uint32_t IN_G = 32768;      // g tile
-constexpr uint32_t IN_V = 49152;      // v tile (MN-major A of V^T (T Diag beta)^T as loaded)
-constexpr uint32_t XY = 65536;        // 64 KB region with two lives per block:
-constexpr uint32_t XK = XY;           //   X rows 0..63 (k side), MN-major A panel 0
-constexpr uint32_t XQ = XY + 16384;   //   X rows 64..127 (q side), MN-major A panel 1
-constexpr uint32_t YP = XY + 32768;   //   [Y_B | Y_A], N = 96 columns in 2 MN-major B panels
-constexpr uint32_t WS = XY;           // after D: fp32 A then T ([64][WLD], 18 KB)
-constexpr uint32_t PT = XY + 18432;   //   P [r][j], K-major B of O^T += U^T P^T (8 KB)
-constexpr uint32_t TB = XY + 26624;   //   fp32 M_R during the solve, then T Diag(beta) [r][j]
-constexpr uint32_t KG = XY + 65536;   // (K e^Gamma)^T [c][r]: MN-major B panel 0 of [Z^T | O^T]
-constexpr uint32_t QG = KG + 16384;   // (Q e^Gamma)^T [c][r]: MN-major B panel 1 of [Z^T | O^T]
-constexpr uint32_t KH = QG + 16384;   // Khat^T [c][r]: K-major B of S^T += U^T Khat
-constexpr uint32_t OS = KH + 16384;   // O staging for the TMA store: two [64 tokens][64] boxes
-constexpr uint32_t SMEM_BYTES = OS + 16384;
+constexpr uint32_t IN_K = 0;           // k tile (two 64-channel boxes of [64 tokens][64])
+constexpr uint32_t IN_Q = 16384;       // q tile
+constexpr uint32_t IN_G = 32768;       // g tile
+constexpr uint32_t IN_V = 49152;       // v tile (MN-major A of V^T (T Diag beta)^T as loaded)
+constexpr uint32_t XK = 65536;         // X rows 0..63 (k side), MN-major A panel 0
+constexpr uint32_t XQ = XK + 16384;    // X rows 64..127 (q side), MN-major A panel 1
+constexpr uint32_t YP = XQ + 16384;    // [Y_B | Y_A], N = 96 columns in 2 MN-major B panels
+constexpr uint32_t KG = YP + 32768;    // (K e^Gamma)^T [c][r]: MN-major B panel 0 of [Z^T | O^T]
+constexpr uint32_t QG = KG + 16384;    // (Q e^Gamma)^T [c][r]: MN-major B panel 1 of [Z^T | O^T]
+constexpr uint32_t KH = QG + 16384;    // Khat^T [c][r]: K-major B of S^T += U^T Khat
+constexpr uint32_t WS = KH + 16384;    // fp32 A, then T ([64][WLD], 18 KB)
+constexpr uint32_t PT = WS + 18432;    // P [r][j], K-major B of O^T += U^T P^T (8 KB)
+constexpr uint32_t TB = PT + 8192;     // fp32 M_R during the solve, then T Diag(beta) [r][j]
+constexpr uint32_t SMEM_BYTES = TB + 8192;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for aligning the base
 constexpr uint32_t BOX_BYTES = 8192;                // one 64-channel x 64-token TMA box
 
 // ---- TMEM columns (512 allocated)
 constexpr uint32_t T_ST = 0;    // S^T fp32 [v][c], 128
 constexpr uint32_t T_SB = 128;  // S^T bf16 (A operand), 64
-constexpr uint32_t T_D = 192;   // X Y^T, 96; once read: U^T fp32 (64) and U^T bf16 (32)
-constexpr uint32_t T_UT = 192;
-constexpr uint32_t T_UB = 256;
-constexpr uint32_t T_ZT = 352;  // Z^T fp32, 64
-constexpr uint32_t T_OT = 416;  // O^T fp32, 64 (directly after Z^T: one product writes both)
-constexpr uint32_t T_ZB = 480;  // Z^T bf16 (A operand), 32
+constexpr uint32_t T_D = 192;   // X [Y_B | Y_A]^T, 96
+constexpr uint32_t T_ZT = 288;  // Z^T fp32, 64; after its bf16 copy: U^T fp32
+constexpr uint32_t T_OT = 352;  // O^T fp32, 64 (directly after Z^T: one product writes both)
+constexpr uint32_t T_ZB = 416;  // Z^T bf16 (A operand), 32; after its use: U^T bf16
+constexpr uint32_t T_UT = T_ZT;
+constexpr uint32_t T_UB = T_ZB;
 
-// Columns of the X Y^T product: Y_B (reference rho_B) at 0..63, Y_A (rho_A) at 64..95.
+// Columns of the A/P product: Y_B (reference rho_B) at 0..63, Y_A (rho_A) at 64..95.
 constexpr int Y_A = 64;
 
 // Row stride (floats) of the fp32 64 x 64 solve workspace: 72 makes the tf32 B-fragment loads
@@ -106,7 +108,7 @@ constexpr int WLD = 72;
 __host__ __device__ constexpr int mb_off(int R) { return R == 1 ? 0 : (R == 2 ? 320 : 896); }
 
 struct TmaMaps {
-  CUtensorMap q, k, v, g, o;
+  CUtensorMap q, k, v, g;
 };
 
 using namespace sm100;
@@ -120,25 +122,33 @@ __device__ __forceinline__ void st_pack8(uint32_t saddr, const float (&x)[8]) {
                pack_bf16(x[6], x[7]));
 }
 
+__device__ __forceinline__ void st_words4(uint32_t saddr, const uint32_t (&w)[4]) {
+  st_shared_v4(saddr, w[0], w[1], w[2], w[3]);
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
     chunk_tc_kernel(const __grid_constant__ TmaMaps maps, SeqParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(sm);
-  __shared__ uint64_t bar_in, bar_v, bar_mma;
+  // bar_in: k, q, g tiles landed          bar_v: v tile landed
+  // bar_prep: P finished a block's operands (release / acquire for its generic stores)
+  // bar_D, bar_ZO, bar_G2, bar_G3: tcgen05 products complete
+  __shared__ uint64_t bar_in, bar_v, bar_prep, bar_D, bar_ZO, bar_G2, bar_G3;
   __shared__ uint32_t tmem_base_s;
-  __shared__ __align__(16) float beta_s[C];
-  __shared__ float xch[4][D];
-  __shared__ float bnd[5][D];  // log2-domain Gamma at the block boundaries: B_0..B_3, B_4 = Gamma_L
-  __shared__ __align__(16) float gl_s[D];  // e^{Gamma_L} per key channel
-  __shared__ float trr[4][16][17];         // diagonal blocks T_RR of the solve
+  __shared__ __align__(16) float beta_s[2][C];  // by block parity
+  __shared__ __align__(16) float gl_s[2][D];    // e^{Gamma_L} per key channel, by block parity
+  __shared__ float xch[4][D];                   // sub-block sums of g (group P)
+  __shared__ float trr[4][16][17];              // diagonal blocks T_RR of the solve (group S)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  const int quarter = warp & 3;  // TMEM lane quarter this warp may address
-  const int c = tid & (D - 1);   // channel (= TMEM lane) owned in the elementwise phases
-  const int qq = tid >> 7;       // which 16-token quarter (and 32-column quarter) it handles
+  const int quarter = warp & 3;   // TMEM lane quarter this warp may address
+  const bool isP = tid < GROUP;
+  const int lt = tid & (GROUP - 1);  // index inside the group
+  const int c = lt & (D - 1);        // channel (= TMEM lane) owned in the elementwise phases
+  const int hh = lt >> 7;            // which half this thread handles inside its group
   const int g = (tid & 31) >> 2, t = tid & 3;  // m16n8k8 fragment coordinates
 
   int h, len;
@@ -147,18 +157,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (!resolve_problem(P, p, h, row0, len)) return;
   const int H = P.H;
   const int nblocks = (len + C - 1) / C;
-  __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(P.out);
 
   if (tid == 0) {
     mbar_init(&bar_in, 1);
     mbar_init(&bar_v, 1);
-    mbar_init(&bar_mma, 1);
+    mbar_init(&bar_prep, 1);
+    mbar_init(&bar_D, 1);
+    mbar_init(&bar_ZO, 1);
+    mbar_init(&bar_G2, 1);
+    mbar_init(&bar_G3, 1);
     fence_mbar_init();
     prefetch_tensormap(&maps.q);
     prefetch_tensormap(&maps.k);
     prefetch_tensormap(&maps.v);
     prefetch_tensormap(&maps.g);
-    prefetch_tensormap(&maps.o);
   }
   if (warp == 0) tmem_alloc(&tmem_base_s, 512);
   tc_fence_before();
@@ -167,467 +179,528 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = tmem_base_s;
   const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);  // this warp's lane quarter
 
-  // ---- TMA issue (thread 0 only)
   auto load2 = [&](uint32_t dst, const CUtensorMap* m, int row, uint64_t* bar) {
     tma_load_3d(sm + dst, m, 0, h, row, bar);
     tma_load_3d(sm + dst + BOX_BYTES, m, 64, h, row, bar);
   };
-  auto issue_in = [&](int b) {
-    const int row = (int)(row0 + (size_t)b * C);
-    mbar_arrive_expect_tx(&bar_in, 6 * BOX_BYTES);
-    load2(IN_K, &maps.k, row, &bar_in);
-    load2(IN_Q, &maps.q, row, &bar_in);
-    load2(IN_G, &maps.g, row, &bar_in);
-  };
-  auto issue_v = [&](int b) {
-    mbar_arrive_expect_tx(&bar_v, 2 * BOX_BYTES);
-    load2(IN_V, &maps.v, (int)(row0 + (size_t)b * C), &bar_v);
-  };
-
-  // ---- initial state S^T: lane v = c, key channels 32 q .. 32 q + 31 (coalesced over v)
-  {
-    const float* s0 = P.S0 ? P.S0 + (size_t)p * D * D + c : nullptr;
-    uint32_t sv[32], sbf[16];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) sv[j] = s0 ? __float_as_uint(s0[(size_t)(32 * qq + j) * D]) : 0u;
-    tmem_st32(tl + T_ST + 32 * qq, sv);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) sbf[j] = pack_bf16(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]));
-    tmem_st16(tl + T_SB + 16 * qq, sbf);
-    tmem_st_wait();
-  }
-  uint32_t ph_in = 0u, ph_v = 0u, ph_mma = 0u;
-  bool pend_in = false, pend_v = false, pend_mma = false;
-  if (tid == 0 && nblocks > 0) {
-    issue_in(0);
-    issue_v(0);
-  }
-  if (nblocks > 0) pend_in = pend_v = true;
-  // beta of the next block is loaded one block ahead (a strided global read), kept as raw bits
-  // so that nothing waits on the load until the block that needs it
-  const unsigned short* __restrict__ beta_u = static_cast<const unsigned short*>(P.beta);
-  unsigned short beta_next = 0;
-  if (tid < C && tid < len) beta_next = beta_u[(row0 + tid) * H + h];
-  tc_fence_before();
-  __syncthreads();
-
   bool aborted = false;
-  auto mma_done = [&]() -> bool {
-    const bool ok = mbar_wait(&bar_mma, ph_mma);
-    if (ok) ph_mma ^= 1u;  // a timed-out phase stays the one to drain
-    pend_mma = !ok;
-    tc_fence_after();
-    return ok;
+  // Waits of a whole group: one thread polls the mbarrier while the others sleep in the
+  // group's hardware barrier (no issue slots spent spinning); the outcome is shared.
+  auto group_wait2 = [&](uint64_t* b1, uint32_t p1, uint64_t* b2, uint32_t p2, int id) -> bool {
+    bool ok = true;
+    if (lt == 0) {
+      ok = mbar_wait(b1, p1);
+      if (b2 != nullptr) ok = ok && mbar_wait(b2, p2);
+    }
+    return !named_sync_or(id, GROUP, !ok);
   };
 
-  for (int blk = 0; blk < nblocks; ++blk) {
-    const int t0 = blk * C;
-    const int n = min(C, len - t0);
-    if (tid < C) {
-      beta_s[tid] = __uint_as_float((uint32_t)beta_next << 16);  // zero past the end
-      beta_next = 0;
-      if (tid < len - t0 - C) beta_next = beta_u[(row0 + t0 + C + tid) * H + h];
-    }
-    {
-      const bool ok = mbar_wait(&bar_in, ph_in);
-      if (ok) ph_in ^= 1u;
-      pend_in = !ok;
-      if (__syncthreads_or(!ok)) { aborted = true; break; }
-    }
-    // ---------------- Gamma (log2 domain): cumulative sum of this quarter, then its offset
-    float Gm[16];
-    {
-      const uint8_t* gp = sm + IN_G + (c >> 6) * BOX_BYTES;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) Gm[i] = ld_bf16(gp, sw128_off(16 * qq + i, c & 63));
-      float acc = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        acc = fmaf(16 * qq + i < n ? Gm[i] : 0.f, LOG2E, acc);
-        Gm[i] = acc;
-      }
-      xch[qq][c] = acc;
-    }
-    __syncthreads();
-    {
-      float base = 0.f;
-#pragma unroll
-      for (int q2 = 0; q2 < 3; ++q2) base += q2 < qq ? xch[q2][c] : 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) Gm[i] += base;
-      bnd[qq][c] = base;  // B_q = Gamma at the last row of quarter q - 1
-      if (qq == 3) {
-        bnd[4][c] = Gm[15];
-        gl_s[c] = ex2(Gm[15]);
-      }
-    }
-    __syncthreads();
-    // ---------------- operands: X, Y, (K e^Gamma)^T, (Q e^Gamma)^T, Khat^T (block R = q)
-    {
-      const int R = qq;
-      const bool first = R < 2;  // first half: reference rho_A, else rho_B
-      const uint8_t* kp = sm + IN_K + (c >> 6) * BOX_BYTES;
-      const uint8_t* qp = sm + IN_Q + (c >> 6) * BOX_BYTES;
-      const float rhoB = bnd[3][c];
-      const float rho = first ? bnd[1][c] : rhoB;
-      const float gL = bnd[4][c];
-      float kv[16], qv[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const uint32_t o = sw128_off(16 * R + e, c & 63);
-        kv[e] = ld_bf16(kp, o);
-        qv[e] = ld_bf16(qp, o);
-      }
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const bool live = 16 * R + e < n;
-        kv[e] = live ? kv[e] : 0.f;
-        qv[e] = live ? qv[e] : 0.f;
-      }
-#pragma unroll
-      for (int gi = 0; gi < 2; ++gi) {
-        float xk[8], xq[8], y[8], yb[8], kg[8], qg[8], kh[8];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const int i = 8 * gi + e;
-          const float L0 = Gm[i] - rho, L1 = Gm[i + 1] - rho;
-          const float2 F = make_float2(ex2(L0), ex2(L1));                  // e^{Gamma - rho}
-          const float2 Fi = make_float2(ex2(-L0), ex2(-L1));               // e^{rho - Gamma}
-          const float2 eG = make_float2(ex2(Gm[i]), ex2(Gm[i + 1]));       // e^{Gamma}
-          const float2 eH = make_float2(ex2(gL - Gm[i]), ex2(gL - Gm[i + 1]));  // e^{Gamma_L - Gamma}
-          const float2 k2 = make_float2(kv[i], kv[i + 1]);
-          const float2 q2 = make_float2(qv[i], qv[i + 1]);
-          const float2 xk2 = mul2(k2, F), xq2 = mul2(q2, F), y2 = mul2(k2, Fi);
-          const float2 kg2 = mul2(k2, eG), qg2 = mul2(q2, eG), kh2 = mul2(k2, eH);
-          float2 yb2 = y2;
-          if (first)  // e^{rho_B - Gamma}
-            yb2 = mul2(k2, make_float2(ex2(rhoB - Gm[i]), ex2(rhoB - Gm[i + 1])));
-          xk[e] = xk2.x; xk[e + 1] = xk2.y;
-          xq[e] = xq2.x; xq[e + 1] = xq2.y;
-          y[e] = y2.x; y[e + 1] = y2.y;
-          yb[e] = yb2.x; yb[e + 1] = yb2.y;
-          kg[e] = kg2.x; kg[e + 1] = kg2.y;
-          qg[e] = qg2.x; qg[e + 1] = qg2.y;
-          kh[e] = kh2.x; kh[e + 1] = kh2.y;
-        }
-        const uint32_t r0 = 16 * R + 8 * gi;  // first token of these 8 rows
-        const uint32_t o = sw128_off(c, r0);
-        st_pack8(sb + XK + o, xk);
-        st_pack8(sb + XQ + o, xq);
-        st_pack8(sb + KG + o, kg);
-        st_pack8(sb + QG + o, qg);
-        st_pack8(sb + KH + o, kh);
-        if (first) {
-          st_pack8(sb + YP + 16384u + o, y);  // Y_A (panel 1, columns 64 + r)
-          st_pack8(sb + YP + o, yb);           // Y_B (panel 0)
-        } else {
-          st_pack8(sb + YP + o, y);            // Y_B
-        }
-      }
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (blk + 1 < nblocks) {  // the k, q and g tiles are dead
-      if (tid == 0) issue_in(blk + 1);
+  if (isP) {
+    // =====================================================================  group P
+    const unsigned short* __restrict__ beta_u = static_cast<const unsigned short*>(P.beta);
+    auto issue_in = [&](int b) {
+      const int row = (int)(row0 + (size_t)b * C);
+      mbar_arrive_expect_tx(&bar_in, 6 * BOX_BYTES);
+      load2(IN_K, &maps.k, row, &bar_in);
+      load2(IN_Q, &maps.q, row, &bar_in);
+      load2(IN_G, &maps.g, row, &bar_in);
+    };
+    bool pend_in = false;
+    int in_blk = 0, d_blk = -1;  // block of the last input load / A/P product issued
+    if (nblocks > 0) {
+      if (lt == 0) issue_in(0);
       pend_in = true;
     }
-    // ---------------- tcgen05: D = X [Y_B | Y_A]^T ; [Z^T | O^T] = S^T [(K e^Gamma)^T | (Q e^Gamma)^T]
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t id_d = idesc_bf16(128, 96, 1, 1, 0);
-      const uint32_t id_z = idesc_bf16(128, 128, 0, 1, 0);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        umma_bf16(tmem + T_D, desc_sw128(sb + XK + 2048u * kk, 16384, 1024),
-                  desc_sw128(sb + YP + 2048u * kk, 16384, 1024), id_d, kk > 0);
-        umma_bf16_tmem_a(tmem + T_ZT, tmem + T_SB + 8u * kk,
-                         desc_sw128(sb + KG + 2048u * kk, QG - KG, 1024), id_z, kk > 0);
+    // beta of the next block is loaded one block ahead, kept as raw bits so that nothing waits
+    // on the load until the block that needs it
+    unsigned short beta_next = 0;
+    if (lt < C && lt < len) beta_next = beta_u[(row0 + lt) * H + h];
+
+    for (int blk = 0; blk < nblocks; ++blk) {
+      const int t0 = blk * C;
+      const int n = min(C, len - t0);
+      const int par = blk & 1;
+      // S has started the previous block (its first product read (K/Q e^Gamma)^T and the
+      // per-parity arrays of two blocks ago are no longer read) and the previous A/P product
+      // has released X and Y.
+      if (blk > 0 && !group_wait2(&bar_ZO, (blk - 1) & 1, &bar_D, (blk - 1) & 1, BAR_P)) {
+        aborted = true;
+        break;
       }
-      umma_commit(&bar_mma);
-    }
-    pend_mma = true;
-    // ---------------- meanwhile: S^T <- S^T Diag(e^{Gamma_L}) (the products above read the
-    // bf16 copy; Khat^T U accumulates onto this one)
-    {
-      uint32_t v[32];
-      {
-        const int c0 = 32 * qq;
-        tmem_ld32(tl + T_ST + c0, v);
-        tmem_ld_wait();
+      if (lt < C) {
+        beta_s[par][lt] = __uint_as_float((uint32_t)beta_next << 16);  // zero past the end
+        beta_next = 0;
+        if (lt < len - t0 - C) beta_next = beta_u[(row0 + t0 + C + lt) * H + h];
+      }
+      if (!group_wait2(&bar_in, blk & 1, nullptr, 0, BAR_P)) { aborted = true; break; }
+      pend_in = false;
+      // ---------------- sums of g (log2 domain) over this thread's sub-blocks hh and 2 + hh
+      const uint8_t* gp = sm + IN_G + (c >> 6) * BOX_BYTES;
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const float4 gv = *reinterpret_cast<const float4*>(gl_s + c0 + j);
-          const float2 a0 = mul2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])),
-                                 make_float2(gv.x, gv.y));
-          const float2 a1 = mul2(make_float2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])),
-                                 make_float2(gv.z, gv.w));
-          v[j] = __float_as_uint(a0.x); v[j + 1] = __float_as_uint(a0.y);
-          v[j + 2] = __float_as_uint(a1.x); v[j + 3] = __float_as_uint(a1.y);
+      for (int a = 0; a < 2; ++a) {
+        float gv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) gv[i] = ld_bf16(gp, sw128_off(16 * (2 * a + hh) + i, c & 63));
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          acc0 += 16 * (2 * a + hh) + i < n ? gv[i] : 0.f;
+          acc1 += 16 * (2 * a + hh) + i + 1 < n ? gv[i + 1] : 0.f;
         }
-        tmem_st32(tl + T_ST + c0, v);
+        xch[2 * a + hh][c] = (acc0 + acc1) * LOG2E;
+      }
+      named_sync(BAR_P, GROUP);
+      const float s0 = xch[0][c], s1 = xch[1][c], s2 = xch[2][c], s3 = xch[3][c];
+      const float rhoA = s0, b2 = s0 + s1, rhoB = b2 + s2, gL = rhoB + s3;
+      if (hh == 0) gl_s[par][c] = ex2(gL);
+      // ---------------- operands: X, Y, (K e^Gamma)^T, (Q e^Gamma)^T; Khat^T kept packed
+      uint32_t khA[8], khB[8];  // Khat^T of sub-blocks hh and 2 + hh, bf16 pairs
+      {
+        const uint8_t* kp = sm + IN_K + (c >> 6) * BOX_BYTES;
+        const uint8_t* qp = sm + IN_Q + (c >> 6) * BOX_BYTES;
+#pragma unroll 1
+        for (int a = 0; a < 2; ++a) {
+          const int R = 2 * a + hh;  // a = 0: first half (reference rho_A), a = 1: second
+          const float rho = a == 0 ? rhoA : rhoB;
+          float acc = a == 0 ? (hh ? s0 : 0.f) : (hh ? rhoB : b2);  // Gamma before the sub-block
+#pragma unroll
+          for (int gi = 0; gi < 2; ++gi) {
+            const int r0 = 16 * R + 8 * gi;  // first token of these 8 rows
+            float G[8], kv[8], qv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const uint32_t o = sw128_off(r0 + e, c & 63);
+              G[e] = ld_bf16(gp, o);
+              kv[e] = ld_bf16(kp, o);
+              qv[e] = ld_bf16(qp, o);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const bool live = r0 + e < n;
+              acc = fmaf(live ? G[e] : 0.f, LOG2E, acc);
+              G[e] = acc;
+              kv[e] = live ? kv[e] : 0.f;
+              qv[e] = live ? qv[e] : 0.f;
+            }
+            uint32_t xk[4], xq[4], y[4], yb[4], kg[4], qg[4];  // bf16 pairs
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const float G0 = G[2 * w], G1 = G[2 * w + 1];
+              const float L0 = G0 - rho, L1 = G1 - rho;
+              const float2 F = make_float2(ex2(L0), ex2(L1));               // e^{Gamma - rho}
+              const float2 Fi = make_float2(ex2(-L0), ex2(-L1));            // e^{rho - Gamma}
+              const float2 eG = make_float2(ex2(G0), ex2(G1));              // e^{Gamma}
+              const float2 eH = make_float2(ex2(gL - G0), ex2(gL - G1));    // e^{Gamma_L - Gamma}
+              const float2 eYB = make_float2(ex2(rhoB - G0), ex2(rhoB - G1));  // e^{rho_B - Gamma}
+              const float2 k2 = make_float2(kv[2 * w], kv[2 * w + 1]);
+              const float2 q2 = make_float2(qv[2 * w], qv[2 * w + 1]);
+              const float2 xk2 = mul2(k2, F), xq2 = mul2(q2, F), y2 = mul2(k2, Fi);
+              const float2 kg2 = mul2(k2, eG), qg2 = mul2(q2, eG), kh2 = mul2(k2, eH);
+              const float2 yb2 = mul2(k2, eYB);
+              xk[w] = pack_bf16(xk2.x, xk2.y);
+              xq[w] = pack_bf16(xq2.x, xq2.y);
+              y[w] = pack_bf16(y2.x, y2.y);
+              yb[w] = pack_bf16(yb2.x, yb2.y);
+              kg[w] = pack_bf16(kg2.x, kg2.y);
+              qg[w] = pack_bf16(qg2.x, qg2.y);
+              const uint32_t khw = pack_bf16(kh2.x, kh2.y);
+              if (a == 0) khA[4 * gi + w] = khw;
+              else khB[4 * gi + w] = khw;
+            }
+            const uint32_t o = sw128_off(c, r0);
+            st_words4(sb + XK + o, xk);
+            st_words4(sb + XQ + o, xq);
+            st_words4(sb + KG + o, kg);
+            st_words4(sb + QG + o, qg);
+            if (a == 0) {
+              st_words4(sb + YP + 16384u + o, y);  // Y_A (panel 1, columns 64 + r)
+              st_words4(sb + YP + o, yb);           // Y_B (panel 0)
+            } else {
+              st_words4(sb + YP + o, y);            // Y_B (here e^{rho - Gamma} = e^{rho_B - Gamma})
+            }
+          }
+        }
+      }
+      // ---------------- Khat^T: wait until S's last product of the previous block has read it
+      if (blk > 0 && !group_wait2(&bar_G3, (blk - 1) & 1, nullptr, 0, BAR_P)) {
+        aborted = true;
+        break;
+      }
+      {
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int gi = 0; gi < 2; ++gi) {
+            const uint32_t* kw = a == 0 ? khA : khB;
+            st_shared_v4(sb + KH + sw128_off(c, 16 * (2 * a + hh) + 8 * gi), kw[4 * gi],
+                         kw[4 * gi + 1], kw[4 * gi + 2], kw[4 * gi + 3]);
+          }
+      }
+      fence_proxy_async_smem();
+      named_sync(BAR_P, GROUP);
+      if (lt == 0) {
+        if (blk + 1 < nblocks) issue_in(blk + 1);  // the k, q and g tiles are dead
+        mbar_arrive(&bar_prep);
+        // ---------------- tcgen05: D = X [Y_B | Y_A]^T (M 128, N 96, K 128); S's extraction of
+        // the previous block's D finished before its last product, awaited above
+        tc_fence_after();
+        const uint32_t id_d = idesc_bf16(128, 96, 1, 1, 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16(tmem + T_D, desc_sw128(sb + XK + 2048u * kk, 16384, 1024),
+                    desc_sw128(sb + YP + 2048u * kk, 16384, 1024), id_d, kk > 0);
+        umma_commit(&bar_D);
+      }
+      if (blk + 1 < nblocks) {
+        pend_in = true;
+        in_blk = blk + 1;
+      }
+      d_blk = blk;
+    }
+    if (aborted) record_status(4u /* KDA_ERR_TIMEOUT */);
+    if (lt == 0) {  // let anything already issued land before the CTA's memory goes away
+      if (aborted && pend_in) (void)mbar_wait(&bar_in, in_blk & 1);
+      if (d_blk >= 0) (void)mbar_wait(&bar_D, d_blk & 1);
+    }
+  } else {
+    // =====================================================================  group S
+    const bool leader = lt == 0;
+    __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(P.out);
+    auto issue_v = [&](int b) {
+      mbar_arrive_expect_tx(&bar_v, 2 * BOX_BYTES);
+      load2(IN_V, &maps.v, (int)(row0 + (size_t)b * C), &bar_v);
+    };
+    // ---- initial state S^T: lane v = c, key channels 64 hh .. 64 hh + 63 (coalesced over v)
+    {
+      const float* s0 = P.S0 ? P.S0 + (size_t)p * D * D + c : nullptr;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sv[32], sbf[16];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          sv[j] = s0 ? __float_as_uint(s0[(size_t)(64 * hh + 32 * half + j) * D]) : 0u;
+        tmem_st32(tl + T_ST + 64 * hh + 32 * half, sv);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) sbf[j] = pack_bf16(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]));
+        tmem_st16(tl + T_SB + 32 * hh + 16 * half, sbf);
       }
       tmem_st_wait();
       tc_fence_before();
     }
-    if (__syncthreads_or(!mma_done())) { aborted = true; break; }
-    // ---------------- A (fp32, into WS) and P (bf16, into PT) out of TMEM; Z^T -> bf16
-    // Lane m: rows 0..63 are the k side (A), 64..127 the q side (P); row r = m & 63 reads the
-    // Y_A columns in the first half of the block, the Y_B columns in the second (warp-uniform).
-    // This thread covers columns j in [16 q, +16).
-    {
-      float* ws = reinterpret_cast<float*>(sm + WS);
-      const int r = c & 63;
-      const bool pside = c >= 64;
-      const bool firsthalf = (quarter & 1) == 0;
-      float vals[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) vals[j] = 0.f;
-      if (!firsthalf || qq < 2) {  // the first half has columns j < 32 only
-        uint32_t v[16];
-        tmem_ld16(tl + T_D + (uint32_t)((firsthalf ? Y_A : 0) + 16 * qq), v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) vals[j] = __uint_as_float(v[j]);
-      }
-      if (!pside) {
-        const float b = beta_s[r];
-#pragma unroll
-        for (int j4 = 0; j4 < 4; ++j4) {
-          float4 x;
-          const int j = 16 * qq + 4 * j4;
-          x.x = (j < r) ? b * vals[4 * j4] : 0.f;
-          x.y = (j + 1 < r) ? b * vals[4 * j4 + 1] : 0.f;
-          x.z = (j + 2 < r) ? b * vals[4 * j4 + 2] : 0.f;
-          x.w = (j + 3 < r) ? b * vals[4 * j4 + 3] : 0.f;
-          *reinterpret_cast<float4*>(ws + r * WLD + j) = x;
-        }
-      } else {
-#pragma unroll
-        for (int j8 = 0; j8 < 2; ++j8) {
-          float x[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = 16 * qq + 8 * j8 + e;
-            x[e] = (j <= r) ? vals[8 * j8 + e] : 0.f;
-          }
-          st_pack8(sb + PT + sw128_off(r, 16 * qq + 8 * j8), x);
-        }
-      }
-      // Z^T (lane v = c, tokens 16 q ..) -> bf16 A operand
-      uint32_t v[16], zb[8];
-      tmem_ld16(tl + T_ZT + 16 * qq, v);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 8; ++j) zb[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-      tmem_st8(tl + T_ZB + 8 * qq, zb);
-    }
-    __syncthreads();
-    // ---------------- T = (I + A)^{-1} (unit lower triangular), in place in WS
-    {
-      float* ws = reinterpret_cast<float*>(sm + WS);
-      float* mb = reinterpret_cast<float*>(sm + TB);
-      // (1) diagonal 16 x 16 blocks T_RR by forward substitution, one column per thread; the
-      // result goes to trr so that A_RR stays readable until every column is done
-      float x[16];
-      const int Rd = tid >> 4, jj = tid & 15;
-      if (tid < 64) {
-        const float* bp = ws + 16 * Rd * (WLD + 1);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float arow[16];
-#pragma unroll
-          for (int m4 = 0; m4 < 4; ++m4) {
-            const float4 v4 = *reinterpret_cast<const float4*>(bp + i * WLD + 4 * m4);
-            arow[4 * m4] = v4.x; arow[4 * m4 + 1] = v4.y; arow[4 * m4 + 2] = v4.z; arow[4 * m4 + 3] = v4.w;
-          }
-          float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-          for (int m = 0; m < i; ++m) {
-            if (m & 1) acc1 = fmaf(arow[m], x[m], acc1);
-            else acc0 = fmaf(arow[m], x[m], acc0);
-          }
-          x[i] = (i == jj) ? 1.f : (i > jj ? -(acc0 + acc1) : 0.f);
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) trr[Rd][i][jj] = x[i];
-      }
-      __syncthreads();
-      // (2) M_R = -T_RR A_{R,<16R} for R = 1..3 (independent): 12 tiles of 16 x 8, two k steps.
-      // Meanwhile the diagonal blocks of WS receive T_RR.
-      if (tid < 64) {
-        float* cp = ws + 16 * Rd * (WLD + 1) + jj;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) cp[i * WLD] = x[i];
-      }
-      for (int tile = warp; tile < 12; tile += THREADS / 32) {
-        const int R = tile < 2 ? 1 : (tile < 6 ? 2 : 3);
-        const int nt = tile - (R == 1 ? 0 : (R == 2 ? 2 : 6));
-        const float* ar = ws + 16 * R * WLD + 8 * nt;
-        float acc[3][4] = {};
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          const float a[4] = {trr[R][g][8 * ks + t], trr[R][g + 8][8 * ks + t],
-                              trr[R][g][8 * ks + t + 4], trr[R][g + 8][8 * ks + t + 4]};
-          const float b[2] = {ar[(8 * ks + t) * WLD + g], ar[(8 * ks + t + 4) * WLD + g]};
-          mma_3xtf32_split(acc, a, b);
-        }
-        const int ld = 16 * R + 4;
-        float* mo = mb + mb_off(R) + 8 * nt;
-        *reinterpret_cast<float2*>(mo + g * ld + 2 * t) =
-            make_float2(-(acc[0][0] + acc[1][0] + acc[2][0]), -(acc[0][1] + acc[1][1] + acc[2][1]));
-        *reinterpret_cast<float2*>(mo + (g + 8) * ld + 2 * t) =
-            make_float2(-(acc[0][2] + acc[1][2] + acc[2][2]), -(acc[0][3] + acc[1][3] + acc[2][3]));
-      }
-      __syncthreads();
-      // (3) block rows in order: T_{R,<16R} = M_R T_{<16R,<16R}; T is zero above its diagonal,
-      // so k steps above the output tile's columns are skipped
-#pragma unroll
-      for (int R = 1; R < 4; ++R) {
-        const int ld = 16 * R + 4;
-        const float* mr = mb + mb_off(R);
-        if (warp < 2 * R) {
-          const int nt = warp;
-          float acc[3][4] = {};
-#pragma unroll
-          for (int ks = 0; ks < 2 * R; ++ks) {
-            if (ks < nt) continue;
-            const float a[4] = {mr[g * ld + 8 * ks + t], mr[(g + 8) * ld + 8 * ks + t],
-                                mr[g * ld + 8 * ks + t + 4], mr[(g + 8) * ld + 8 * ks + t + 4]};
-            const float b[2] = {ws[(8 * ks + t) * WLD + 8 * nt + g],
-                                ws[(8 * ks + t + 4) * WLD + 8 * nt + g]};
-            mma_3xtf32_split(acc, a, b);
-          }
-          float* to = ws + 16 * R * WLD + 8 * nt;
-          *reinterpret_cast<float2*>(to + g * WLD + 2 * t) =
-              make_float2(acc[0][0] + acc[1][0] + acc[2][0], acc[0][1] + acc[1][1] + acc[2][1]);
-          *reinterpret_cast<float2*>(to + (g + 8) * WLD + 2 * t) =
-              make_float2(acc[0][2] + acc[1][2] + acc[2][2], acc[0][3] + acc[1][3] + acc[2][3]);
-        }
-        __syncthreads();
-      }
-      // (4) T Diag(beta) -> bf16, K-major [r][j]
-      {
-        const int r = tid >> 3, j0 = (tid & 7) * 8;
-        float y[8];
-#pragma unroll
-        for (int e4 = 0; e4 < 2; ++e4) {
-          const float4 v4 = *reinterpret_cast<const float4*>(ws + r * WLD + j0 + 4 * e4);
-          const float4 b4 = *reinterpret_cast<const float4*>(beta_s + j0 + 4 * e4);
-          y[4 * e4] = v4.x * b4.x; y[4 * e4 + 1] = v4.y * b4.y;
-          y[4 * e4 + 2] = v4.z * b4.z; y[4 * e4 + 3] = v4.w * b4.w;
-        }
-        st_pack8(sb + TB + sw128_off(r, j0), y);
-      }
-    }
-    fence_proxy_async_smem();
-    tmem_st_wait();
-    tc_fence_before();
-    {
-      const bool ok = mbar_wait(&bar_v, ph_v);
-      if (ok) ph_v ^= 1u;
-      pend_v = !ok;
-      if (__syncthreads_or(!ok)) { aborted = true; break; }
-    }
-    // ---------------- tcgen05: U^T = V^T (T Diag beta)^T - Z^T (T Diag beta)^T  (M 128, N 64, K 64)
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t id_v = idesc_bf16(128, 64, 1, 0, 0);
-      const uint32_t id_z = idesc_bf16(128, 64, 0, 0, 1);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t b = desc_sw128(sb + TB + 32u * kk, 16, 1024);
-        umma_bf16(tmem + T_UT, desc_sw128(sb + IN_V + 2048u * kk, BOX_BYTES, 1024), b, id_v, kk > 0);
-        umma_bf16_tmem_a(tmem + T_UT, tmem + T_ZB + 8u * kk, b, id_z, 1);
-      }
-      umma_commit(&bar_mma);
-    }
-    pend_mma = true;
-    if (tid == 0) bulk_wait_read();  // the previous block's O store has left the staging tiles
-    if (__syncthreads_or(!mma_done())) { aborted = true; break; }
-    if (blk + 1 < nblocks) {  // the v tile is dead
-      if (tid == 0) issue_v(blk + 1);
+    bool pend_v = false, pend_mma = false;
+    int v_blk = 0;  // block of the last v load issued
+    uint64_t* last_mma = &bar_ZO;
+    uint32_t last_par = 0;
+    if (nblocks > 0) {
+      if (leader) issue_v(0);
       pend_v = true;
     }
-    // ---------------- U^T -> bf16 A operand
-    {
-      uint32_t v[16], ub[8];
-      tmem_ld16(tl + T_UT + 16 * qq, v);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 8; ++j) ub[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-      tmem_st8(tl + T_UB + 8 * qq, ub);
-      tmem_st_wait();
-    }
-    tc_fence_before();
-    __syncthreads();
-    // ---------------- tcgen05: O^T += U^T P^T (N 64) ; S^T += U^T Khat (N 128), K 64
-    if (tid == 0) {
+    named_sync(BAR_S, GROUP);
+
+    for (int blk = 0; blk < nblocks; ++blk) {
+      const int t0 = blk * C;
+      const int n = min(C, len - t0);
+      const int par = blk & 1;
+      const uint32_t ph = (uint32_t)par;
+      if (!group_wait2(&bar_prep, ph, &bar_D, ph, BAR_S)) { aborted = true; break; }
       tc_fence_after();
-      const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
-      const uint32_t id_s = idesc_bf16(128, 128, 0, 0, 0);
+      // ---------------- tcgen05: [Z^T | O^T] = S^T [(K e^Gamma)^T | (Q e^Gamma)^T] (N 128, K 128)
+      if (leader) {
+        tc_fence_after();
+        const uint32_t id_z = idesc_bf16(128, 128, 0, 1, 0);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        umma_bf16_tmem_a(tmem + T_OT, tmem + T_UB + 8u * kk, desc_sw128(sb + PT + 32u * kk, 16, 1024),
-                         id_o, 1);
-        umma_bf16_tmem_a(tmem + T_ST, tmem + T_UB + 8u * kk, desc_sw128(sb + KH + 32u * kk, 16, 1024),
-                         id_s, 1);
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_tmem_a(tmem + T_ZT, tmem + T_SB + 8u * kk,
+                           desc_sw128(sb + KG + 2048u * kk, QG - KG, 1024), id_z, kk > 0);
+        umma_commit(&bar_ZO);
       }
-      umma_commit(&bar_mma);
-    }
-    pend_mma = true;
-    if (__syncthreads_or(!mma_done())) { aborted = true; break; }
-    // ---------------- outputs; bf16 copy of the new state for the next block
-    {
-      uint32_t v[32];
-      tmem_ld16(tl + T_OT + 16 * qq, *reinterpret_cast<uint32_t(*)[16]>(v));
-      tmem_ld_wait();
-      if (n == C) {  // full block: stage [token][channel] boxes for one TMA store
-        uint8_t* ob = sm + OS + (c >> 6) * BOX_BYTES;
+      pend_mma = true; last_mma = &bar_ZO; last_par = ph;
+      // ---------------- meanwhile: S^T <- S^T Diag(e^{Gamma_L}) (the product above reads the
+      // bf16 copy; Khat^T U accumulates onto this one)
+      {
+        uint32_t v[32];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          *reinterpret_cast<__nv_bfloat16*>(ob + sw128_off(16 * qq + j, c & 63)) =
-              __float2bfloat16_rn(__uint_as_float(v[j]));
-      } else {  // partial last block: plain stores of the valid rows only
-        __nv_bfloat16* op = out + ((row0 + t0) * H + h) * D + c;
+        for (int half = 0; half < 2; ++half) {
+          const int c0 = 64 * hh + 32 * half;
+          tmem_ld32(tl + T_ST + c0, v);
+          tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = 16 * qq + j;
-          if (r < n) op[(size_t)r * H * D] = __float2bfloat16_rn(__uint_as_float(v[j]));
+          for (int j = 0; j < 32; j += 4) {
+            const float4 gv = *reinterpret_cast<const float4*>(&gl_s[par][c0 + j]);
+            const float2 a0 = mul2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])),
+                                   make_float2(gv.x, gv.y));
+            const float2 a1 = mul2(make_float2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])),
+                                   make_float2(gv.z, gv.w));
+            v[j] = __float_as_uint(a0.x); v[j + 1] = __float_as_uint(a0.y);
+            v[j + 2] = __float_as_uint(a1.x); v[j + 3] = __float_as_uint(a1.y);
+          }
+          tmem_st32(tl + T_ST + c0, v);
         }
       }
-      uint32_t sbf[16];
-      tmem_ld32(tl + T_ST + 32 * qq, v);
-      tmem_ld_wait();
+      // ---------------- A (fp32, into WS) and P (bf16, into PT) out of TMEM
+      // Lane m: rows 0..63 are the k side (A), 64..127 the q side (P); row r = m & 63 reads the
+      // Y_A columns in the first half of the block, the Y_B columns in the second (warp-uniform).
+      // This thread covers columns j in [32 hh, +32).
+      {
+        float* ws = reinterpret_cast<float*>(sm + WS);
+        const int r = c & 63;
+        const bool pside = c >= 64;
+        const bool firsthalf = (quarter & 1) == 0;
+        const float b = beta_s[par][r];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) sbf[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-      tmem_st16(tl + T_SB + 16 * qq, sbf);
+        for (int part = 0; part < 2; ++part) {
+          const int j0 = 32 * hh + 16 * part;  // columns j0 .. j0 + 15
+          float vals[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) vals[j] = 0.f;
+          if (!firsthalf || hh == 0) {  // the first half has columns j < 32 only
+            uint32_t v[16];
+            tmem_ld16(tl + T_D + (uint32_t)(firsthalf ? Y_A + 16 * part : j0), v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) vals[j] = __uint_as_float(v[j]);
+          }
+          if (!pside) {
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4) {
+              float4 x;
+              const int j = j0 + 4 * j4;
+              x.x = (j < r) ? b * vals[4 * j4] : 0.f;
+              x.y = (j + 1 < r) ? b * vals[4 * j4 + 1] : 0.f;
+              x.z = (j + 2 < r) ? b * vals[4 * j4 + 2] : 0.f;
+              x.w = (j + 3 < r) ? b * vals[4 * j4 + 3] : 0.f;
+              *reinterpret_cast<float4*>(ws + r * WLD + j) = x;
+            }
+          } else {
+#pragma unroll
+            for (int j8 = 0; j8 < 2; ++j8) {
+              float x[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int j = j0 + 8 * j8 + e;
+                x[e] = (j <= r) ? vals[8 * j8 + e] : 0.f;
+              }
+              st_pack8(sb + PT + sw128_off(r, j0 + 8 * j8), x);
+            }
+          }
+        }
+      }
+      // ---------------- Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand
+      // (the group wait also orders the A / P stores above before the solve below)
+      if (!group_wait2(&bar_ZO, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
+      pend_mma = false;
+      tc_fence_after();
+      {
+        uint32_t v[32], zb[16];
+        tmem_ld32(tl + T_ZT + 32 * hh, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) zb[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+        tmem_st16(tl + T_ZB + 16 * hh, zb);
+      }
+      // ---------------- T = (I + A)^{-1} (unit lower triangular), in place in WS
+      {
+        float* ws = reinterpret_cast<float*>(sm + WS);
+        float* mb = reinterpret_cast<float*>(sm + TB);
+        const int sw = warp - GROUP / 32;  // warp index inside the group
+        // (1) diagonal 16 x 16 blocks T_RR by forward substitution, one column per thread; the
+        // result goes to trr so that A_RR stays readable until every column is done
+        float x[16];
+        const int Rd = lt >> 4, jj = lt & 15;
+        if (lt < 64) {
+          const float* bp = ws + 16 * Rd * (WLD + 1);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float arow[16];
+#pragma unroll
+            for (int m4 = 0; m4 < 4; ++m4) {
+              const float4 v4 = *reinterpret_cast<const float4*>(bp + i * WLD + 4 * m4);
+              arow[4 * m4] = v4.x; arow[4 * m4 + 1] = v4.y; arow[4 * m4 + 2] = v4.z; arow[4 * m4 + 3] = v4.w;
+            }
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < i; ++m) {
+              if (m & 1) acc1 = fmaf(arow[m], x[m], acc1);
+              else acc0 = fmaf(arow[m], x[m], acc0);
+            }
+            x[i] = (i == jj) ? 1.f : (i > jj ? -(acc0 + acc1) : 0.f);
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) trr[Rd][i][jj] = x[i];
+        }
+        named_sync(BAR_S, GROUP);
+        // (2) M_R = -T_RR A_{R,<16R} for R = 1..3 (independent): 12 tiles of 16 x 8, two k
+        // steps. Meanwhile the diagonal blocks of WS receive T_RR.
+        if (lt < 64) {
+          float* cp = ws + 16 * Rd * (WLD + 1) + jj;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) cp[i * WLD] = x[i];
+        }
+        for (int tile = sw; tile < 12; tile += GROUP / 32) {
+          const int R = tile < 2 ? 1 : (tile < 6 ? 2 : 3);
+          const int nt = tile - (R == 1 ? 0 : (R == 2 ? 2 : 6));
+          const float* ar = ws + 16 * R * WLD + 8 * nt;
+          float acc[3][4] = {};
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            const float a[4] = {trr[R][g][8 * ks + t], trr[R][g + 8][8 * ks + t],
+                                trr[R][g][8 * ks + t + 4], trr[R][g + 8][8 * ks + t + 4]};
+            const float b[2] = {ar[(8 * ks + t) * WLD + g], ar[(8 * ks + t + 4) * WLD + g]};
+            mma_3xtf32_split(acc, a, b);
+          }
+          const int ld = 16 * R + 4;
+          float* mo = mb + mb_off(R) + 8 * nt;
+          *reinterpret_cast<float2*>(mo + g * ld + 2 * t) =
+              make_float2(-(acc[0][0] + acc[1][0] + acc[2][0]), -(acc[0][1] + acc[1][1] + acc[2][1]));
+          *reinterpret_cast<float2*>(mo + (g + 8) * ld + 2 * t) =
+              make_float2(-(acc[0][2] + acc[1][2] + acc[2][2]), -(acc[0][3] + acc[1][3] + acc[2][3]));
+        }
+        named_sync(BAR_S, GROUP);
+        // (3) block rows in order: T_{R,<16R} = M_R T_{<16R,<16R}; T is zero above its
+        // diagonal, so k steps above the output tile's columns are skipped
+#pragma unroll
+        for (int R = 1; R < 4; ++R) {
+          const int ld = 16 * R + 4;
+          const float* mr = mb + mb_off(R);
+          if (sw < 2 * R) {
+            const int nt = sw;
+            float acc[3][4] = {};
+#pragma unroll
+            for (int ks = 0; ks < 2 * R; ++ks) {
+              if (ks < nt) continue;
+              const float a[4] = {mr[g * ld + 8 * ks + t], mr[(g + 8) * ld + 8 * ks + t],
+                                  mr[g * ld + 8 * ks + t + 4], mr[(g + 8) * ld + 8 * ks + t + 4]};
+              const float b[2] = {ws[(8 * ks + t) * WLD + 8 * nt + g],
+                                  ws[(8 * ks + t + 4) * WLD + 8 * nt + g]};
+              mma_3xtf32_split(acc, a, b);
+            }
+            float* to = ws + 16 * R * WLD + 8 * nt;
+            *reinterpret_cast<float2*>(to + g * WLD + 2 * t) =
+                make_float2(acc[0][0] + acc[1][0] + acc[2][0], acc[0][1] + acc[1][1] + acc[2][1]);
+            *reinterpret_cast<float2*>(to + (g + 8) * WLD + 2 * t) =
+                make_float2(acc[0][2] + acc[1][2] + acc[2][2], acc[0][3] + acc[1][3] + acc[2][3]);
+          }
+          named_sync(BAR_S, GROUP);
+        }
+        // (4) T Diag(beta) -> bf16, K-major [r][j]
+        {
+          const int r = lt >> 2, j0 = (lt & 3) * 16;
+          float y[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 v4 = *reinterpret_cast<const float4*>(ws + r * WLD + j0 + 4 * e4);
+            const float4 b4 = *reinterpret_cast<const float4*>(&beta_s[par][j0 + 4 * e4]);
+            y[4 * e4] = v4.x * b4.x; y[4 * e4 + 1] = v4.y * b4.y;
+            y[4 * e4 + 2] = v4.z * b4.z; y[4 * e4 + 3] = v4.w * b4.w;
+          }
+          st_shared_v4(sb + TB + sw128_off(r, j0), pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
+                       pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+          st_shared_v4(sb + TB + sw128_off(r, j0 + 8), pack_bf16(y[8], y[9]), pack_bf16(y[10], y[11]),
+                       pack_bf16(y[12], y[13]), pack_bf16(y[14], y[15]));
+        }
+      }
+      fence_proxy_async_smem();
       tmem_st_wait();
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (n == C && tid == 0) {
-      tma_store_3d(&maps.o, sm + OS, 0, h, (int)(row0 + t0));
-      tma_store_3d(&maps.o, sm + OS + BOX_BYTES, 64, h, (int)(row0 + t0));
-      bulk_commit();
-    }
-  }
-  if (tid == 0) bulk_wait_all();
-
-  if (aborted) {
-    record_status(4u /* KDA_ERR_TIMEOUT */);
-    if (tid == 0) {  // let anything already issued land before the CTA's memory goes away
-      if (pend_mma) (void)mbar_wait(&bar_mma, ph_mma);
-      if (pend_in) (void)mbar_wait(&bar_in, ph_in);
-      if (pend_v) (void)mbar_wait(&bar_v, ph_v);
-    }
-  } else if (P.S_final) {  // S_final[c'][v] from S^T (lane v): coalesced over v
-    float* sf = P.S_final + (size_t)p * D * D + c;
-    uint32_t v[32];
-    tmem_ld32(tl + T_ST + 32 * qq, v);
-    tmem_ld_wait();
+      tc_fence_before();
+      if (!group_wait2(&bar_v, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
+      pend_v = false;
+      // ---------------- tcgen05: U^T = V^T (T Diag beta)^T - Z^T (T Diag beta)^T (N 64, K 64)
+      if (leader) {
+        tc_fence_after();
+        const uint32_t id_v = idesc_bf16(128, 64, 1, 0, 0);
+        const uint32_t id_z = idesc_bf16(128, 64, 0, 0, 1);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) sf[(size_t)(32 * qq + j) * D] = __uint_as_float(v[j]);
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t b = desc_sw128(sb + TB + 32u * kk, 16, 1024);
+          umma_bf16(tmem + T_UT, desc_sw128(sb + IN_V + 2048u * kk, BOX_BYTES, 1024), b, id_v, kk > 0);
+          umma_bf16_tmem_a(tmem + T_UT, tmem + T_ZB + 8u * kk, b, id_z, 1);
+        }
+        umma_commit(&bar_G2);
+      }
+      pend_mma = true; last_mma = &bar_G2; last_par = ph;
+      if (!group_wait2(&bar_G2, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
+      pend_mma = false;
+      tc_fence_after();
+      if (blk + 1 < nblocks) {  // the v tile is dead
+        if (leader) issue_v(blk + 1);
+        pend_v = true;
+        v_blk = blk + 1;
+      }
+      // ---------------- U^T -> bf16 A operand (into the Z^T bf16 columns, read by now)
+      {
+        uint32_t v[32], ub[16];
+        tmem_ld32(tl + T_UT + 32 * hh, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ub[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+        tmem_st16(tl + T_UB + 16 * hh, ub);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      named_sync(BAR_S, GROUP);
+      // ---------------- tcgen05: O^T += U^T P^T (N 64) ; S^T += U^T Khat (N 128), K 64
+      if (leader) {
+        tc_fence_after();
+        const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
+        const uint32_t id_s = idesc_bf16(128, 128, 0, 0, 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          umma_bf16_tmem_a(tmem + T_OT, tmem + T_UB + 8u * kk,
+                           desc_sw128(sb + PT + 32u * kk, 16, 1024), id_o, 1);
+          umma_bf16_tmem_a(tmem + T_ST, tmem + T_UB + 8u * kk,
+                           desc_sw128(sb + KH + 32u * kk, 16, 1024), id_s, 1);
+        }
+        umma_commit(&bar_G3);
+      }
+      pend_mma = true; last_mma = &bar_G3; last_par = ph;
+      if (!group_wait2(&bar_G3, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
+      pend_mma = false;
+      tc_fence_after();
+      // ---------------- outputs; bf16 copy of the new state for the next block
+      {
+        __nv_bfloat16* op = out + ((row0 + t0) * H + h) * D + c;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          uint32_t v[16];
+          tmem_ld16(tl + T_OT + 32 * hh + 16 * part, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int r = 32 * hh + 16 * part + j;
+            if (r < n) op[(size_t)r * H * D] = __float2bfloat16_rn(__uint_as_float(v[j]));
+          }
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[32], sbf[16];
+          tmem_ld32(tl + T_ST + 64 * hh + 32 * half, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) sbf[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+          tmem_st16(tl + T_SB + 32 * hh + 16 * half, sbf);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      named_sync(BAR_S, GROUP);
+    }
+    if (aborted) {
+      record_status(4u /* KDA_ERR_TIMEOUT */);
+      if (leader) {  // let anything already issued land before the CTA's memory goes away
+        if (pend_mma) (void)mbar_wait(last_mma, last_par);
+        if (pend_v) (void)mbar_wait(&bar_v, v_blk & 1);
+      }
+    } else if (P.S_final) {  // S_final[c'][v] from S^T (lane v): coalesced over v
+      float* sf = P.S_final + (size_t)p * D * D + c;
+      uint32_t v[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        tmem_ld32(tl + T_ST + 64 * hh + 32 * half, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sf[(size_t)(64 * hh + 32 * half + j) * D] = __uint_as_float(v[j]);
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -677,8 +750,7 @@ inline kda_status_t launch_chunk_tc(const SeqParams& P, int n_problems, int C, c
   tc::TmaMaps maps;
   const long long rows = P.cu_seqlens ? (long long)P.T : (long long)P.n_seq * P.T;
   if (!tc::encode_token_map(&maps.q, P.q, rows, P.H) || !tc::encode_token_map(&maps.k, P.k, rows, P.H) ||
-      !tc::encode_token_map(&maps.v, P.v, rows, P.H) || !tc::encode_token_map(&maps.g, P.g, rows, P.H) ||
-      !tc::encode_token_map(&maps.o, P.out, rows, P.H)) {
+      !tc::encode_token_map(&maps.v, P.v, rows, P.H) || !tc::encode_token_map(&maps.g, P.g, rows, P.H)) {
     err = "cuTensorMapEncodeTiled failed";
     return KDA_ERR_CUDA;
   }
