@@ -83,8 +83,8 @@ constexpr uint32_t QG = KG + 16384;    // (Q e^Gamma)^T [c][r]: MN-major B panel
 constexpr uint32_t KH = QG + 16384;    // Khat^T [c][r]: K-major B of S^T += U^T Khat
 constexpr uint32_t WS = KH + 16384;    // fp32 A, then T ([64][WLD], 18 KB)
 constexpr uint32_t PT = WS + 18432;    // P [r][j], K-major B of O^T += U^T P^T (8 KB)
-constexpr uint32_t TB = PT + 8192;     // fp32 M_R during the solve, then T Diag(beta) [r][j]
-constexpr uint32_t SMEM_BYTES = TB + 8192;
+constexpr uint32_t SUB = PT + 8192;    // bf16 16 x 16 B operands of the substitution (6 KB)
+constexpr uint32_t SMEM_BYTES = SUB + 6144;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for aligning the base
 constexpr uint32_t BOX_BYTES = 8192;                // one 64-channel x 64-token TMA box
 
@@ -94,9 +94,9 @@ constexpr uint32_t T_SB = 128;  // S^T bf16 (A operand), 64
 constexpr uint32_t T_D = 192;   // X [Y_B | Y_A]^T, 96
 constexpr uint32_t T_ZT = 288;  // Z^T fp32, 64; after its bf16 copy: U^T fp32
 constexpr uint32_t T_OT = 352;  // O^T fp32, 64 (directly after Z^T: one product writes both)
-constexpr uint32_t T_ZB = 416;  // Z^T bf16 (A operand), 32; after its use: U^T bf16
-constexpr uint32_t T_UT = T_ZT;
-constexpr uint32_t T_UB = T_ZB;
+constexpr uint32_t T_ZB = 416;  // Z^T bf16 (A operand), 32
+constexpr uint32_t T_UT = T_ZT;  // U^T fp32 once Z^T has its bf16 copy
+constexpr uint32_t T_UB = 448;   // U^T bf16 (A operand), 32
 
 // Columns of the A/P product: Y_B (reference rho_B) at 0..63, Y_A (rho_A) at 64..95.
 constexpr int Y_A = 64;
@@ -104,8 +104,14 @@ constexpr int Y_A = 64;
 // Row stride (floats) of the fp32 64 x 64 solve workspace: 72 makes the tf32 B-fragment loads
 // (rows t, columns g) conflict-free.
 constexpr int WLD = 72;
-// M_R = -T_RR A_{R,<16R} (16 x 16R, row stride 16R + 4) inside the TB region.
-__host__ __device__ constexpr int mb_off(int R) { return R == 1 ? 0 : (R == 2 ? 320 : 896); }
+// Operand tiles of the block substitution in SUB: M_{R,m} (m < R) at index R(R-1)/2 + m (0..5),
+// G_R at 6 + R. Tile s sits in panel s / 4 (2 KB, 16 rows x 128 B, 128-byte swizzle) at
+// columns 16 (s % 4) .. 16 (s % 4) + 15 (its 16-element k range).
+__host__ __device__ constexpr int m_tile(int R, int m) { return R * (R - 1) / 2 + m; }
+__host__ __device__ constexpr int g_tile(int R) { return 6 + R; }
+__device__ __forceinline__ uint64_t sub_desc(uint32_t sbase, int s) {
+  return sm100::desc_sw128(sbase + SUB + 2048u * (uint32_t)(s >> 2) + 32u * (uint32_t)(s & 3), 16, 1024);
+}
 
 struct TmaMaps {
   CUtensorMap q, k, v, g;
@@ -501,7 +507,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       // ---------------- T = (I + A)^{-1} (unit lower triangular), in place in WS
       {
         float* ws = reinterpret_cast<float*>(sm + WS);
-        float* mb = reinterpret_cast<float*>(sm + TB);
         const int sw = warp - GROUP / 32;  // warp index inside the group
         // (1) diagonal 16 x 16 blocks T_RR by forward substitution, one column per thread; the
         // result goes to trr so that A_RR stays readable until every column is done
@@ -529,16 +534,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int i = 0; i < 16; ++i) trr[Rd][i][jj] = x[i];
         }
         named_sync(BAR_S, GROUP);
-        // (2) M_R = -T_RR A_{R,<16R} for R = 1..3 (independent): 12 tiles of 16 x 8, two k
-        // steps. Meanwhile the diagonal blocks of WS receive T_RR.
-        if (lt < 64) {
-          float* cp = ws + 16 * Rd * (WLD + 1) + jj;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) cp[i * WLD] = x[i];
-        }
+        // (2) M_{R,m} = -T_RR A_{R,m} (m < R) and G_R = T_RR Diag(beta_R), as bf16 B operands of
+        // the substitution below (16 x 16 tiles, four side by side in each 2 KB swizzled panel)
         for (int tile = sw; tile < 12; tile += GROUP / 32) {
           const int R = tile < 2 ? 1 : (tile < 6 ? 2 : 3);
-          const int nt = tile - (R == 1 ? 0 : (R == 2 ? 2 : 6));
+          const int nt = tile - (R == 1 ? 0 : (R == 2 ? 2 : 6));  // 8-column slice of A_{R,<16R}
           const float* ar = ws + 16 * R * WLD + 8 * nt;
           float acc[3][4] = {};
 #pragma unroll
@@ -548,55 +548,25 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float b[2] = {ar[(8 * ks + t) * WLD + g], ar[(8 * ks + t + 4) * WLD + g]};
             mma_3xtf32_split(acc, a, b);
           }
-          const int ld = 16 * R + 4;
-          float* mo = mb + mb_off(R) + 8 * nt;
-          *reinterpret_cast<float2*>(mo + g * ld + 2 * t) =
-              make_float2(-(acc[0][0] + acc[1][0] + acc[2][0]), -(acc[0][1] + acc[1][1] + acc[2][1]));
-          *reinterpret_cast<float2*>(mo + (g + 8) * ld + 2 * t) =
-              make_float2(-(acc[0][2] + acc[1][2] + acc[2][2]), -(acc[0][3] + acc[1][3] + acc[2][3]));
+          const int sidx = m_tile(R, nt >> 1);
+          const int col = 16 * (sidx & 3) + 8 * (nt & 1) + 2 * t;
+          uint8_t* panel = sm + SUB + 2048u * (uint32_t)(sidx >> 2);
+          *reinterpret_cast<uint32_t*>(panel + sw128_off(g, col)) =
+              pack_bf16(-(acc[0][0] + acc[1][0] + acc[2][0]), -(acc[0][1] + acc[1][1] + acc[2][1]));
+          *reinterpret_cast<uint32_t*>(panel + sw128_off(g + 8, col)) =
+              pack_bf16(-(acc[0][2] + acc[1][2] + acc[2][2]), -(acc[0][3] + acc[1][3] + acc[2][3]));
         }
-        named_sync(BAR_S, GROUP);
-        // (3) block rows in order: T_{R,<16R} = M_R T_{<16R,<16R}; T is zero above its
-        // diagonal, so k steps above the output tile's columns are skipped
+        if (lt < 64) {  // G_R row i: T_RR[i][j] beta_{16 R + j}
+          const int R = lt >> 4, i = lt & 15;
+          const int sidx = g_tile(R);
+          uint8_t* panel = sm + SUB + 2048u * (uint32_t)(sidx >> 2);
+          float gv[16];
 #pragma unroll
-        for (int R = 1; R < 4; ++R) {
-          const int ld = 16 * R + 4;
-          const float* mr = mb + mb_off(R);
-          if (sw < 2 * R) {
-            const int nt = sw;
-            float acc[3][4] = {};
-#pragma unroll
-            for (int ks = 0; ks < 2 * R; ++ks) {
-              if (ks < nt) continue;
-              const float a[4] = {mr[g * ld + 8 * ks + t], mr[(g + 8) * ld + 8 * ks + t],
-                                  mr[g * ld + 8 * ks + t + 4], mr[(g + 8) * ld + 8 * ks + t + 4]};
-              const float b[2] = {ws[(8 * ks + t) * WLD + 8 * nt + g],
-                                  ws[(8 * ks + t + 4) * WLD + 8 * nt + g]};
-              mma_3xtf32_split(acc, a, b);
-            }
-            float* to = ws + 16 * R * WLD + 8 * nt;
-            *reinterpret_cast<float2*>(to + g * WLD + 2 * t) =
-                make_float2(acc[0][0] + acc[1][0] + acc[2][0], acc[0][1] + acc[1][1] + acc[2][1]);
-            *reinterpret_cast<float2*>(to + (g + 8) * WLD + 2 * t) =
-                make_float2(acc[0][2] + acc[1][2] + acc[2][2], acc[0][3] + acc[1][3] + acc[2][3]);
-          }
-          named_sync(BAR_S, GROUP);
-        }
-        // (4) T Diag(beta) -> bf16, K-major [r][j]
-        {
-          const int r = lt >> 2, j0 = (lt & 3) * 16;
-          float y[16];
-#pragma unroll
-          for (int e4 = 0; e4 < 4; ++e4) {
-            const float4 v4 = *reinterpret_cast<const float4*>(ws + r * WLD + j0 + 4 * e4);
-            const float4 b4 = *reinterpret_cast<const float4*>(&beta_s[par][j0 + 4 * e4]);
-            y[4 * e4] = v4.x * b4.x; y[4 * e4 + 1] = v4.y * b4.y;
-            y[4 * e4 + 2] = v4.z * b4.z; y[4 * e4 + 3] = v4.w * b4.w;
-          }
-          st_shared_v4(sb + TB + sw128_off(r, j0), pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
-                       pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
-          st_shared_v4(sb + TB + sw128_off(r, j0 + 8), pack_bf16(y[8], y[9]), pack_bf16(y[10], y[11]),
-                       pack_bf16(y[12], y[13]), pack_bf16(y[14], y[15]));
+          for (int j = 0; j < 16; ++j) gv[j] = trr[R][i][j] * beta_s[par][16 * R + j];
+          st_shared_v4(smem_u32(panel) + sw128_off(i, 16 * (sidx & 3)), pack_bf16(gv[0], gv[1]),
+                       pack_bf16(gv[2], gv[3]), pack_bf16(gv[4], gv[5]), pack_bf16(gv[6], gv[7]));
+          st_shared_v4(smem_u32(panel) + sw128_off(i, 16 * (sidx & 3) + 8), pack_bf16(gv[8], gv[9]),
+                       pack_bf16(gv[10], gv[11]), pack_bf16(gv[12], gv[13]), pack_bf16(gv[14], gv[15]));
         }
       }
       fence_proxy_async_smem();
@@ -604,40 +574,45 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       if (!group_wait2(&bar_v, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       pend_v = false;
-      // ---------------- tcgen05: U^T = V^T (T Diag beta)^T - Z^T (T Diag beta)^T (N 64, K 64)
-      if (leader) {
-        tc_fence_after();
-        const uint32_t id_v = idesc_bf16(128, 64, 1, 0, 0);
-        const uint32_t id_z = idesc_bf16(128, 64, 0, 0, 1);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t b = desc_sw128(sb + TB + 32u * kk, 16, 1024);
-          umma_bf16(tmem + T_UT, desc_sw128(sb + IN_V + 2048u * kk, BOX_BYTES, 1024), b, id_v, kk > 0);
-          umma_bf16_tmem_a(tmem + T_UT, tmem + T_ZB + 8u * kk, b, id_z, 1);
+      // ---------------- block forward substitution on the tensor cores, R = 0..3 (M 128, N 16):
+      //   U_R^T = V_R^T G_R^T - Z_R^T G_R^T + sum_{m<R} U_m^T M_{R,m}^T,   U_R^T -> bf16
+      // which is U = T Diag(beta) (V - Z) solved block by block: (I + A) U = Diag(beta)(V - Z)
+      for (int R = 0; R < 4; ++R) {
+        if (leader) {
+          tc_fence_after();
+          const uint32_t id_v = idesc_bf16(128, 16, 1, 0, 0);
+          const uint32_t id_z = idesc_bf16(128, 16, 0, 0, 1);
+          const uint32_t id_u = idesc_bf16(128, 16, 0, 0, 0);
+          const uint32_t d = tmem + T_UT + 16u * R;
+          const uint64_t bg = sub_desc(sb, g_tile(R));
+          umma_bf16(d, desc_sw128(sb + IN_V + 2048u * R, BOX_BYTES, 1024), bg, id_v, 0);
+          umma_bf16_tmem_a(d, tmem + T_ZB + 8u * R, bg, id_z, 1);
+          for (int m = 0; m < R; ++m)
+            umma_bf16_tmem_a(d, tmem + T_UB + 8u * m, sub_desc(sb, m_tile(R, m)), id_u, 1);
+          umma_commit(&bar_G2);
         }
-        umma_commit(&bar_G2);
+        pend_mma = true; last_mma = &bar_G2; last_par = (uint32_t)(R & 1);
+        if (!group_wait2(&bar_G2, (uint32_t)(R & 1), nullptr, 0, BAR_S)) { aborted = true; break; }
+        pend_mma = false;
+        tc_fence_after();
+        if (hh == 0) {  // U_R^T (lane v, 16 tokens) -> bf16 A operand
+          uint32_t v[16], ub[8];
+          tmem_ld16(tl + T_UT + 16u * R, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) ub[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+          tmem_st8(tl + T_UB + 8u * R, ub);
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        named_sync(BAR_S, GROUP);
       }
-      pend_mma = true; last_mma = &bar_G2; last_par = ph;
-      if (!group_wait2(&bar_G2, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
-      pend_mma = false;
-      tc_fence_after();
+      if (aborted) break;
       if (blk + 1 < nblocks) {  // the v tile is dead
         if (leader) issue_v(blk + 1);
         pend_v = true;
         v_blk = blk + 1;
       }
-      // ---------------- U^T -> bf16 A operand (into the Z^T bf16 columns, read by now)
-      {
-        uint32_t v[32], ub[16];
-        tmem_ld32(tl + T_UT + 32 * hh, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) ub[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-        tmem_st16(tl + T_UB + 16 * hh, ub);
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      named_sync(BAR_S, GROUP);
       // ---------------- tcgen05: O^T += U^T P^T (N 64) ; S^T += U^T Khat (N 128), K 64
       if (leader) {
         tc_fence_after();
