@@ -140,8 +140,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t sb = smem_u32(sm);
   // bar_in: k, q, g tiles landed          bar_v: v tile landed
   // bar_prep: P finished a block's operands (release / acquire for its generic stores)
+  // bar_ext: P has taken A (into WS) and P (into PT) out of the A/P product
+  // bar_oread: P has written a block's O out of TMEM (its columns may be reused)
   // bar_D, bar_ZO, bar_G2, bar_G3: tcgen05 products complete
-  __shared__ uint64_t bar_in, bar_v, bar_prep, bar_D, bar_ZO, bar_G2, bar_G3;
+  __shared__ uint64_t bar_in, bar_v, bar_prep, bar_ext, bar_oread, bar_D, bar_ZO, bar_G2, bar_G3;
   __shared__ uint32_t tmem_base_s;
   __shared__ __align__(16) float beta_s[2][C];  // by block parity
   __shared__ __align__(16) float gl_s[2][D];    // e^{Gamma_L} per key channel, by block parity
@@ -168,6 +170,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bar_in, 1);
     mbar_init(&bar_v, 1);
     mbar_init(&bar_prep, 1);
+    mbar_init(&bar_ext, 1);
+    mbar_init(&bar_oread, 1);
     mbar_init(&bar_D, 1);
     mbar_init(&bar_ZO, 1);
     mbar_init(&bar_G2, 1);
@@ -221,6 +225,25 @@ __global__ void __launch_bounds__(THREADS, 1)
     // on the load until the block that needs it
     unsigned short beta_next = 0;
     if (lt < C && lt < len) beta_next = beta_u[(row0 + lt) * H + h];
+    __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(P.out);
+    // O of block b straight from TMEM (lane v = c, tokens 32 hh .. 32 hh + 31)
+    auto emit_o = [&](int b) {
+      const int tb = b * C;
+      const int nb = min(C, len - tb);
+      __nv_bfloat16* op = out + ((row0 + tb) * H + h) * D + c;
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        uint32_t v[16];
+        tmem_ld16(tl + T_OT + 32 * hh + 16 * part, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r = 32 * hh + 16 * part + j;
+          if (r < nb) op[(size_t)r * H * D] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        }
+      }
+      tc_fence_before();
+    };
 
     for (int blk = 0; blk < nblocks; ++blk) {
       const int t0 = blk * C;
@@ -346,9 +369,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       named_sync(BAR_P, GROUP);
       if (lt == 0) {
         if (blk + 1 < nblocks) issue_in(blk + 1);  // the k, q and g tiles are dead
+      }
+      if (blk + 1 < nblocks) {
+        pend_in = true;
+        in_blk = blk + 1;
+      }
+      if (lt == 0) {
         mbar_arrive(&bar_prep);
-        // ---------------- tcgen05: D = X [Y_B | Y_A]^T (M 128, N 96, K 128); S's extraction of
-        // the previous block's D finished before its last product, awaited above
+        // ---------------- tcgen05: D = X [Y_B | Y_A]^T (M 128, N 96, K 128); this group read the
+        // previous block's D out already
         tc_fence_after();
         const uint32_t id_d = idesc_bf16(128, 96, 1, 1, 0);
 #pragma unroll
@@ -357,92 +386,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                     desc_sw128(sb + YP + 2048u * kk, 16384, 1024), id_d, kk > 0);
         umma_commit(&bar_D);
       }
-      if (blk + 1 < nblocks) {
-        pend_in = true;
-        in_blk = blk + 1;
+      // ---------------- the previous block's O (final since its last product, awaited above),
+      // written while this block's A/P product runs
+      if (blk > 0) {
+        tc_fence_after();
+        emit_o(blk - 1);
+        named_sync(BAR_P, GROUP);
+        if (lt == 0) mbar_arrive(&bar_oread);
       }
       d_blk = blk;
-    }
-    if (aborted) record_status(4u /* KDA_ERR_TIMEOUT */);
-    if (lt == 0) {  // let anything already issued land before the CTA's memory goes away
-      if (aborted && pend_in) (void)mbar_wait(&bar_in, in_blk & 1);
-      if (d_blk >= 0) (void)mbar_wait(&bar_D, d_blk & 1);
-    }
-  } else {
-    // =====================================================================  group S
-    const bool leader = lt == 0;
-    __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(P.out);
-    auto issue_v = [&](int b) {
-      mbar_arrive_expect_tx(&bar_v, 2 * BOX_BYTES);
-      load2(IN_V, &maps.v, (int)(row0 + (size_t)b * C), &bar_v);
-    };
-    // ---- initial state S^T: lane v = c, key channels 64 hh .. 64 hh + 63 (coalesced over v)
-    {
-      const float* s0 = P.S0 ? P.S0 + (size_t)p * D * D + c : nullptr;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sv[32], sbf[16];
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          sv[j] = s0 ? __float_as_uint(s0[(size_t)(64 * hh + 32 * half + j) * D]) : 0u;
-        tmem_st32(tl + T_ST + 64 * hh + 32 * half, sv);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) sbf[j] = pack_bf16(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]));
-        tmem_st16(tl + T_SB + 32 * hh + 16 * half, sbf);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-    }
-    bool pend_v = false, pend_mma = false;
-    int v_blk = 0;  // block of the last v load issued
-    uint64_t* last_mma = &bar_ZO;
-    uint32_t last_par = 0;
-    if (nblocks > 0) {
-      if (leader) issue_v(0);
-      pend_v = true;
-    }
-    named_sync(BAR_S, GROUP);
-
-    for (int blk = 0; blk < nblocks; ++blk) {
-      const int t0 = blk * C;
-      const int n = min(C, len - t0);
-      const int par = blk & 1;
-      const uint32_t ph = (uint32_t)par;
-      if (!group_wait2(&bar_prep, ph, &bar_D, ph, BAR_S)) { aborted = true; break; }
+      if (!group_wait2(&bar_D, blk & 1, nullptr, 0, BAR_P)) { aborted = true; break; }
       tc_fence_after();
-      // ---------------- tcgen05: [Z^T | O^T] = S^T [(K e^Gamma)^T | (Q e^Gamma)^T] (N 128, K 128)
-      if (leader) {
-        tc_fence_after();
-        const uint32_t id_z = idesc_bf16(128, 128, 0, 1, 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_tmem_a(tmem + T_ZT, tmem + T_SB + 8u * kk,
-                           desc_sw128(sb + KG + 2048u * kk, QG - KG, 1024), id_z, kk > 0);
-        umma_commit(&bar_ZO);
-      }
-      pend_mma = true; last_mma = &bar_ZO; last_par = ph;
-      // ---------------- meanwhile: S^T <- S^T Diag(e^{Gamma_L}) (the product above reads the
-      // bf16 copy; Khat^T U accumulates onto this one)
-      {
-        uint32_t v[32];
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int c0 = 64 * hh + 32 * half;
-          tmem_ld32(tl + T_ST + c0, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            const float4 gv = *reinterpret_cast<const float4*>(&gl_s[par][c0 + j]);
-            const float2 a0 = mul2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])),
-                                   make_float2(gv.x, gv.y));
-            const float2 a1 = mul2(make_float2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])),
-                                   make_float2(gv.z, gv.w));
-            v[j] = __float_as_uint(a0.x); v[j + 1] = __float_as_uint(a0.y);
-            v[j + 2] = __float_as_uint(a1.x); v[j + 3] = __float_as_uint(a1.y);
-          }
-          tmem_st32(tl + T_ST + c0, v);
-        }
-      }
       // ---------------- A (fp32, into WS) and P (bf16, into PT) out of TMEM
       // Lane m: rows 0..63 are the k side (A), 64..127 the q side (P); row r = m & 63 reads the
       // Y_A columns in the first half of the block, the Y_B columns in the second (warp-uniform).
@@ -491,9 +445,104 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      // ---------------- Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand
-      // (the group wait also orders the A / P stores above before the solve below)
-      if (!group_wait2(&bar_ZO, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
+      fence_proxy_async_smem();  // P is a tensor-core operand of S's last product
+      named_sync(BAR_P, GROUP);
+      if (lt == 0) mbar_arrive(&bar_ext);
+    }
+    if (!aborted && nblocks > 0) {  // the last block's O
+      if (group_wait2(&bar_G3, (nblocks - 1) & 1, nullptr, 0, BAR_P)) {
+        tc_fence_after();
+        emit_o(nblocks - 1);
+      } else {
+        aborted = true;
+      }
+    }
+    if (aborted) record_status(4u /* KDA_ERR_TIMEOUT */);
+    if (lt == 0) {  // let anything already issued land before the CTA's memory goes away
+      if (aborted && pend_in) (void)mbar_wait(&bar_in, in_blk & 1);
+      if (d_blk >= 0) (void)mbar_wait(&bar_D, d_blk & 1);
+    }
+  } else {
+    // =====================================================================  group S
+    const bool leader = lt == 0;
+    auto issue_v = [&](int b) {
+      mbar_arrive_expect_tx(&bar_v, 2 * BOX_BYTES);
+      load2(IN_V, &maps.v, (int)(row0 + (size_t)b * C), &bar_v);
+    };
+    // ---- initial state S^T: lane v = c, key channels 64 hh .. 64 hh + 63 (coalesced over v)
+    {
+      const float* s0 = P.S0 ? P.S0 + (size_t)p * D * D + c : nullptr;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sv[32], sbf[16];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          sv[j] = s0 ? __float_as_uint(s0[(size_t)(64 * hh + 32 * half + j) * D]) : 0u;
+        tmem_st32(tl + T_ST + 64 * hh + 32 * half, sv);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) sbf[j] = pack_bf16(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]));
+        tmem_st16(tl + T_SB + 32 * hh + 16 * half, sbf);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+    }
+    bool pend_v = false, pend_mma = false;
+    int v_blk = 0;  // block of the last v load issued
+    uint64_t* last_mma = &bar_ZO;
+    uint32_t last_par = 0;
+    if (nblocks > 0) {
+      if (leader) issue_v(0);
+      pend_v = true;
+    }
+    named_sync(BAR_S, GROUP);
+
+    for (int blk = 0; blk < nblocks; ++blk) {
+      const int t0 = blk * C;
+      const int n = min(C, len - t0);
+      const int par = blk & 1;
+      const uint32_t ph = (uint32_t)par;
+      // P's operands of this block are in place, and P has written the previous block's O
+      if (!group_wait2(&bar_prep, ph, blk > 0 ? &bar_oread : nullptr, (blk - 1) & 1, BAR_S)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      // ---------------- tcgen05: [Z^T | O^T] = S^T [(K e^Gamma)^T | (Q e^Gamma)^T] (N 128, K 128)
+      if (leader) {
+        tc_fence_after();
+        const uint32_t id_z = idesc_bf16(128, 128, 0, 1, 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_tmem_a(tmem + T_ZT, tmem + T_SB + 8u * kk,
+                           desc_sw128(sb + KG + 2048u * kk, QG - KG, 1024), id_z, kk > 0);
+        umma_commit(&bar_ZO);
+      }
+      pend_mma = true; last_mma = &bar_ZO; last_par = ph;
+      // ---------------- meanwhile: S^T <- S^T Diag(e^{Gamma_L}) (the product above reads the
+      // bf16 copy; Khat^T U accumulates onto this one)
+      {
+        uint32_t v[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int c0 = 64 * hh + 32 * half;
+          tmem_ld32(tl + T_ST + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const float4 gv = *reinterpret_cast<const float4*>(&gl_s[par][c0 + j]);
+            const float2 a0 = mul2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])),
+                                   make_float2(gv.x, gv.y));
+            const float2 a1 = mul2(make_float2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])),
+                                   make_float2(gv.z, gv.w));
+            v[j] = __float_as_uint(a0.x); v[j + 1] = __float_as_uint(a0.y);
+            v[j + 2] = __float_as_uint(a1.x); v[j + 3] = __float_as_uint(a1.y);
+          }
+          tmem_st32(tl + T_ST + c0, v);
+        }
+      }
+      // ---------------- Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand; group P has written
+      // A and P of this block by bar_ext
+      if (!group_wait2(&bar_ZO, ph, &bar_ext, ph, BAR_S)) { aborted = true; break; }
       pend_mma = false;
       tc_fence_after();
       {
@@ -540,21 +589,21 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int R = tile < 2 ? 1 : (tile < 6 ? 2 : 3);
           const int nt = tile - (R == 1 ? 0 : (R == 2 ? 2 : 6));  // 8-column slice of A_{R,<16R}
           const float* ar = ws + 16 * R * WLD + 8 * nt;
-          float acc[3][4] = {};
+          // one tf32 product per k step: the result is rounded to bf16 right after, so tf32's
+          // 10-bit mantissa already exceeds what is kept
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks) {
-            const float a[4] = {trr[R][g][8 * ks + t], trr[R][g + 8][8 * ks + t],
-                                trr[R][g][8 * ks + t + 4], trr[R][g + 8][8 * ks + t + 4]};
-            const float b[2] = {ar[(8 * ks + t) * WLD + g], ar[(8 * ks + t + 4) * WLD + g]};
-            mma_3xtf32_split(acc, a, b);
+            const uint32_t a[4] = {to_tf32(trr[R][g][8 * ks + t]), to_tf32(trr[R][g + 8][8 * ks + t]),
+                                   to_tf32(trr[R][g][8 * ks + t + 4]), to_tf32(trr[R][g + 8][8 * ks + t + 4])};
+            const uint32_t b[2] = {to_tf32(ar[(8 * ks + t) * WLD + g]), to_tf32(ar[(8 * ks + t + 4) * WLD + g])};
+            mma_tf32(acc, a, b);
           }
           const int sidx = m_tile(R, nt >> 1);
           const int col = 16 * (sidx & 3) + 8 * (nt & 1) + 2 * t;
           uint8_t* panel = sm + SUB + 2048u * (uint32_t)(sidx >> 2);
-          *reinterpret_cast<uint32_t*>(panel + sw128_off(g, col)) =
-              pack_bf16(-(acc[0][0] + acc[1][0] + acc[2][0]), -(acc[0][1] + acc[1][1] + acc[2][1]));
-          *reinterpret_cast<uint32_t*>(panel + sw128_off(g + 8, col)) =
-              pack_bf16(-(acc[0][2] + acc[1][2] + acc[2][2]), -(acc[0][3] + acc[1][3] + acc[2][3]));
+          *reinterpret_cast<uint32_t*>(panel + sw128_off(g, col)) = pack_bf16(-acc[0], -acc[1]);
+          *reinterpret_cast<uint32_t*>(panel + sw128_off(g + 8, col)) = pack_bf16(-acc[2], -acc[3]);
         }
         if (lt < 64) {  // G_R row i: T_RR[i][j] beta_{16 R + j}
           const int R = lt >> 4, i = lt & 15;
@@ -631,20 +680,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!group_wait2(&bar_G3, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       pend_mma = false;
       tc_fence_after();
-      // ---------------- outputs; bf16 copy of the new state for the next block
+      // ---------------- bf16 copy of the new state for the next block (group P writes O)
       {
-        __nv_bfloat16* op = out + ((row0 + t0) * H + h) * D + c;
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          uint32_t v[16];
-          tmem_ld16(tl + T_OT + 32 * hh + 16 * part, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int r = 32 * hh + 16 * part + j;
-            if (r < n) op[(size_t)r * H * D] = __float2bfloat16_rn(__uint_as_float(v[j]));
-          }
-        }
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t v[32], sbf[16];
