@@ -3,12 +3,15 @@
 // Mathematics (Kimi K3 wiki: "Notations mathématiques", table "Attention et KDA" for the
 // recurrence; "Glossaire", entries "Chunkwise", "UT" and "Décroissance bornée"). For one block
 // of C tokens with incoming state S, Gamma the inclusive cumulative sum of g inside the block:
-//   A_rj = beta_r sum_c k_rc k_jc e^{Gamma_rc - Gamma_jc} (j < r),  T = (I + A)^{-1}
-//   U = T Diag(beta) (V - (K e^Gamma) S)          (the UT transform applied to the residual)
+//   A_rj = beta_r sum_c k_rc k_jc e^{Gamma_rc - Gamma_jc} (j < r)
+//   (I + A) U = Diag(beta) (V - (K e^Gamma) S)     (the UT transform of the residual)
 //   P_rj = sum_c q_rc k_jc e^{Gamma_rc - Gamma_jc} (j <= r),  O = (Q e^Gamma) S + P U
 //   S' = Diag(e^{Gamma_L}) S + Khat^T U,  Khat_j = k_j e^{Gamma_L - Gamma_j}
-// (U equals U~ - W S with U~ = T Diag(beta) V and W = T Diag(beta) K e^Gamma; forming the
-// residual V - (K e^Gamma) S first needs no W and lets that product start before the solve.)
+// U equals U~ - W S with U~ = T Diag(beta) V, W = T Diag(beta) K e^Gamma and T = (I + A)^{-1};
+// forming the residual V - (K e^Gamma) S first needs no W. U is found by forward substitution
+// over the four 16-row sub-blocks R of the block:
+//   U_R = G_R (V_R - Z_R) + sum_{m<R} M_{R,m} U_m,  G_R = T_RR Diag(beta_R),  M_{R,m} = -T_RR A_{R,m}
+// with Z = (K e^Gamma) S and T_RR = (I + A_RR)^{-1} the 16 x 16 diagonal inverses.
 //
 // Bounded decay. Over a block of 64 tokens Gamma can fall to -320, so e^{-Gamma} overflows any
 // floating type and A, P cannot be one product (K e^Gamma)(K e^{-Gamma})^T. With
@@ -35,20 +38,23 @@
 //
 // Two warp groups work on consecutive blocks at the same time:
 //   group P (warps 0-7), block n + 1: Gamma; X, Y, (K e^Gamma)^T, (Q e^Gamma)^T, Khat^T
-//     ([channel][token] rows, 16-byte stores); then the A/P product D = X [Y_B | Y_A]^T.
+//     ([channel][token] rows, 16-byte stores); the A/P product D = X [Y_B | Y_A]^T; A (fp32)
+//     and P (bf16) out of TMEM; and, once S has finished block n, block n's O out of TMEM.
 //   group S (warps 8-15), block n:
 //     tcgen05: [Z^T | O^T] = S^T [(K e^Gamma)^T | (Q e^Gamma)^T]; meanwhile S^T <- S^T e^{Gamma_L}
-//     SIMT: A and P out of TMEM; Z^T -> bf16; T = (I + A)^{-1} (16 x 16 blocks, fp32 with
-//           3xTF32 warp MMAs); T Diag(beta) -> bf16
-//     tcgen05: U^T = V^T (T Diag beta)^T - Z^T (T Diag beta)^T;  SIMT: U^T -> bf16
-//     tcgen05: O^T += U^T P^T;  S^T += U^T Khat;  SIMT: O out, bf16 copy of S^T
-// Shared buffers pass between the groups through mbarriers: P may rewrite X and Y once the A/P
-// product of the previous block has completed, (K/Q e^Gamma)^T once S's first product has, and
-// Khat^T (held in registers until then) once S's last product has; S starts a block once its
-// A/P product is complete. Transposed forms keep every product at M = 128 (TMEM lane = row).
-// Only the bf16 copy of the state feeds the tensor cores; the fp32 state accumulates in TMEM,
-// so rounding does not accumulate in S itself. Every wait is bounded; a timeout latches
-// KDA_ERR_TIMEOUT, lets issued copies and products land, frees TMEM and returns.
+//     SIMT: Z^T -> bf16; T_RR by forward substitution (fp32); M_{R,m} (tf32 warp MMAs) and G_R
+//           as bf16 16 x 16 operand tiles
+//     tcgen05, four steps R: U_R^T = V_R^T G_R^T - Z_R^T G_R^T + sum_{m<R} U_m^T M_{R,m}^T (N 16),
+//           each followed by U_R^T -> bf16 in TMEM
+//     tcgen05: O^T += U^T P^T;  S^T += U^T Khat;  SIMT: bf16 copy of S^T
+// Shared buffers pass between the groups through mbarriers: P may rewrite X and Y once its
+// A/P product of the previous block has completed, (K/Q e^Gamma)^T once S's first product has,
+// and Khat^T (held in registers until then), A and P once S's last product has; S starts a
+// block once P has written that block's operands and the previous block's O. Transposed forms
+// keep every product at M = 128 (TMEM lane = row). Only the bf16 copy of the state feeds the
+// tensor cores; the fp32 state accumulates in TMEM, so rounding does not accumulate in S
+// itself. Every wait is bounded; a timeout latches KDA_ERR_TIMEOUT, lets issued copies and
+// products land, frees TMEM and returns.
 #pragma once
 
 #include <cuda.h>
