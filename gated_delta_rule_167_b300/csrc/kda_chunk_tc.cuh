@@ -88,8 +88,8 @@ constexpr uint32_t KG = YP + 32768;    // (K e^Gamma)^T [c][r]: MN-major B panel
 constexpr uint32_t QG = KG + 16384;    // (Q e^Gamma)^T [c][r]: MN-major B panel 1 of [Z^T | O^T]
 constexpr uint32_t KH = QG + 16384;    // Khat^T [c][r]: K-major B of S^T += U^T Khat
 constexpr uint32_t WS = KH + 16384;    // fp32 A, then T ([64][WLD], 18 KB)
-constexpr uint32_t PT = WS + 18432;    // P [r][j], K-major B of O^T += U^T P^T (8 KB)
-constexpr uint32_t SUB = PT + 8192;    // bf16 16 x 16 B operands of the substitution (6 KB)
+constexpr uint32_t PT = WS + 18432;    // P [r][j], K-major B of O^T += U^T P^T, 2 x 8 KB by parity
+constexpr uint32_t SUB = PT + 16384;   // bf16 16 x 16 B operands of the substitution (6 KB)
 constexpr uint32_t SMEM_BYTES = SUB + 6144;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for aligning the base
 constexpr uint32_t BOX_BYTES = 8192;                // one 64-channel x 64-token TMA box
@@ -99,10 +99,12 @@ constexpr uint32_t T_ST = 0;    // S^T fp32 [v][c], 128
 constexpr uint32_t T_SB = 128;  // S^T bf16 (A operand), 64
 constexpr uint32_t T_D = 192;   // X [Y_B | Y_A]^T, 96
 constexpr uint32_t T_ZT = 288;  // Z^T fp32, 64; after its bf16 copy: U^T fp32
-constexpr uint32_t T_OT = 352;  // O^T fp32, 64 (directly after Z^T: one product writes both)
-constexpr uint32_t T_ZB = 416;  // Z^T bf16 (A operand), 32
+constexpr uint32_t T_OT = 352;  // O^T fp32, 2 x 64 by block parity (P writes one out while S
+                                // accumulates the other)
+constexpr uint32_t T_ZB = 480;  // Z^T bf16 (A operand), 32; U_R^T bf16 replaces Z_R^T once
+                                // step R of the substitution has read it
 constexpr uint32_t T_UT = T_ZT;  // U^T fp32 once Z^T has its bf16 copy
-constexpr uint32_t T_UB = 448;   // U^T bf16 (A operand), 32
+constexpr uint32_t T_UB = T_ZB;  // U^T bf16 (A operand), written over Z^T bf16 step by step
 
 // Columns of the A/P product: Y_B (reference rho_B) at 0..63, Y_A (rho_A) at 64..95.
 constexpr int Y_A = 64;
@@ -147,9 +149,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   // bar_in: k, q, g tiles landed          bar_v: v tile landed
   // bar_prep: P finished a block's operands (release / acquire for its generic stores)
   // bar_ext: P has taken A (into WS) and P (into PT) out of the A/P product
-  // bar_oread: P has written a block's O out of TMEM (its columns may be reused)
+  // bar_wsfree: S has read a block's A out of WS (P may put the next one there)
+  // bar_khr: P has stored a block's Khat^T and written the previous block's O out of TMEM
   // bar_D, bar_ZO, bar_G2, bar_G3: tcgen05 products complete
-  __shared__ uint64_t bar_in, bar_v, bar_prep, bar_ext, bar_oread, bar_D, bar_ZO, bar_G2, bar_G3;
+  __shared__ uint64_t bar_in, bar_v, bar_prep, bar_ext, bar_wsfree, bar_khr, bar_D, bar_ZO, bar_G2,
+      bar_G3;
   __shared__ uint32_t tmem_base_s;
   __shared__ __align__(16) float beta_s[2][C];  // by block parity
   __shared__ __align__(16) float gl_s[2][D];    // e^{Gamma_L} per key channel, by block parity
@@ -177,7 +181,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bar_v, 1);
     mbar_init(&bar_prep, 1);
     mbar_init(&bar_ext, 1);
-    mbar_init(&bar_oread, 1);
+    mbar_init(&bar_wsfree, 1);
+    mbar_init(&bar_khr, 1);
     mbar_init(&bar_D, 1);
     mbar_init(&bar_ZO, 1);
     mbar_init(&bar_G2, 1);
@@ -240,7 +245,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         uint32_t v[16];
-        tmem_ld16(tl + T_OT + 32 * hh + 16 * part, v);
+        tmem_ld16(tl + T_OT + 64u * (uint32_t)(b & 1) + 32 * hh + 16 * part, v);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -356,31 +361,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      // ---------------- Khat^T: wait until S's last product of the previous block has read it
-      if (blk > 0 && !group_wait2(&bar_G3, (blk - 1) & 1, nullptr, 0, BAR_P)) {
-        aborted = true;
-        break;
-      }
-      {
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int gi = 0; gi < 2; ++gi) {
-            const uint32_t* kw = a == 0 ? khA : khB;
-            st_shared_v4(sb + KH + sw128_off(c, 16 * (2 * a + hh) + 8 * gi), kw[4 * gi],
-                         kw[4 * gi + 1], kw[4 * gi + 2], kw[4 * gi + 3]);
-          }
-      }
+      // X, Y and (K/Q e^Gamma)^T are in place: release them and start the A/P product
       fence_proxy_async_smem();
       named_sync(BAR_P, GROUP);
       if (lt == 0) {
         if (blk + 1 < nblocks) issue_in(blk + 1);  // the k, q and g tiles are dead
-      }
-      if (blk + 1 < nblocks) {
-        pend_in = true;
-        in_blk = blk + 1;
-      }
-      if (lt == 0) {
         mbar_arrive(&bar_prep);
         // ---------------- tcgen05: D = X [Y_B | Y_A]^T (M 128, N 96, K 128); this group read the
         // previous block's D out already
@@ -392,16 +377,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     desc_sw128(sb + YP + 2048u * kk, 16384, 1024), id_d, kk > 0);
         umma_commit(&bar_D);
       }
-      // ---------------- the previous block's O (final since its last product, awaited above),
-      // written while this block's A/P product runs
-      if (blk > 0) {
-        tc_fence_after();
-        emit_o(blk - 1);
-        named_sync(BAR_P, GROUP);
-        if (lt == 0) mbar_arrive(&bar_oread);
+      if (blk + 1 < nblocks) {
+        pend_in = true;
+        in_blk = blk + 1;
       }
       d_blk = blk;
-      if (!group_wait2(&bar_D, blk & 1, nullptr, 0, BAR_P)) { aborted = true; break; }
+      // A goes into WS once S has read the previous block's A out of it
+      if (!group_wait2(&bar_D, blk & 1, blk > 0 ? &bar_wsfree : nullptr, (blk - 1) & 1, BAR_P)) {
+        aborted = true;
+        break;
+      }
       tc_fence_after();
       // ---------------- A (fp32, into WS) and P (bf16, into PT) out of TMEM
       // Lane m: rows 0..63 are the k side (A), 64..127 the q side (P); row r = m & 63 reads the
@@ -446,7 +431,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int j = j0 + 8 * j8 + e;
                 x[e] = (j <= r) ? vals[8 * j8 + e] : 0.f;
               }
-              st_pack8(sb + PT + sw128_off(r, j0 + 8 * j8), x);
+              st_pack8(sb + PT + 8192u * (uint32_t)par + sw128_off(r, j0 + 8 * j8), x);
             }
           }
         }
@@ -454,6 +439,26 @@ __global__ void __launch_bounds__(THREADS, 1)
       fence_proxy_async_smem();  // P is a tensor-core operand of S's last product
       named_sync(BAR_P, GROUP);
       if (lt == 0) mbar_arrive(&bar_ext);
+      // ---------------- once S's last product of the previous block is complete: Khat^T of this
+      // block (that product read the previous one) and the previous block's O
+      if (blk > 0) {
+        if (!group_wait2(&bar_G3, (blk - 1) & 1, nullptr, 0, BAR_P)) { aborted = true; break; }
+        tc_fence_after();
+      }
+      {
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int gi = 0; gi < 2; ++gi) {
+            const uint32_t* kw = a == 0 ? khA : khB;
+            st_shared_v4(sb + KH + sw128_off(c, 16 * (2 * a + hh) + 8 * gi), kw[4 * gi],
+                         kw[4 * gi + 1], kw[4 * gi + 2], kw[4 * gi + 3]);
+          }
+      }
+      fence_proxy_async_smem();
+      if (blk > 0) emit_o(blk - 1);
+      named_sync(BAR_P, GROUP);
+      if (lt == 0) mbar_arrive(&bar_khr);
     }
     if (!aborted && nblocks > 0) {  // the last block's O
       if (group_wait2(&bar_G3, (nblocks - 1) & 1, nullptr, 0, BAR_P)) {
@@ -507,20 +512,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int n = min(C, len - t0);
       const int par = blk & 1;
       const uint32_t ph = (uint32_t)par;
-      // P's operands of this block are in place, and P has written the previous block's O
-      if (!group_wait2(&bar_prep, ph, blk > 0 ? &bar_oread : nullptr, (blk - 1) & 1, BAR_S)) {
+      // P's operands of this block are in place, and P has written out the O of two blocks ago,
+      // whose TMEM columns this block's O takes
+      if (!group_wait2(&bar_prep, ph, blk > 0 ? &bar_khr : nullptr, (blk - 1) & 1, BAR_S)) {
         aborted = true;
         break;
       }
       tc_fence_after();
-      // ---------------- tcgen05: [Z^T | O^T] = S^T [(K e^Gamma)^T | (Q e^Gamma)^T] (N 128, K 128)
+      const uint32_t t_ot = T_OT + 64u * (uint32_t)par;  // this block's O^T columns
+      // ---------------- tcgen05: Z^T = S^T (K e^Gamma)^T, O^T = S^T (Q e^Gamma)^T (N 64, K 128)
       if (leader) {
         tc_fence_after();
-        const uint32_t id_z = idesc_bf16(128, 128, 0, 1, 0);
+        const uint32_t id_z = idesc_bf16(128, 64, 0, 1, 0);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
+        for (int kk = 0; kk < 8; ++kk) {
           umma_bf16_tmem_a(tmem + T_ZT, tmem + T_SB + 8u * kk,
-                           desc_sw128(sb + KG + 2048u * kk, QG - KG, 1024), id_z, kk > 0);
+                           desc_sw128(sb + KG + 2048u * kk, 16384, 1024), id_z, kk > 0);
+          umma_bf16_tmem_a(tmem + t_ot, tmem + T_SB + 8u * kk,
+                           desc_sw128(sb + QG + 2048u * kk, 16384, 1024), id_z, kk > 0);
+        }
         umma_commit(&bar_ZO);
       }
       pend_mma = true; last_mma = &bar_ZO; last_par = ph;
@@ -629,6 +639,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       if (!group_wait2(&bar_v, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       pend_v = false;
+      if (leader) mbar_arrive(&bar_wsfree);  // A has been read out of WS (T_RR, M, G are made)
       // ---------------- block forward substitution on the tensor cores, R = 0..3 (M 128, N 16):
       //   U_R^T = V_R^T G_R^T - Z_R^T G_R^T + sum_{m<R} U_m^T M_{R,m}^T,   U_R^T -> bf16
       // which is U = T Diag(beta) (V - Z) solved block by block: (I + A) U = Diag(beta)(V - Z)
@@ -668,15 +679,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         pend_v = true;
         v_blk = blk + 1;
       }
-      // ---------------- tcgen05: O^T += U^T P^T (N 64) ; S^T += U^T Khat (N 128), K 64
+      // ---------------- tcgen05: O^T += U^T P^T (N 64) ; S^T += U^T Khat (N 128), K 64; P has
+      // stored this block's Khat^T by bar_khr
+      if (!group_wait2(&bar_khr, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       if (leader) {
         tc_fence_after();
         const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
         const uint32_t id_s = idesc_bf16(128, 128, 0, 0, 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          umma_bf16_tmem_a(tmem + T_OT, tmem + T_UB + 8u * kk,
-                           desc_sw128(sb + PT + 32u * kk, 16, 1024), id_o, 1);
+          umma_bf16_tmem_a(tmem + t_ot, tmem + T_UB + 8u * kk,
+                           desc_sw128(sb + PT + 8192u * (uint32_t)par + 32u * kk, 16, 1024), id_o, 1);
           umma_bf16_tmem_a(tmem + T_ST, tmem + T_UB + 8u * kk,
                            desc_sw128(sb + KH + 32u * kk, 16, 1024), id_s, 1);
         }
