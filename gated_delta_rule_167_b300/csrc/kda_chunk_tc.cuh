@@ -89,8 +89,8 @@ constexpr uint32_t QG = KG + 16384;    // (Q e^Gamma)^T [c][r]: MN-major B panel
 constexpr uint32_t KH = QG + 16384;    // Khat^T [c][r]: K-major B of S^T += U^T Khat
 constexpr uint32_t WS = KH + 16384;    // fp32 A, then T ([64][WLD], 18 KB)
 constexpr uint32_t PT = WS + 18432;    // P [r][j], K-major B of O^T += U^T P^T, 2 x 8 KB by parity
-constexpr uint32_t SUB = PT + 16384;   // bf16 16 x 16 B operands of the substitution (6 KB)
-constexpr uint32_t SMEM_BYTES = SUB + 6144;
+constexpr uint32_t GB = PT + 16384;    // G = T Diag(beta) [r][j] bf16, K-major B of U^T (8 KB)
+constexpr uint32_t SMEM_BYTES = GB + 8192;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for aligning the base
 constexpr uint32_t BOX_BYTES = 8192;                // one 64-channel x 64-token TMA box
 
@@ -101,10 +101,9 @@ constexpr uint32_t T_D = 192;   // X [Y_B | Y_A]^T, 96
 constexpr uint32_t T_ZT = 288;  // Z^T fp32, 64; after its bf16 copy: U^T fp32
 constexpr uint32_t T_OT = 352;  // O^T fp32, 2 x 64 by block parity (P writes one out while S
                                 // accumulates the other)
-constexpr uint32_t T_ZB = 480;  // Z^T bf16 (A operand), 32; U_R^T bf16 replaces Z_R^T once
-                                // step R of the substitution has read it
+constexpr uint32_t T_ZB = 480;  // Z^T bf16 (A operand), 32
 constexpr uint32_t T_UT = T_ZT;  // U^T fp32 once Z^T has its bf16 copy
-constexpr uint32_t T_UB = T_ZB;  // U^T bf16 (A operand), written over Z^T bf16 step by step
+constexpr uint32_t T_UB = T_ZB;  // U^T bf16 (A operand), over Z^T bf16 once the U product read it
 
 // Columns of the A/P product: Y_B (reference rho_B) at 0..63, Y_A (rho_A) at 64..95.
 constexpr int Y_A = 64;
@@ -112,15 +111,6 @@ constexpr int Y_A = 64;
 // Row stride (floats) of the fp32 64 x 64 solve workspace: 72 makes the tf32 B-fragment loads
 // (rows t, columns g) conflict-free.
 constexpr int WLD = 72;
-// Operand tiles of the block substitution in SUB: M_{R,m} (m < R) at index R(R-1)/2 + m (0..5),
-// G_R at 6 + R. Tile s sits in panel s / 4 (2 KB, 16 rows x 128 B, 128-byte swizzle) at
-// columns 16 (s % 4) .. 16 (s % 4) + 15 (its 16-element k range).
-__host__ __device__ constexpr int m_tile(int R, int m) { return R * (R - 1) / 2 + m; }
-__host__ __device__ constexpr int g_tile(int R) { return 6 + R; }
-__device__ __forceinline__ uint64_t sub_desc(uint32_t sbase, int s) {
-  return sm100::desc_sw128(sbase + SUB + 2048u * (uint32_t)(s >> 2) + 32u * (uint32_t)(s & 3), 16, 1024);
-}
-
 struct TmaMaps {
   CUtensorMap q, k, v, g;
 };
@@ -291,9 +281,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       named_sync(BAR_P, GROUP);
       const float s0 = xch[0][c], s1 = xch[1][c], s2 = xch[2][c], s3 = xch[3][c];
-      const float rhoA = s0, b2 = s0 + s1, rhoB = b2 + s2, gL = rhoB + s3;
+      const float b2 = s0 + s1, rhoB = b2 + s2, gL = rhoB + s3;  // rho_A = s0
       if (hh == 0) gl_s[par][c] = ex2(gL);
       // ---------------- operands: X, Y, (K e^Gamma)^T, (Q e^Gamma)^T; Khat^T kept packed
+      // Two exponentials per element, of the running sum inside the sub-block and its negative:
+      //   u_r = e^{Gamma_r - Gamma_{rb-1}},  w_r = e^{Gamma_{rb-1} - Gamma_r}   (rb = first token)
+      // and every factor is one of these times an anchor, an exponential of a sum of g over whole
+      // sub-blocks. Where an anchor may underflow it is <= 1 and multiplies a factor <= 1, so a
+      // product flushes to zero only when its own value is below the fp32 range.
       uint32_t khA[8], khB[8];  // Khat^T of sub-blocks hh and 2 + hh, bf16 pairs
       {
         const uint8_t* kp = sm + IN_K + (c >> 6) * BOX_BYTES;
@@ -301,8 +296,27 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll 1
         for (int a = 0; a < 2; ++a) {
           const int R = 2 * a + hh;  // a = 0: first half (reference rho_A), a = 1: second
-          const float rho = a == 0 ? rhoA : rhoB;
-          float acc = a == 0 ? (hh ? s0 : 0.f) : (hh ? rhoB : b2);  // Gamma before the sub-block
+          // anchors e^{Gamma_{rb-1}}, e^{Gamma_L - Gamma_{rb+15}}, e^{rho_B - Gamma_{rb+15}} and the
+          // sub-block's own e^{+-(Gamma_{rb+15} - Gamma_{rb-1})}
+          float before, after, tob, sR;
+          if (a == 0) {
+            before = hh ? s0 : 0.f;
+            after = hh ? s2 + s3 : s1 + s2 + s3;
+            tob = hh ? s2 : s1 + s2;
+            sR = hh ? s1 : s0;
+          } else {
+            before = hh ? rhoB : b2;
+            after = hh ? 0.f : s3;
+            tob = 0.f;
+            sR = hh ? s3 : s2;
+          }
+          const float eb = ex2(before), ea = ex2(after), et = ex2(tob), es = ex2(sR);
+          const float2 aG = make_float2(eb, eb), aH = make_float2(ea, ea), aY = make_float2(et, et);
+          const float2 cS = make_float2(es, es);
+          // the sub-block ends at rho (hh = 0) or starts right after it (hh = 1)
+          const float cf = hh ? 1.f : ex2(-sR);
+          const float2 cF = make_float2(cf, cf);
+          float acc = 0.f;  // Gamma_r - Gamma_{rb-1}, log2 units
 #pragma unroll
           for (int gi = 0; gi < 2; ++gi) {
             const int r0 = 16 * R + 8 * gi;  // first token of these 8 rows
@@ -325,27 +339,31 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t xk[4], xq[4], y[4], yb[4], kg[4], qg[4];  // bf16 pairs
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-              const float G0 = G[2 * w], G1 = G[2 * w + 1];
-              const float L0 = G0 - rho, L1 = G1 - rho;
-              const float2 F = make_float2(ex2(L0), ex2(L1));               // e^{Gamma - rho}
-              const float2 Fi = make_float2(ex2(-L0), ex2(-L1));            // e^{rho - Gamma}
-              const float2 eG = make_float2(ex2(G0), ex2(G1));              // e^{Gamma}
-              const float2 eH = make_float2(ex2(gL - G0), ex2(gL - G1));    // e^{Gamma_L - Gamma}
-              const float2 eYB = make_float2(ex2(rhoB - G0), ex2(rhoB - G1));  // e^{rho_B - Gamma}
+              const float L0 = G[2 * w], L1 = G[2 * w + 1];
+              const float2 u = make_float2(ex2(L0), ex2(L1));
+              const float2 wv = make_float2(ex2(-L0), ex2(-L1));
+              const float2 sfx = mul2(cS, wv);   // e^{Gamma_{rb+15} - Gamma}
+              const float2 F = mul2(cF, u);      // e^{Gamma - rho}
+              const float2 Fi = hh ? wv : sfx;   // e^{rho - Gamma}
+              const float2 eG = mul2(aG, u);     // e^{Gamma}
+              const float2 eH = mul2(aH, sfx);   // e^{Gamma_L - Gamma}
               const float2 k2 = make_float2(kv[2 * w], kv[2 * w + 1]);
               const float2 q2 = make_float2(qv[2 * w], qv[2 * w + 1]);
               const float2 xk2 = mul2(k2, F), xq2 = mul2(q2, F), y2 = mul2(k2, Fi);
               const float2 kg2 = mul2(k2, eG), qg2 = mul2(q2, eG), kh2 = mul2(k2, eH);
-              const float2 yb2 = mul2(k2, eYB);
               xk[w] = pack_bf16(xk2.x, xk2.y);
               xq[w] = pack_bf16(xq2.x, xq2.y);
               y[w] = pack_bf16(y2.x, y2.y);
-              yb[w] = pack_bf16(yb2.x, yb2.y);
               kg[w] = pack_bf16(kg2.x, kg2.y);
               qg[w] = pack_bf16(qg2.x, qg2.y);
               const uint32_t khw = pack_bf16(kh2.x, kh2.y);
-              if (a == 0) khA[4 * gi + w] = khw;
-              else khB[4 * gi + w] = khw;
+              if (a == 0) {
+                const float2 yb2 = mul2(k2, mul2(aY, sfx));  // k e^{rho_B - Gamma}
+                yb[w] = pack_bf16(yb2.x, yb2.y);
+                khA[4 * gi + w] = khw;
+              } else {
+                khB[4 * gi + w] = khw;
+              }
             }
             const uint32_t o = sw128_off(c, r0);
             st_words4(sb + XK + o, xk);
@@ -505,6 +523,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (leader) issue_v(0);
       pend_v = true;
     }
+    // G is zero above the diagonal blocks; those entries are never written again
+    for (int i = lt; i < 8192 / 16; i += GROUP) st_shared_v4(sb + GB + 16u * (uint32_t)i, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
     named_sync(BAR_S, GROUP);
 
     for (int blk = 0; blk < nblocks; ++blk) {
@@ -537,14 +558,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       // ---------------- meanwhile: S^T <- S^T Diag(e^{Gamma_L}) (the product above reads the
       // bf16 copy; Khat^T U accumulates onto this one)
       {
-        uint32_t v[32];
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int c0 = 64 * hh + 32 * half;
-          tmem_ld32(tl + T_ST + c0, v);
+        uint32_t v[16];
+#pragma unroll 1
+        for (int part = 0; part < 4; ++part) {
+          const int c0 = 64 * hh + 16 * part;
+          tmem_ld16(tl + T_ST + c0, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
+          for (int j = 0; j < 16; j += 4) {
             const float4 gv = *reinterpret_cast<const float4*>(&gl_s[par][c0 + j]);
             const float2 a0 = mul2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])),
                                    make_float2(gv.x, gv.y));
@@ -553,7 +574,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             v[j] = __float_as_uint(a0.x); v[j + 1] = __float_as_uint(a0.y);
             v[j + 2] = __float_as_uint(a1.x); v[j + 3] = __float_as_uint(a1.y);
           }
-          tmem_st32(tl + T_ST + c0, v);
+          tmem_st16(tl + T_ST + c0, v);
         }
       }
       // ---------------- Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand; group P has written
@@ -569,110 +590,152 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int j = 0; j < 16; ++j) zb[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
         tmem_st16(tl + T_ZB + 16 * hh, zb);
       }
-      // ---------------- T = (I + A)^{-1} (unit lower triangular), in place in WS
+      // ---------------- T = (I + A)^{-1} (unit lower triangular) and G = T Diag(beta) (bf16)
+      // The four 16 x 16 diagonal inverses T_RR by forward substitution in fp32; then, from the
+      // block-inverse identity [[P, 0], [C, Q]]^{-1} = [[P^{-1}, 0], [-Q^{-1} C P^{-1}, Q^{-1}]],
+      // the off-diagonal 16 x 16 block of each 32 x 32 half and then the off-diagonal 32 x 32
+      // block, as tf32 warp MMAs on fp32 blocks in WS (T overwrites A where A is no longer read).
       {
         float* ws = reinterpret_cast<float*>(sm + WS);
+        // scratch: rows 0..31, columns 32..63 of WS, where A is zero and no block of T is kept
+        float* qs = ws + 32;
         const int sw = warp - GROUP / 32;  // warp index inside the group
-        // (1) diagonal 16 x 16 blocks T_RR by forward substitution, one column per thread; the
-        // result goes to trr so that A_RR stays readable until every column is done
-        float x[16];
-        const int Rd = lt >> 4, jj = lt & 15;
-        if (lt < 64) {
-          const float* bp = ws + 16 * Rd * (WLD + 1);
+        const float* bt = beta_s[par];
+        // 16 x 8 tile: acc += A B over K = 8 nk, operands rounded to tf32 from fp32 shared memory
+        auto tile_mma = [&](float (&acc)[4], const float* Ab, int lda, const float* Bb, int ldb,
+                            int nk) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float arow[16];
-#pragma unroll
-            for (int m4 = 0; m4 < 4; ++m4) {
-              const float4 v4 = *reinterpret_cast<const float4*>(bp + i * WLD + 4 * m4);
-              arow[4 * m4] = v4.x; arow[4 * m4 + 1] = v4.y; arow[4 * m4 + 2] = v4.z; arow[4 * m4 + 3] = v4.w;
+          for (int ks = 0; ks < 4; ++ks) {
+            if (ks < nk) {
+              const uint32_t a[4] = {to_tf32(Ab[g * lda + 8 * ks + t]),
+                                     to_tf32(Ab[(g + 8) * lda + 8 * ks + t]),
+                                     to_tf32(Ab[g * lda + 8 * ks + t + 4]),
+                                     to_tf32(Ab[(g + 8) * lda + 8 * ks + t + 4])};
+              const uint32_t b[2] = {to_tf32(Bb[(8 * ks + t) * ldb + g]),
+                                     to_tf32(Bb[(8 * ks + t + 4) * ldb + g])};
+              mma_tf32(acc, a, b);
             }
-            float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-            for (int m = 0; m < i; ++m) {
-              if (m & 1) acc1 = fmaf(arow[m], x[m], acc1);
-              else acc0 = fmaf(arow[m], x[m], acc0);
-            }
-            x[i] = (i == jj) ? 1.f : (i > jj ? -(acc0 + acc1) : 0.f);
           }
+        };
+        // two adjacent entries of G = T Diag(beta): row r, columns j and j + 1 (j even)
+        auto g_store = [&](int r, int j, float x0, float x1) {
+          *reinterpret_cast<uint32_t*>(sm + GB + sw128_off((uint32_t)r, (uint32_t)j)) =
+              pack_bf16(x0 * bt[j], x1 * bt[j + 1]);
+        };
+        // (1) T_RR: thread (Rd, jj) of the last two warps solves (I + A_RR) x = e_jj by column
+        //     sweeps (x_i -= A_im x_m for i > m), one fma per step on the chain through x
+        if (lt >= GROUP - 64) {
+          const int q = lt - (GROUP - 64), Rd = q >> 4, jj = q & 15;
+          const float* ab = ws + 16 * Rd * (WLD + 1);
+          float x[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[i] = i == jj ? 1.f : 0.f;
+#pragma unroll
+          for (int m = 0; m < 15; ++m)
+#pragma unroll
+            for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-ab[i * WLD + m], x[m], x[i]);
 #pragma unroll
           for (int i = 0; i < 16; ++i) trr[Rd][i][jj] = x[i];
         }
         named_sync(BAR_S, GROUP);
-        // (2) M_{R,m} = -T_RR A_{R,m} (m < R) and G_R = T_RR Diag(beta_R), as bf16 B operands of
-        // the substitution below (16 x 16 tiles, four side by side in each 2 KB swizzled panel)
-        for (int tile = sw; tile < 12; tile += GROUP / 32) {
-          const int R = tile < 2 ? 1 : (tile < 6 ? 2 : 3);
-          const int nt = tile - (R == 1 ? 0 : (R == 2 ? 2 : 6));  // 8-column slice of A_{R,<16R}
-          const float* ar = ws + 16 * R * WLD + 8 * nt;
-          // one tf32 product per k step: the result is rounded to bf16 right after, so tf32's
-          // 10-bit mantissa already exceeds what is kept
+        // (2) Y_10 = A_10 T_00 and Y_32 = A_32 T_22 side by side in qs (warps 0-3); the T_RR into the
+        //     diagonal blocks of WS, whose A_RR is no longer read (warps 4-7)
+        if (sw < 4) {
+          const int tile = sw >> 1, nh = sw & 1;
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma(acc, ws + (16 + 32 * tile) * WLD + 32 * tile, WLD, &trr[2 * tile][0][8 * nh], 17, 2);
+          float* y = qs + 16 * tile + 8 * nh + 2 * t;
+          y[g * WLD] = acc[0];
+          y[g * WLD + 1] = acc[1];
+          y[(g + 8) * WLD] = acc[2];
+          y[(g + 8) * WLD + 1] = acc[3];
+        } else {
 #pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            const uint32_t a[4] = {to_tf32(trr[R][g][8 * ks + t]), to_tf32(trr[R][g + 8][8 * ks + t]),
-                                   to_tf32(trr[R][g][8 * ks + t + 4]), to_tf32(trr[R][g + 8][8 * ks + t + 4])};
-            const uint32_t b[2] = {to_tf32(ar[(8 * ks + t) * WLD + g]), to_tf32(ar[(8 * ks + t + 4) * WLD + g])};
-            mma_tf32(acc, a, b);
+          for (int e = lt - 128; e < 1024; e += 128) {
+            const int R = e >> 8, i = (e >> 4) & 15, j = e & 15;
+            ws[(16 * R + i) * WLD + 16 * R + j] = trr[R][i][j];
           }
-          const int sidx = m_tile(R, nt >> 1);
-          const int col = 16 * (sidx & 3) + 8 * (nt & 1) + 2 * t;
-          uint8_t* panel = sm + SUB + 2048u * (uint32_t)(sidx >> 2);
-          *reinterpret_cast<uint32_t*>(panel + sw128_off(g, col)) = pack_bf16(-acc[0], -acc[1]);
-          *reinterpret_cast<uint32_t*>(panel + sw128_off(g + 8, col)) = pack_bf16(-acc[2], -acc[3]);
         }
-        if (lt < 64) {  // G_R row i: T_RR[i][j] beta_{16 R + j}
-          const int R = lt >> 4, i = lt & 15;
-          const int sidx = g_tile(R);
-          uint8_t* panel = sm + SUB + 2048u * (uint32_t)(sidx >> 2);
-          float gv[16];
+        named_sync(BAR_S, GROUP);
+        // (3) T_10 = -T_11 Y_10 and T_32 = -T_33 Y_32 into WS (warps 0-3); G of the diagonal
+        //     blocks (warps 4-7)
+        if (sw < 4) {
+          const int tile = sw >> 1, nh = sw & 1;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma(acc, &trr[2 * tile + 1][0][0], 17, qs + 16 * tile + 8 * nh, WLD, 2);
+          float* o = ws + (16 + 32 * tile) * WLD + 32 * tile + 8 * nh + 2 * t;
+          o[g * WLD] = -acc[0];
+          o[g * WLD + 1] = -acc[1];
+          o[(g + 8) * WLD] = -acc[2];
+          o[(g + 8) * WLD + 1] = -acc[3];
+        } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) gv[j] = trr[R][i][j] * beta_s[par][16 * R + j];
-          st_shared_v4(smem_u32(panel) + sw128_off(i, 16 * (sidx & 3)), pack_bf16(gv[0], gv[1]),
-                       pack_bf16(gv[2], gv[3]), pack_bf16(gv[4], gv[5]), pack_bf16(gv[6], gv[7]));
-          st_shared_v4(smem_u32(panel) + sw128_off(i, 16 * (sidx & 3) + 8), pack_bf16(gv[8], gv[9]),
-                       pack_bf16(gv[10], gv[11]), pack_bf16(gv[12], gv[13]), pack_bf16(gv[14], gv[15]));
+          for (int e = lt - 128; e < 512; e += 128) {
+            const int R = e >> 7, i = (e >> 3) & 15, jp = 2 * (e & 7);
+            g_store(16 * R + i, 16 * R + jp, trr[R][i][jp], trr[R][i][jp + 1]);
+          }
+        }
+        named_sync(BAR_S, GROUP);
+        // (4) Q = A_(32)10 T_(32)00 (rows 32..63 x columns 0..31, K 32) into qs; G of T_10, T_32
+        {
+          const int mt = sw >> 2, nt = sw & 3;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma(acc, ws + (32 + 16 * mt) * WLD, WLD, ws + 8 * nt, WLD, 4);
+          float* o = qs + 16 * mt * WLD + 8 * nt + 2 * t;
+          o[g * WLD] = acc[0];
+          o[g * WLD + 1] = acc[1];
+          o[(g + 8) * WLD] = acc[2];
+          o[(g + 8) * WLD + 1] = acc[3];
+          const int tile = lt >> 7, i = (lt >> 3) & 15, jp = 2 * (lt & 7);
+          const int r = 16 + 32 * tile + i, j = 32 * tile + jp;
+          g_store(r, j, ws[r * WLD + j], ws[r * WLD + j + 1]);
+        }
+        named_sync(BAR_S, GROUP);
+        // (5) G rows 32..63, columns 0..31: T_(32)10 = -T_(32)11 Q
+        {
+          const int mt = sw >> 2, nt = sw & 3;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma(acc, ws + (32 + 16 * mt) * WLD + 32, WLD, qs + 8 * nt, WLD, 4);
+          const int r = 32 + 16 * mt + g, j = 8 * nt + 2 * t;
+          g_store(r, j, -acc[0], -acc[1]);
+          g_store(r + 8, j, -acc[2], -acc[3]);
         }
       }
-      fence_proxy_async_smem();
+      fence_proxy_async_smem();  // G is a tensor-core operand
       tmem_st_wait();
       tc_fence_before();
       if (!group_wait2(&bar_v, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       pend_v = false;
-      if (leader) mbar_arrive(&bar_wsfree);  // A has been read out of WS (T_RR, M, G are made)
-      // ---------------- block forward substitution on the tensor cores, R = 0..3 (M 128, N 16):
-      //   U_R^T = V_R^T G_R^T - Z_R^T G_R^T + sum_{m<R} U_m^T M_{R,m}^T,   U_R^T -> bf16
-      // which is U = T Diag(beta) (V - Z) solved block by block: (I + A) U = Diag(beta)(V - Z)
-      for (int R = 0; R < 4; ++R) {
-        if (leader) {
-          tc_fence_after();
-          const uint32_t id_v = idesc_bf16(128, 16, 1, 0, 0);
-          const uint32_t id_z = idesc_bf16(128, 16, 0, 0, 1);
-          const uint32_t id_u = idesc_bf16(128, 16, 0, 0, 0);
-          const uint32_t d = tmem + T_UT + 16u * R;
-          const uint64_t bg = sub_desc(sb, g_tile(R));
-          umma_bf16(d, desc_sw128(sb + IN_V + 2048u * R, BOX_BYTES, 1024), bg, id_v, 0);
-          umma_bf16_tmem_a(d, tmem + T_ZB + 8u * R, bg, id_z, 1);
-          for (int m = 0; m < R; ++m)
-            umma_bf16_tmem_a(d, tmem + T_UB + 8u * m, sub_desc(sb, m_tile(R, m)), id_u, 1);
-          umma_commit(&bar_G2);
-        }
-        pend_mma = true; last_mma = &bar_G2; last_par = (uint32_t)(R & 1);
-        if (!group_wait2(&bar_G2, (uint32_t)(R & 1), nullptr, 0, BAR_S)) { aborted = true; break; }
-        pend_mma = false;
+      if (leader) mbar_arrive(&bar_wsfree);  // WS is no longer read
+      // ---------------- tcgen05: U^T = V^T G^T - Z^T G^T (M 128, N 64, K 64), which is
+      // U = T Diag(beta) (V - Z), the solution of (I + A) U = Diag(beta) (V - Z)
+      if (leader) {
         tc_fence_after();
-        if (hh == 0) {  // U_R^T (lane v, 16 tokens) -> bf16 A operand
-          uint32_t v[16], ub[8];
-          tmem_ld16(tl + T_UT + 16u * R, v);
-          tmem_ld_wait();
+        const uint32_t id_v = idesc_bf16(128, 64, 1, 0, 0);
+        const uint32_t id_z = idesc_bf16(128, 64, 0, 0, 1);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) ub[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-          tmem_st8(tl + T_UB + 8u * R, ub);
-          tmem_st_wait();
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bg = desc_sw128(sb + GB + 32u * kk, 16, 1024);
+          umma_bf16(tmem + T_UT, desc_sw128(sb + IN_V + 2048u * kk, BOX_BYTES, 1024), bg, id_v, kk > 0);
+          umma_bf16_tmem_a(tmem + T_UT, tmem + T_ZB + 8u * kk, bg, id_z, 1);
         }
-        tc_fence_before();
-        named_sync(BAR_S, GROUP);
+        umma_commit(&bar_G2);
       }
+      pend_mma = true; last_mma = &bar_G2; last_par = ph;
+      if (!group_wait2(&bar_G2, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
+      pend_mma = false;
+      tc_fence_after();
+      {  // U^T (lane v, tokens 32 hh ..) -> bf16 A operand, over Z^T bf16 (read by the product)
+        uint32_t v[32], ub[16];
+        tmem_ld32(tl + T_UT + 32 * hh, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ub[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+        tmem_st16(tl + T_UB + 16 * hh, ub);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      named_sync(BAR_S, GROUP);
       if (aborted) break;
       if (blk + 1 < nblocks) {  // the v tile is dead
         if (leader) issue_v(blk + 1);
@@ -701,14 +764,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       // ---------------- bf16 copy of the new state for the next block (group P writes O)
       {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t v[32], sbf[16];
-          tmem_ld32(tl + T_ST + 64 * hh + 32 * half, v);
+#pragma unroll 1
+        for (int part = 0; part < 4; ++part) {
+          uint32_t v[16], sbf[8];
+          tmem_ld16(tl + T_ST + 64 * hh + 16 * part, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) sbf[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-          tmem_st16(tl + T_SB + 32 * hh + 16 * half, sbf);
+          for (int j = 0; j < 8; ++j) sbf[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+          tmem_st8(tl + T_SB + 32 * hh + 8 * part, sbf);
         }
         tmem_st_wait();
       }
