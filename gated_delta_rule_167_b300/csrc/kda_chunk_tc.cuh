@@ -227,23 +227,34 @@ __global__ void __launch_bounds__(THREADS, 1)
     unsigned short beta_next = 0;
     if (lt < C && lt < len) beta_next = beta_u[(row0 + lt) * H + h];
     __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(P.out);
-    // O of block b straight from TMEM (lane v = c, tokens 32 hh .. 32 hh + 31)
+    // O of block b: TMEM (lane v = c, tokens 32 hh .. 32 hh + 31) -> bf16 rows [token][128]
+    // staged in XK (free: this group's A/P product of the block after b has completed, and the
+    // next operands are written after the group's closing barrier) -> 16-byte global stores,
+    // each warp writing two whole 256-byte rows
     auto emit_o = [&](int b) {
       const int tb = b * C;
       const int nb = min(C, len - tb);
-      __nv_bfloat16* op = out + ((row0 + tb) * H + h) * D + c;
+      uint8_t* stg = sm + XK;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         uint32_t v[16];
         tmem_ld16(tl + T_OT + 64u * (uint32_t)(b & 1) + 32 * hh + 16 * part, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = 32 * hh + 16 * part + j;
-          if (r < nb) op[(size_t)r * H * D] = __float2bfloat16_rn(__uint_as_float(v[j]));
-        }
+        for (int j = 0; j < 16; ++j)
+          *reinterpret_cast<__nv_bfloat16*>(stg + (32 * hh + 16 * part + j) * 256 + 2 * c) =
+              __float2bfloat16_rn(__uint_as_float(v[j]));
       }
       tc_fence_before();
+      named_sync(BAR_P, GROUP);
+      const int q = lt & 15;  // 16-byte chunk of a row; rows lt / 16 + 16 i
+      __nv_bfloat16* ob = out + ((row0 + tb + (lt >> 4)) * H + h) * D + 8 * q;
+      const uint8_t* sp = stg + (lt >> 4) * 256 + 16 * q;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if ((lt >> 4) + 16 * i < nb)
+          *reinterpret_cast<uint4*>(ob + (size_t)(16 * i) * H * D) =
+              *reinterpret_cast<const uint4*>(sp + 4096 * i);
     };
 
     for (int blk = 0; blk < nblocks; ++blk) {
@@ -556,12 +567,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       pend_mma = true; last_mma = &bar_ZO; last_par = ph;
       // ---------------- meanwhile: S^T <- S^T Diag(e^{Gamma_L}) (the product above reads the
-      // bf16 copy; Khat^T U accumulates onto this one)
-      {
+      // bf16 copy; Khat^T U accumulates onto this one). The issuing thread's warp waits while its
+      // products enter the tensor pipe, so the warp of the same lane quarter in the other half
+      // scales all 128 columns of those lanes.
+      if (lt >= 32) {
+        const bool both = lt >= 128 && lt < 160;  // lane quarter 0, second half
+        const int np = both ? 8 : 4;
+        const int cb = both ? 0 : 64 * hh;
         uint32_t v[16];
 #pragma unroll 1
-        for (int part = 0; part < 4; ++part) {
-          const int c0 = 64 * hh + 16 * part;
+        for (int part = 0; part < np; ++part) {
+          const int c0 = cb + 16 * part;
           tmem_ld16(tl + T_ST + c0, v);
           tmem_ld_wait();
 #pragma unroll
@@ -638,67 +654,75 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int i = 0; i < 16; ++i) trr[Rd][i][jj] = x[i];
         }
         named_sync(BAR_S, GROUP);
-        // (2) Y_10 = A_10 T_00 and Y_32 = A_32 T_22 side by side in qs (warps 0-3); the T_RR into the
-        //     diagonal blocks of WS, whose A_RR is no longer read (warps 4-7)
-        if (sw < 4) {
-          const int tile = sw >> 1, nh = sw & 1;
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          tile_mma(acc, ws + (16 + 32 * tile) * WLD + 32 * tile, WLD, &trr[2 * tile][0][8 * nh], 17, 2);
-          float* y = qs + 16 * tile + 8 * nh + 2 * t;
-          y[g * WLD] = acc[0];
-          y[g * WLD + 1] = acc[1];
-          y[(g + 8) * WLD] = acc[2];
-          y[(g + 8) * WLD + 1] = acc[3];
-        } else {
+        // (2) warp h (0, 1), one per 32-row half: Y = A_10 T_00 (16 x 16, into qs), then
+        //     T_10 = -T_11 Y into WS (h = 1: A_32, T_22, T_33, T_32); warps 2-7: the T_RR into the
+        //     diagonal blocks of WS, whose A_RR is no longer read, and G of the diagonal blocks
+        if (sw < 2) {
+          const int tile = sw;
+          float* y = qs + 16 * tile;
 #pragma unroll
-          for (int e = lt - 128; e < 1024; e += 128) {
+          for (int nh = 0; nh < 2; ++nh) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            tile_mma(acc, ws + (16 + 32 * tile) * WLD + 32 * tile, WLD, &trr[2 * tile][0][8 * nh], 17, 2);
+            float* yo = y + 8 * nh + 2 * t;
+            yo[g * WLD] = acc[0];
+            yo[g * WLD + 1] = acc[1];
+            yo[(g + 8) * WLD] = acc[2];
+            yo[(g + 8) * WLD + 1] = acc[3];
+          }
+          __syncwarp();
+#pragma unroll
+          for (int nh = 0; nh < 2; ++nh) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            tile_mma(acc, &trr[2 * tile + 1][0][0], 17, y + 8 * nh, WLD, 2);
+            float* o = ws + (16 + 32 * tile) * WLD + 32 * tile + 8 * nh + 2 * t;
+            o[g * WLD] = -acc[0];
+            o[g * WLD + 1] = -acc[1];
+            o[(g + 8) * WLD] = -acc[2];
+            o[(g + 8) * WLD + 1] = -acc[3];
+          }
+        } else {
+          for (int e = lt - 64; e < 1024; e += GROUP - 64) {
             const int R = e >> 8, i = (e >> 4) & 15, j = e & 15;
             ws[(16 * R + i) * WLD + 16 * R + j] = trr[R][i][j];
           }
-        }
-        named_sync(BAR_S, GROUP);
-        // (3) T_10 = -T_11 Y_10 and T_32 = -T_33 Y_32 into WS (warps 0-3); G of the diagonal
-        //     blocks (warps 4-7)
-        if (sw < 4) {
-          const int tile = sw >> 1, nh = sw & 1;
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          tile_mma(acc, &trr[2 * tile + 1][0][0], 17, qs + 16 * tile + 8 * nh, WLD, 2);
-          float* o = ws + (16 + 32 * tile) * WLD + 32 * tile + 8 * nh + 2 * t;
-          o[g * WLD] = -acc[0];
-          o[g * WLD + 1] = -acc[1];
-          o[(g + 8) * WLD] = -acc[2];
-          o[(g + 8) * WLD + 1] = -acc[3];
-        } else {
-#pragma unroll
-          for (int e = lt - 128; e < 512; e += 128) {
+          for (int e = lt - 64; e < 512; e += GROUP - 64) {
             const int R = e >> 7, i = (e >> 3) & 15, jp = 2 * (e & 7);
             g_store(16 * R + i, 16 * R + jp, trr[R][i][jp], trr[R][i][jp + 1]);
           }
         }
         named_sync(BAR_S, GROUP);
-        // (4) Q = A_(32)10 T_(32)00 (rows 32..63 x columns 0..31, K 32) into qs; G of T_10, T_32
-        {
-          const int mt = sw >> 2, nt = sw & 3;
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          tile_mma(acc, ws + (32 + 16 * mt) * WLD, WLD, ws + 8 * nt, WLD, 4);
-          float* o = qs + 16 * mt * WLD + 8 * nt + 2 * t;
-          o[g * WLD] = acc[0];
-          o[g * WLD + 1] = acc[1];
-          o[(g + 8) * WLD] = acc[2];
-          o[(g + 8) * WLD + 1] = acc[3];
-          const int tile = lt >> 7, i = (lt >> 3) & 15, jp = 2 * (lt & 7);
-          const int r = 16 + 32 * tile + i, j = 32 * tile + jp;
-          g_store(r, j, ws[r * WLD + j], ws[r * WLD + j + 1]);
-        }
-        named_sync(BAR_S, GROUP);
-        // (5) G rows 32..63, columns 0..31: T_(32)10 = -T_(32)11 Q
-        {
-          const int mt = sw >> 2, nt = sw & 3;
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          tile_mma(acc, ws + (32 + 16 * mt) * WLD + 32, WLD, qs + 8 * nt, WLD, 4);
-          const int r = 32 + 16 * mt + g, j = 8 * nt + 2 * t;
-          g_store(r, j, -acc[0], -acc[1]);
-          g_store(r + 8, j, -acc[2], -acc[3]);
+        // (3) warp nt (0-3): columns 8 nt .. 8 nt + 7 of Q = A_(32)10 T_(32)00 (rows 32..63 x
+        //     columns 0..31, K 32; into qs), then of G rows 32..63: T_(32)10 = -T_(32)11 Q;
+        //     warps 4-7: G of T_10 and T_32
+        if (sw < 4) {
+          const int nt = sw;
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            tile_mma(acc, ws + (32 + 16 * mt) * WLD, WLD, ws + 8 * nt, WLD, 4);
+            float* o = qs + 16 * mt * WLD + 8 * nt + 2 * t;
+            o[g * WLD] = acc[0];
+            o[g * WLD + 1] = acc[1];
+            o[(g + 8) * WLD] = acc[2];
+            o[(g + 8) * WLD + 1] = acc[3];
+          }
+          __syncwarp();
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            tile_mma(acc, ws + (32 + 16 * mt) * WLD + 32, WLD, qs + 8 * nt, WLD, 4);
+            const int r = 32 + 16 * mt + g, j = 8 * nt + 2 * t;
+            g_store(r, j, -acc[0], -acc[1]);
+            g_store(r + 8, j, -acc[2], -acc[3]);
+          }
+        } else {
+#pragma unroll
+          for (int e = lt - 128; e < 256; e += 128) {
+            const int tile = e >> 7, i = (e >> 3) & 15, jp = 2 * (e & 7);
+            const int r = 16 + 32 * tile + i, j = 32 * tile + jp;
+            g_store(r, j, ws[r * WLD + j], ws[r * WLD + j + 1]);
+          }
         }
       }
       fence_proxy_async_smem();  // G is a tensor-core operand
