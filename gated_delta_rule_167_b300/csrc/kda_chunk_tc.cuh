@@ -147,7 +147,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   __shared__ uint32_t tmem_base_s;
   __shared__ __align__(16) float beta_s[2][C];  // by block parity
   __shared__ __align__(16) float gl_s[2][D];    // e^{Gamma_L} per key channel, by block parity
-  __shared__ float xch[4][D];                   // sub-block sums of g (group P)
   __shared__ float trr[4][16][17];              // diagonal blocks T_RR of the solve (group S)
 
   const int tid = threadIdx.x;
@@ -157,7 +156,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int lt = tid & (GROUP - 1);  // index inside the group
   const int c = lt & (D - 1);        // channel (= TMEM lane) owned in the elementwise phases
   const int hh = lt >> 7;            // which half this thread handles inside its group
-  const int g = (tid & 31) >> 2, t = tid & 3;  // m16n8k8 fragment coordinates
+  const int lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;  // mma fragment coordinates
 
   int h, len;
   size_t row0;
@@ -275,117 +275,119 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!group_wait2(&bar_in, blk & 1, nullptr, 0, BAR_P)) { aborted = true; break; }
       pend_in = false;
-      // ---------------- sums of g (log2 domain) over this thread's sub-blocks hh and 2 + hh
-      const uint8_t* gp = sm + IN_G + (c >> 6) * BOX_BYTES;
-#pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        float gv[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) gv[i] = ld_bf16(gp, sw128_off(16 * (2 * a + hh) + i, c & 63));
-        float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-          acc0 += 16 * (2 * a + hh) + i < n ? gv[i] : 0.f;
-          acc1 += 16 * (2 * a + hh) + i + 1 < n ? gv[i + 1] : 0.f;
-        }
-        xch[2 * a + hh][c] = (acc0 + acc1) * LOG2E;
-      }
-      named_sync(BAR_P, GROUP);
-      const float s0 = xch[0][c], s1 = xch[1][c], s2 = xch[2][c], s3 = xch[3][c];
-      const float b2 = s0 + s1, rhoB = b2 + s2, gL = rhoB + s3;  // rho_A = s0
-      if (hh == 0) gl_s[par][c] = ex2(gL);
       // ---------------- operands: X, Y, (K e^Gamma)^T, (Q e^Gamma)^T; Khat^T kept packed
-      // Two exponentials per element, of the running sum inside the sub-block and its negative:
-      //   u_r = e^{Gamma_r - Gamma_{rb-1}},  w_r = e^{Gamma_{rb-1} - Gamma_r}   (rb = first token)
-      // and every factor is one of these times an anchor, an exponential of a sum of g over whole
-      // sub-blocks. Where an anchor may underflow it is <= 1 and multiplies a factor <= 1, so a
-      // product flushes to zero only when its own value is below the fp32 range.
-      uint32_t khA[8], khB[8];  // Khat^T of sub-blocks hh and 2 + hh, bf16 pairs
+      // Warp w covers channels 16 w .. 16 w + 15 (channel group cg = 0, 1 of 8) over all 64 tokens:
+      // lane (g, t) holds, for each 8-token block m, the tokens 8 m + 2 t, 8 m + 2 t + 1 of
+      // channels 16 w + 8 cg + g as bf16 pairs (transposed 8 x 8 loads of the [token][channel]
+      // tiles), which is the mma A-fragment layout of g^T and the row layout of the [channel]
+      // [token] operands written back with matrix stores. The running sums of g inside each
+      // 16-token sub-block R come from warp MMAs with a triangular matrix of ones:
+      //   L_r = Gamma_r - Gamma_{16R-1} = sum_{16R <= j <= r} g_j
+      // Every factor is e^{+-L} times an anchor, an exponential of a sum of g over whole
+      // sub-blocks (two exponentials per element). Where an anchor may underflow it is <= 1 and
+      // multiplies a factor <= 1, so a product flushes to zero only when its own value is below
+      // the fp32 range.
+      uint32_t kh[2][8];  // Khat^T: [channel group][8-token block], bf16 pairs
       {
-        const uint8_t* kp = sm + IN_K + (c >> 6) * BOX_BYTES;
-        const uint8_t* qp = sm + IN_Q + (c >> 6) * BOX_BYTES;
-#pragma unroll 1
-        for (int a = 0; a < 2; ++a) {
-          const int R = 2 * a + hh;  // a = 0: first half (reference rho_A), a = 1: second
-          // anchors e^{Gamma_{rb-1}}, e^{Gamma_L - Gamma_{rb+15}}, e^{rho_B - Gamma_{rb+15}} and the
-          // sub-block's own e^{+-(Gamma_{rb+15} - Gamma_{rb-1})}
-          float before, after, tob, sR;
-          if (a == 0) {
-            before = hh ? s0 : 0.f;
-            after = hh ? s2 + s3 : s1 + s2 + s3;
-            tob = hh ? s2 : s1 + s2;
-            sR = hh ? s1 : s0;
-          } else {
-            before = hh ? rhoB : b2;
-            after = hh ? 0.f : s3;
-            tob = 0.f;
-            sR = hh ? s3 : s2;
+        const int cw = 16 * warp;  // first channel of this warp
+        const uint32_t boxo = (uint32_t)(cw >> 6) * BOX_BYTES, cin = (uint32_t)(cw & 63);
+        const int lr = lane & 7, li = lane >> 3;  // row and matrix of this lane's matrix address
+        auto live = [&](int m) -> uint32_t {      // keeps the tokens of block m that exist
+          const int r = 8 * m + 2 * t;
+          return (r < n ? 0x0000FFFFu : 0u) | (r + 1 < n ? 0xFFFF0000u : 0u);
+        };
+        // g^T as A fragments of k step R: {cg 0 | cg 1} x {tokens 16R .. +7 | 16R + 8 .. +15}
+        uint32_t ga[4][4];
+#pragma unroll
+        for (int R = 0; R < 4; ++R) {
+          ldsm_x4_trans(sb + IN_G + boxo + sw128_off(16 * R + 8 * (li >> 1) + lr, cin + 8 * (li & 1)), ga[R]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) ga[R][i] &= live(2 * R + (i >> 1));
+        }
+        // Lr[R][e]: tokens 16 R + 8 e + 2t (+1) of channel groups 0 (regs 0, 1) and 1 (regs 2, 3),
+        // from U_e[j][r] = 1 if j <= 8 e + r (j: token in the sub-block, r: token in the 8-block)
+        const uint32_t tri = ((2 * t <= g) ? 0x3F80u : 0u) | ((2 * t + 1 <= g) ? 0x3F800000u : 0u);
+        float Lr[4][2][4];
+#pragma unroll
+        for (int R = 0; R < 4; ++R)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const uint32_t bu[2] = {e ? 0x3F803F80u : tri, e ? tri : 0u};
+            Lr[R][e][0] = Lr[R][e][1] = Lr[R][e][2] = Lr[R][e][3] = 0.f;
+            mma_bf16_16816(Lr[R][e], ga[R], bu);
           }
-          const float eb = ex2(before), ea = ex2(after), et = ex2(tob), es = ex2(sR);
-          const float2 aG = make_float2(eb, eb), aH = make_float2(ea, ea), aY = make_float2(et, et);
-          const float2 cS = make_float2(es, es);
-          // the sub-block ends at rho (hh = 0) or starts right after it (hh = 1)
-          const float cf = hh ? 1.f : ex2(-sR);
-          const float2 cF = make_float2(cf, cf);
-          float acc = 0.f;  // Gamma_r - Gamma_{rb-1}, log2 units
+        // sub-block sums (log2 units): token 16 R + 15 is held by lane t = 3
+        float sg[2][4];
 #pragma unroll
-          for (int gi = 0; gi < 2; ++gi) {
-            const int r0 = 16 * R + 8 * gi;  // first token of these 8 rows
-            float G[8], kv[8], qv[8];
+        for (int R = 0; R < 4; ++R)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const uint32_t o = sw128_off(r0 + e, c & 63);
-              G[e] = ld_bf16(gp, o);
-              kv[e] = ld_bf16(kp, o);
-              qv[e] = ld_bf16(qp, o);
-            }
+          for (int cg = 0; cg < 2; ++cg)
+            sg[cg][R] = __shfl_sync(0xffffffffu, Lr[R][1][2 * cg + 1], (lane & ~3) | 3) * LOG2E;
+        if (t == 0) {  // e^{Gamma_L} per key channel for the state decay
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const bool live = r0 + e < n;
-              acc = fmaf(live ? G[e] : 0.f, LOG2E, acc);
-              G[e] = acc;
-              kv[e] = live ? kv[e] : 0.f;
-              qv[e] = live ? qv[e] : 0.f;
-            }
-            uint32_t xk[4], xq[4], y[4], yb[4], kg[4], qg[4];  // bf16 pairs
+          for (int cg = 0; cg < 2; ++cg)
+            gl_s[par][cw + 8 * cg + g] = ex2(sg[cg][0] + sg[cg][1] + sg[cg][2] + sg[cg][3]);
+        }
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const float L0 = G[2 * w], L1 = G[2 * w + 1];
+        for (int cg = 0; cg < 2; ++cg) {
+          const float s0 = sg[cg][0], s1 = sg[cg][1], s2 = sg[cg][2], s3 = sg[cg][3];
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {  // tokens 32 hf .. 32 hf + 31: sub-blocks 2 hf, 2 hf + 1
+            uint32_t kw[4], qw[4];
+            const uint32_t lo = boxo + sw128_off(32 * hf + 8 * li + lr, cin + 8 * cg);
+            ldsm_x4_trans(sb + IN_K + lo, kw);
+            ldsm_x4_trans(sb + IN_Q + lo, qw);
+            uint32_t oxk[4], oxq[4], oy[4], oyb[4], okg[4], oqg[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int m = 4 * hf + i, R = m >> 1, e = m & 1;
+              const bool odd = R & 1;  // sub-block starts right after its reference (else ends at it)
+              const uint32_t lv = live(m);
+              kw[i] &= lv;
+              qw[i] &= lv;
+              // anchors e^{Gamma_{16R-1}}, e^{Gamma_L - Gamma_{16R+15}}, e^{rho_B - Gamma_{16R+15}},
+              // e^{+-(Gamma_{16R+15} - Gamma_{16R-1})}
+              const float before = R == 0 ? 0.f : (R == 1 ? s0 : (R == 2 ? s0 + s1 : s0 + s1 + s2));
+              const float after = R == 0 ? s1 + s2 + s3 : (R == 1 ? s2 + s3 : (R == 2 ? s3 : 0.f));
+              const float tob = R == 0 ? s1 + s2 : s2;
+              const float sR = R == 0 ? s0 : (R == 1 ? s1 : (R == 2 ? s2 : s3));
+              const float eb = R == 0 ? 1.f : ex2(before), ea = R == 3 ? 1.f : ex2(after);
+              const float es = ex2(sR), ef = odd ? 1.f : ex2(-sR);
+              const float L0 = Lr[R][e][2 * cg] * LOG2E, L1 = Lr[R][e][2 * cg + 1] * LOG2E;
               const float2 u = make_float2(ex2(L0), ex2(L1));
               const float2 wv = make_float2(ex2(-L0), ex2(-L1));
-              const float2 sfx = mul2(cS, wv);   // e^{Gamma_{rb+15} - Gamma}
-              const float2 F = mul2(cF, u);      // e^{Gamma - rho}
-              const float2 Fi = hh ? wv : sfx;   // e^{rho - Gamma}
-              const float2 eG = mul2(aG, u);     // e^{Gamma}
-              const float2 eH = mul2(aH, sfx);   // e^{Gamma_L - Gamma}
-              const float2 k2 = make_float2(kv[2 * w], kv[2 * w + 1]);
-              const float2 q2 = make_float2(qv[2 * w], qv[2 * w + 1]);
+              const float2 sfx = mul2(make_float2(es, es), wv);  // e^{Gamma_{16R+15} - Gamma}
+              const float2 F = mul2(make_float2(ef, ef), u);     // e^{Gamma - rho}
+              const float2 Fi = odd ? wv : sfx;                  // e^{rho - Gamma}
+              const float2 eG = mul2(make_float2(eb, eb), u);    // e^{Gamma}
+              const float2 eH = mul2(make_float2(ea, ea), sfx);  // e^{Gamma_L - Gamma}
+              const float2 k2 = make_float2(__uint_as_float(kw[i] << 16), __uint_as_float(kw[i] & 0xffff0000u));
+              const float2 q2 = make_float2(__uint_as_float(qw[i] << 16), __uint_as_float(qw[i] & 0xffff0000u));
               const float2 xk2 = mul2(k2, F), xq2 = mul2(q2, F), y2 = mul2(k2, Fi);
               const float2 kg2 = mul2(k2, eG), qg2 = mul2(q2, eG), kh2 = mul2(k2, eH);
-              xk[w] = pack_bf16(xk2.x, xk2.y);
-              xq[w] = pack_bf16(xq2.x, xq2.y);
-              y[w] = pack_bf16(y2.x, y2.y);
-              kg[w] = pack_bf16(kg2.x, kg2.y);
-              qg[w] = pack_bf16(qg2.x, qg2.y);
-              const uint32_t khw = pack_bf16(kh2.x, kh2.y);
-              if (a == 0) {
-                const float2 yb2 = mul2(k2, mul2(aY, sfx));  // k e^{rho_B - Gamma}
-                yb[w] = pack_bf16(yb2.x, yb2.y);
-                khA[4 * gi + w] = khw;
-              } else {
-                khB[4 * gi + w] = khw;
+              oxk[i] = pack_bf16(xk2.x, xk2.y);
+              oxq[i] = pack_bf16(xq2.x, xq2.y);
+              oy[i] = pack_bf16(y2.x, y2.y);
+              okg[i] = pack_bf16(kg2.x, kg2.y);
+              oqg[i] = pack_bf16(qg2.x, qg2.y);
+              kh[cg][m] = pack_bf16(kh2.x, kh2.y);
+              if (hf == 0) {
+                const float et = ex2(tob);
+                const float2 yb2 = mul2(k2, mul2(make_float2(et, et), sfx));  // k e^{rho_B - Gamma}
+                oyb[i] = pack_bf16(yb2.x, yb2.y);
               }
             }
-            const uint32_t o = sw128_off(c, r0);
-            st_words4(sb + XK + o, xk);
-            st_words4(sb + XQ + o, xq);
-            st_words4(sb + KG + o, kg);
-            st_words4(sb + QG + o, qg);
-            if (a == 0) {
-              st_words4(sb + YP + 16384u + o, y);  // Y_A (panel 1, columns 64 + r)
-              st_words4(sb + YP + o, yb);           // Y_B (panel 0)
+            // rows: channel cw + 8 cg + lr; 16-byte chunk: 8-token block 4 hf + li
+            const uint32_t so = sw128_off((uint32_t)(cw + 8 * cg + lr), (uint32_t)(8 * (4 * hf + li)));
+            stsm_x4(sb + XK + so, oxk[0], oxk[1], oxk[2], oxk[3]);
+            stsm_x4(sb + XQ + so, oxq[0], oxq[1], oxq[2], oxq[3]);
+            stsm_x4(sb + KG + so, okg[0], okg[1], okg[2], okg[3]);
+            stsm_x4(sb + QG + so, oqg[0], oqg[1], oqg[2], oqg[3]);
+            if (hf == 0) {
+              stsm_x4(sb + YP + 16384u + so, oy[0], oy[1], oy[2], oy[3]);  // Y_A (panel 1)
+              stsm_x4(sb + YP + so, oyb[0], oyb[1], oyb[2], oyb[3]);       // Y_B (panel 0)
             } else {
-              st_words4(sb + YP + o, y);            // Y_B (here e^{rho - Gamma} = e^{rho_B - Gamma})
+              stsm_x4(sb + YP + so, oy[0], oy[1], oy[2], oy[3]);  // Y_B (e^{rho - Gamma} = e^{rho_B - Gamma})
             }
           }
         }
@@ -474,16 +476,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!group_wait2(&bar_G3, (blk - 1) & 1, nullptr, 0, BAR_P)) { aborted = true; break; }
         tc_fence_after();
       }
-      {
 #pragma unroll
-        for (int a = 0; a < 2; ++a)
+      for (int cg = 0; cg < 2; ++cg)
 #pragma unroll
-          for (int gi = 0; gi < 2; ++gi) {
-            const uint32_t* kw = a == 0 ? khA : khB;
-            st_shared_v4(sb + KH + sw128_off(c, 16 * (2 * a + hh) + 8 * gi), kw[4 * gi],
-                         kw[4 * gi + 1], kw[4 * gi + 2], kw[4 * gi + 3]);
-          }
-      }
+        for (int hf = 0; hf < 2; ++hf)
+          stsm_x4(sb + KH + sw128_off((uint32_t)(16 * warp + 8 * cg + (lane & 7)), (uint32_t)(8 * (4 * hf + (lane >> 3)))),
+                  kh[cg][4 * hf], kh[cg][4 * hf + 1], kh[cg][4 * hf + 2], kh[cg][4 * hf + 3]);
       fence_proxy_async_smem();
       if (blk > 0) emit_o(blk - 1);
       named_sync(BAR_P, GROUP);

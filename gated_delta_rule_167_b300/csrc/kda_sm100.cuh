@@ -311,6 +311,37 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+// d += A B for one m16n8k16 step with bf16 operands (fragments as for tf32 above, each register
+// holding two consecutive k elements: a0 (g, 2t..2t+1), a1 (g + 8, 2t..), a2 (g, 2t + 8..),
+// a3 (g + 8, 2t + 8..); b0 (2t..2t+1, g), b1 (2t + 8.., g)).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Four 8 x 8 b16 matrices from shared memory, transposed: lanes 8i .. 8i + 7 give the addresses
+// of the 8 rows (16 bytes each) of matrix i; register i of lane (g, t) receives column g of
+// matrix i at rows 2t (low half) and 2t + 1 (high half).
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t saddr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr)
+               : "memory");
+}
+
+// Four 8 x 8 b16 matrices to shared memory: register i of lane (g, t) holds row g, columns 2t and
+// 2t + 1 of matrix i; lanes 8i .. 8i + 7 give the addresses of the 8 rows of matrix i.
+__device__ __forceinline__ void stsm_x4(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                        uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
 // d += A B for one 8-wide k step, with each operand split into a tf32 head and a tf32 tail
 // (x = hi + lo); the three products hi*hi + hi*lo + lo*hi carry about fp32 accuracy.
 __device__ __forceinline__ void mma_3xtf32(float (&d)[4], const float (&a)[4], const float (&b)[2]) {
