@@ -111,6 +111,7 @@ constexpr int Y_A = 64;
 // Row stride (floats) of the fp32 64 x 64 solve workspace: 72 makes the tf32 B-fragment loads
 // (rows t, columns g) conflict-free.
 constexpr int WLD = 72;
+constexpr int TLD = 20;  // row stride (floats) of the diagonal inverses
 struct TmaMaps {
   CUtensorMap q, k, v, g;
 };
@@ -147,7 +148,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   __shared__ uint32_t tmem_base_s;
   __shared__ __align__(16) float beta_s[2][C];  // by block parity
   __shared__ __align__(16) float gl_s[2][D];    // e^{Gamma_L} per key channel, by block parity
-  __shared__ float trr[4][16][17];              // diagonal blocks T_RR of the solve (group S)
+  // diagonal blocks T_RR of the solve (group S); rows of 20 floats: 16-byte aligned, and the
+  // eight row addresses of a matrix load fall in distinct banks
+  __shared__ __align__(16) float trr[4][16][TLD];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -616,17 +619,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int sw = warp - GROUP / 32;  // warp index inside the group
         const float* bt = beta_s[par];
         // 16 x 8 tile: acc += A B over K = 8 nk, operands rounded to tf32 from fp32 shared memory
+        // Every value of the solve is rounded to tf32 where it is written, so operands load as
+        // they are: A as four 8 x 8 b16 matrices (8 rows x 4 fp32 each: rows 0-7 / 8-15 x columns
+        // 0-3 / 4-7, which is the tf32 A fragment), B as two 32-bit loads. Ab: 16-byte aligned rows.
         auto tile_mma = [&](float (&acc)[4], const float* Ab, int lda, const float* Bb, int ldb,
                             int nk) {
+          const uint32_t ar = smem_u32(Ab) + 4u * (uint32_t)(((lane & 7) + 8 * ((lane >> 3) & 1)) * lda + 4 * (lane >> 4));
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             if (ks < nk) {
-              const uint32_t a[4] = {to_tf32(Ab[g * lda + 8 * ks + t]),
-                                     to_tf32(Ab[(g + 8) * lda + 8 * ks + t]),
-                                     to_tf32(Ab[g * lda + 8 * ks + t + 4]),
-                                     to_tf32(Ab[(g + 8) * lda + 8 * ks + t + 4])};
-              const uint32_t b[2] = {to_tf32(Bb[(8 * ks + t) * ldb + g]),
-                                     to_tf32(Bb[(8 * ks + t + 4) * ldb + g])};
+              uint32_t a[4];
+              ldsm_x4(ar + 32u * (uint32_t)ks, a);
+              const uint32_t b[2] = {__float_as_uint(Bb[(8 * ks + t) * ldb + g]),
+                                     __float_as_uint(Bb[(8 * ks + t + 4) * ldb + g])};
               mma_tf32(acc, a, b);
             }
           }
@@ -649,7 +654,27 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-ab[i * WLD + m], x[m], x[i]);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) trr[Rd][i][jj] = x[i];
+          for (int i = 0; i < 16; ++i) trr[Rd][i][jj] = tf32r(x[i]);
+        } else {
+          // meanwhile the blocks of A used below as MMA A operands (A_10, A_32 and rows 32..63 x
+          // columns 0..31) to tf32, in place: 384 float4, two per thread
+#pragma unroll
+          for (int e = lt; e < 384; e += GROUP - 64) {
+            // e < 64: A_10 (rows 16..31, 4 float4 of columns 0..15); e < 128: A_32 (rows 48..63,
+            // columns 32..47); else rows 32..63 x 8 float4 of columns 0..31
+            int row, col;
+            if (e < 128) {
+              row = 16 + 32 * (e >> 6) + ((e & 63) >> 2);
+              col = 32 * (e >> 6) + 4 * (e & 3);
+            } else {
+              row = 32 + ((e - 128) >> 3);
+              col = 4 * ((e - 128) & 7);
+            }
+            float4* pa = reinterpret_cast<float4*>(ws + row * WLD + col);
+            float4 v4 = *pa;
+            v4.x = tf32r(v4.x); v4.y = tf32r(v4.y); v4.z = tf32r(v4.z); v4.w = tf32r(v4.w);
+            *pa = v4;
+          }
         }
         named_sync(BAR_S, GROUP);
         // (2) warp h (0, 1), one per 32-row half: Y = A_10 T_00 (16 x 16, into qs), then
@@ -661,23 +686,23 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int nh = 0; nh < 2; ++nh) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            tile_mma(acc, ws + (16 + 32 * tile) * WLD + 32 * tile, WLD, &trr[2 * tile][0][8 * nh], 17, 2);
+            tile_mma(acc, ws + (16 + 32 * tile) * WLD + 32 * tile, WLD, &trr[2 * tile][0][8 * nh], TLD, 2);
             float* yo = y + 8 * nh + 2 * t;
-            yo[g * WLD] = acc[0];
-            yo[g * WLD + 1] = acc[1];
-            yo[(g + 8) * WLD] = acc[2];
-            yo[(g + 8) * WLD + 1] = acc[3];
+            yo[g * WLD] = tf32r(acc[0]);
+            yo[g * WLD + 1] = tf32r(acc[1]);
+            yo[(g + 8) * WLD] = tf32r(acc[2]);
+            yo[(g + 8) * WLD + 1] = tf32r(acc[3]);
           }
           __syncwarp();
 #pragma unroll
           for (int nh = 0; nh < 2; ++nh) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            tile_mma(acc, &trr[2 * tile + 1][0][0], 17, y + 8 * nh, WLD, 2);
+            tile_mma(acc, &trr[2 * tile + 1][0][0], TLD, y + 8 * nh, WLD, 2);
             float* o = ws + (16 + 32 * tile) * WLD + 32 * tile + 8 * nh + 2 * t;
-            o[g * WLD] = -acc[0];
-            o[g * WLD + 1] = -acc[1];
-            o[(g + 8) * WLD] = -acc[2];
-            o[(g + 8) * WLD + 1] = -acc[3];
+            o[g * WLD] = tf32r(-acc[0]);
+            o[g * WLD + 1] = tf32r(-acc[1]);
+            o[(g + 8) * WLD] = tf32r(-acc[2]);
+            o[(g + 8) * WLD + 1] = tf32r(-acc[3]);
           }
         } else {
           for (int e = lt - 64; e < 1024; e += GROUP - 64) {
@@ -700,10 +725,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             tile_mma(acc, ws + (32 + 16 * mt) * WLD, WLD, ws + 8 * nt, WLD, 4);
             float* o = qs + 16 * mt * WLD + 8 * nt + 2 * t;
-            o[g * WLD] = acc[0];
-            o[g * WLD + 1] = acc[1];
-            o[(g + 8) * WLD] = acc[2];
-            o[(g + 8) * WLD + 1] = acc[3];
+            o[g * WLD] = tf32r(acc[0]);
+            o[g * WLD + 1] = tf32r(acc[1]);
+            o[(g + 8) * WLD] = tf32r(acc[2]);
+            o[(g + 8) * WLD + 1] = tf32r(acc[3]);
           }
           __syncwarp();
 #pragma unroll

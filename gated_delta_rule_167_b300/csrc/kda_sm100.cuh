@@ -323,6 +323,19 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+// x rounded to the nearest tf32 value (ties away from zero), kept as an fp32 bit pattern.
+__device__ __forceinline__ float tf32r(float x) { return __uint_as_float(to_tf32(x)); }
+
+// Four 8 x 8 b16 matrices from shared memory: lanes 8i .. 8i + 7 give the addresses of the 8 rows
+// (16 bytes each) of matrix i; register i of lane (g, t) receives row g, columns 2t and 2t + 1
+// (as 32-bit elements: row g, element t).
+__device__ __forceinline__ void ldsm_x4(uint32_t saddr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr)
+               : "memory");
+}
+
 // Four 8 x 8 b16 matrices from shared memory, transposed: lanes 8i .. 8i + 7 give the addresses
 // of the 8 rows (16 bytes each) of matrix i; register i of lane (g, t) receives column g of
 // matrix i at rows 2t (low half) and 2t + 1 (high half).
