@@ -472,6 +472,46 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       fence_proxy_async_smem();  // P is a tensor-core operand of S's last product
       named_sync(BAR_P, GROUP);
+      // ---------------- first step of the solve of T = (I + A)^{-1}, which needs A only: the
+      // 16 x 16 diagonal inverses T_RR (fp32, rounded to tf32 into trr; the state group reads trr
+      // from bar_ext until it releases WS), and the blocks of A that the state group uses as MMA
+      // A operands rounded to tf32 in place
+      {
+        float* ws = reinterpret_cast<float*>(sm + WS);
+        if (lt >= GROUP - 64) {
+          // thread (Rd, jj) of the last two warps solves (I + A_RR) x = e_jj by column sweeps
+          // (x_i -= A_im x_m for i > m), one fma per step on the chain through x
+          const int q = lt - (GROUP - 64), Rd = q >> 4, jj = q & 15;
+          const float* ab = ws + 16 * Rd * (WLD + 1);
+          float x[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[i] = i == jj ? 1.f : 0.f;
+#pragma unroll
+          for (int m = 0; m < 15; ++m)
+#pragma unroll
+            for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-ab[i * WLD + m], x[m], x[i]);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) trr[Rd][i][jj] = tf32r(x[i]);
+        } else {
+          // A_10, A_32 and rows 32..63 x columns 0..31: 384 float4, two per thread
+#pragma unroll
+          for (int e = lt; e < 384; e += GROUP - 64) {
+            int row, col;
+            if (e < 128) {  // e < 64: A_10 (rows 16..31, columns 0..15); else A_32 (48.., 32..)
+              row = 16 + 32 * (e >> 6) + ((e & 63) >> 2);
+              col = 32 * (e >> 6) + 4 * (e & 3);
+            } else {
+              row = 32 + ((e - 128) >> 3);
+              col = 4 * ((e - 128) & 7);
+            }
+            float4* pa = reinterpret_cast<float4*>(ws + row * WLD + col);
+            float4 v4 = *pa;
+            v4.x = tf32r(v4.x); v4.y = tf32r(v4.y); v4.z = tf32r(v4.z); v4.w = tf32r(v4.w);
+            *pa = v4;
+          }
+        }
+      }
+      named_sync(BAR_P, GROUP);
       if (lt == 0) mbar_arrive(&bar_ext);
       // ---------------- once S's last product of the previous block is complete: Khat^T of this
       // block (that product read the previous one) and the previous block's O
@@ -608,19 +648,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_st16(tl + T_ZB + 16 * hh, zb);
       }
       // ---------------- T = (I + A)^{-1} (unit lower triangular) and G = T Diag(beta) (bf16)
-      // The four 16 x 16 diagonal inverses T_RR by forward substitution in fp32; then, from the
-      // block-inverse identity [[P, 0], [C, Q]]^{-1} = [[P^{-1}, 0], [-Q^{-1} C P^{-1}, Q^{-1}]],
-      // the off-diagonal 16 x 16 block of each 32 x 32 half and then the off-diagonal 32 x 32
-      // block, as tf32 warp MMAs on fp32 blocks in WS (T overwrites A where A is no longer read).
+      // From the 16 x 16 diagonal inverses T_RR (group P, in trr) and the block-inverse identity
+      // [[P, 0], [C, Q]]^{-1} = [[P^{-1}, 0], [-Q^{-1} C P^{-1}, Q^{-1}]]: the off-diagonal
+      // 16 x 16 block of each 32 x 32 half and then the off-diagonal 32 x 32 block, as tf32 warp
+      // MMAs on fp32 blocks in WS (T overwrites A where A is no longer read).
       {
         float* ws = reinterpret_cast<float*>(sm + WS);
         // scratch: rows 0..31, columns 32..63 of WS, where A is zero and no block of T is kept
         float* qs = ws + 32;
         const int sw = warp - GROUP / 32;  // warp index inside the group
         const float* bt = beta_s[par];
-        // 16 x 8 tile: acc += A B over K = 8 nk, operands rounded to tf32 from fp32 shared memory
-        // Every value of the solve is rounded to tf32 where it is written, so operands load as
-        // they are: A as four 8 x 8 b16 matrices (8 rows x 4 fp32 each: rows 0-7 / 8-15 x columns
+        // 16 x 8 tile: acc += A B over K = 8 nk. Every value of the solve is rounded to tf32 where
+        // it is written, so operands load as they are: A as four 8 x 8 b16 matrices (8 rows x 4 fp32 each: rows 0-7 / 8-15 x columns
         // 0-3 / 4-7, which is the tf32 A fragment), B as two 32-bit loads. Ab: 16-byte aligned rows.
         auto tile_mma = [&](float (&acc)[4], const float* Ab, int lda, const float* Bb, int ldb,
                             int nk) {
@@ -641,42 +680,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           *reinterpret_cast<uint32_t*>(sm + GB + sw128_off((uint32_t)r, (uint32_t)j)) =
               pack_bf16(x0 * bt[j], x1 * bt[j + 1]);
         };
-        // (1) T_RR: thread (Rd, jj) of the last two warps solves (I + A_RR) x = e_jj by column
-        //     sweeps (x_i -= A_im x_m for i > m), one fma per step on the chain through x
-        if (lt >= GROUP - 64) {
-          const int q = lt - (GROUP - 64), Rd = q >> 4, jj = q & 15;
-          const float* ab = ws + 16 * Rd * (WLD + 1);
-          float x[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) x[i] = i == jj ? 1.f : 0.f;
-#pragma unroll
-          for (int m = 0; m < 15; ++m)
-#pragma unroll
-            for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-ab[i * WLD + m], x[m], x[i]);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) trr[Rd][i][jj] = tf32r(x[i]);
-        } else {
-          // meanwhile the blocks of A used below as MMA A operands (A_10, A_32 and rows 32..63 x
-          // columns 0..31) to tf32, in place: 384 float4, two per thread
-#pragma unroll
-          for (int e = lt; e < 384; e += GROUP - 64) {
-            // e < 64: A_10 (rows 16..31, 4 float4 of columns 0..15); e < 128: A_32 (rows 48..63,
-            // columns 32..47); else rows 32..63 x 8 float4 of columns 0..31
-            int row, col;
-            if (e < 128) {
-              row = 16 + 32 * (e >> 6) + ((e & 63) >> 2);
-              col = 32 * (e >> 6) + 4 * (e & 3);
-            } else {
-              row = 32 + ((e - 128) >> 3);
-              col = 4 * ((e - 128) & 7);
-            }
-            float4* pa = reinterpret_cast<float4*>(ws + row * WLD + col);
-            float4 v4 = *pa;
-            v4.x = tf32r(v4.x); v4.y = tf32r(v4.y); v4.z = tf32r(v4.z); v4.w = tf32r(v4.w);
-            *pa = v4;
-          }
-        }
-        named_sync(BAR_S, GROUP);
         // (2) warp h (0, 1), one per 32-row half: Y = A_10 T_00 (16 x 16, into qs), then
         //     T_10 = -T_11 Y into WS (h = 1: A_32, T_22, T_33, T_32); warps 2-7: the T_RR into the
         //     diagonal blocks of WS, whose A_RR is no longer read, and G of the diagonal blocks
