@@ -74,6 +74,7 @@ constexpr int D = 128;
 constexpr int THREADS = 512;  // two groups of 256
 constexpr int GROUP = 256;
 constexpr int BAR_P = 1, BAR_S = 2;  // hardware barrier ids of the groups
+constexpr int BAR_PAIR0 = 3;        // ids 3..6: pairs of warps of the state group in its solve
 constexpr float LOG2E = 1.4426950408889634f;
 
 // ---- shared memory map (bytes from a 1024-aligned base)
@@ -680,75 +681,63 @@ __global__ void __launch_bounds__(THREADS, 1)
           *reinterpret_cast<uint32_t*>(sm + GB + sw128_off((uint32_t)r, (uint32_t)j)) =
               pack_bf16(x0 * bt[j], x1 * bt[j + 1]);
         };
-        // (2) warp h (0, 1), one per 32-row half: Y = A_10 T_00 (16 x 16, into qs), then
-        //     T_10 = -T_11 Y into WS (h = 1: A_32, T_22, T_33, T_32); warps 2-7: the T_RR into the
-        //     diagonal blocks of WS, whose A_RR is no longer read, and G of the diagonal blocks
-        if (sw < 2) {
-          const int tile = sw;
-          float* y = qs + 16 * tile;
-#pragma unroll
-          for (int nh = 0; nh < 2; ++nh) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            tile_mma(acc, ws + (16 + 32 * tile) * WLD + 32 * tile, WLD, &trr[2 * tile][0][8 * nh], TLD, 2);
-            float* yo = y + 8 * nh + 2 * t;
-            yo[g * WLD] = tf32r(acc[0]);
-            yo[g * WLD + 1] = tf32r(acc[1]);
-            yo[(g + 8) * WLD] = tf32r(acc[2]);
-            yo[(g + 8) * WLD + 1] = tf32r(acc[3]);
-          }
+        // (2) warp (h, n) of warps 0-3, h = 32-row half, n = 8-column half: columns 8n .. 8n + 7
+        //     of Y = A_10 T_00 (into qs), then of T_10 = -T_11 Y (into WS), which need no other
+        //     columns of Y (h = 1: A_32, T_22, T_33, T_32); warps 4-7: the T_RR into the diagonal
+        //     blocks of WS, where A_RR is no longer read, and G of the diagonal blocks
+        if (sw < 4) {
+          const int tile = sw >> 1, nh = sw & 1;
+          float* y = qs + 16 * tile + 8 * nh;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma(acc, ws + (16 + 32 * tile) * WLD + 32 * tile, WLD, &trr[2 * tile][0][8 * nh], TLD, 2);
+          float* yo = y + 2 * t;
+          yo[g * WLD] = tf32r(acc[0]);
+          yo[g * WLD + 1] = tf32r(acc[1]);
+          yo[(g + 8) * WLD] = tf32r(acc[2]);
+          yo[(g + 8) * WLD + 1] = tf32r(acc[3]);
           __syncwarp();
-#pragma unroll
-          for (int nh = 0; nh < 2; ++nh) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            tile_mma(acc, &trr[2 * tile + 1][0][0], TLD, y + 8 * nh, WLD, 2);
-            float* o = ws + (16 + 32 * tile) * WLD + 32 * tile + 8 * nh + 2 * t;
-            o[g * WLD] = tf32r(-acc[0]);
-            o[g * WLD + 1] = tf32r(-acc[1]);
-            o[(g + 8) * WLD] = tf32r(-acc[2]);
-            o[(g + 8) * WLD + 1] = tf32r(-acc[3]);
-          }
+          float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma(acc2, &trr[2 * tile + 1][0][0], TLD, y, WLD, 2);
+          float* o = ws + (16 + 32 * tile) * WLD + 32 * tile + 8 * nh + 2 * t;
+          o[g * WLD] = tf32r(-acc2[0]);
+          o[g * WLD + 1] = tf32r(-acc2[1]);
+          o[(g + 8) * WLD] = tf32r(-acc2[2]);
+          o[(g + 8) * WLD + 1] = tf32r(-acc2[3]);
         } else {
-          for (int e = lt - 64; e < 1024; e += GROUP - 64) {
+          for (int e = lt - 128; e < 1024; e += 128) {
             const int R = e >> 8, i = (e >> 4) & 15, j = e & 15;
             ws[(16 * R + i) * WLD + 16 * R + j] = trr[R][i][j];
           }
-          for (int e = lt - 64; e < 512; e += GROUP - 64) {
+          for (int e = lt - 128; e < 512; e += 128) {
             const int R = e >> 7, i = (e >> 3) & 15, jp = 2 * (e & 7);
             g_store(16 * R + i, 16 * R + jp, trr[R][i][jp], trr[R][i][jp + 1]);
           }
         }
         named_sync(BAR_S, GROUP);
-        // (3) warp nt (0-3): columns 8 nt .. 8 nt + 7 of Q = A_(32)10 T_(32)00 (rows 32..63 x
-        //     columns 0..31, K 32; into qs), then of G rows 32..63: T_(32)10 = -T_(32)11 Q;
-        //     warps 4-7: G of T_10 and T_32
-        if (sw < 4) {
-          const int nt = sw;
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            tile_mma(acc, ws + (32 + 16 * mt) * WLD, WLD, ws + 8 * nt, WLD, 4);
-            float* o = qs + 16 * mt * WLD + 8 * nt + 2 * t;
-            o[g * WLD] = tf32r(acc[0]);
-            o[g * WLD + 1] = tf32r(acc[1]);
-            o[(g + 8) * WLD] = tf32r(acc[2]);
-            o[(g + 8) * WLD + 1] = tf32r(acc[3]);
-          }
-          __syncwarp();
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            tile_mma(acc, ws + (32 + 16 * mt) * WLD + 32, WLD, qs + 8 * nt, WLD, 4);
-            const int r = 32 + 16 * mt + g, j = 8 * nt + 2 * t;
-            g_store(r, j, -acc[0], -acc[1]);
-            g_store(r + 8, j, -acc[2], -acc[3]);
-          }
-        } else {
-#pragma unroll
-          for (int e = lt - 128; e < 256; e += 128) {
-            const int tile = e >> 7, i = (e >> 3) & 15, jp = 2 * (e & 7);
+        // (3) warp (n, m), n = sw & 3, m = sw >> 2: tile (m, n) of Q = A_(32)10 T_(32)00 (rows
+        //     32 + 16 m .., columns 8 n .., K 32; into qs); the two warps of column block n meet
+        //     at their own barrier; then tile (m, n) of G rows 32..63: T_(32)10 = -T_(32)11 Q.
+        //     Every thread also writes one pair of G of T_10 and T_32.
+        {
+          const int nt = sw & 3, mt = sw >> 2;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma(acc, ws + (32 + 16 * mt) * WLD, WLD, ws + 8 * nt, WLD, 4);
+          float* o = qs + 16 * mt * WLD + 8 * nt + 2 * t;
+          o[g * WLD] = tf32r(acc[0]);
+          o[g * WLD + 1] = tf32r(acc[1]);
+          o[(g + 8) * WLD] = tf32r(acc[2]);
+          o[(g + 8) * WLD + 1] = tf32r(acc[3]);
+          {
+            const int tile = lt >> 7, i = (lt >> 3) & 15, jp = 2 * (lt & 7);
             const int r = 16 + 32 * tile + i, j = 32 * tile + jp;
             g_store(r, j, ws[r * WLD + j], ws[r * WLD + j + 1]);
           }
+          named_sync(BAR_PAIR0 + nt, 64);
+          float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma(acc2, ws + (32 + 16 * mt) * WLD + 32, WLD, qs + 8 * nt, WLD, 4);
+          const int r = 32 + 16 * mt + g, j = 8 * nt + 2 * t;
+          g_store(r, j, -acc2[0], -acc2[1]);
+          g_store(r + 8, j, -acc2[2], -acc2[3]);
         }
       }
       fence_proxy_async_smem();  // G is a tensor-core operand
