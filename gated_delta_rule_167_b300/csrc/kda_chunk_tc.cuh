@@ -8,10 +8,11 @@
 //   P_rj = sum_c q_rc k_jc e^{Gamma_rc - Gamma_jc} (j <= r),  O = (Q e^Gamma) S + P U
 //   S' = Diag(e^{Gamma_L}) S + Khat^T U,  Khat_j = k_j e^{Gamma_L - Gamma_j}
 // U equals U~ - W S with U~ = T Diag(beta) V, W = T Diag(beta) K e^Gamma and T = (I + A)^{-1};
-// forming the residual V - (K e^Gamma) S first needs no W. U is found by forward substitution
-// over the four 16-row sub-blocks R of the block:
-//   U_R = G_R (V_R - Z_R) + sum_{m<R} M_{R,m} U_m,  G_R = T_RR Diag(beta_R),  M_{R,m} = -T_RR A_{R,m}
-// with Z = (K e^Gamma) S and T_RR = (I + A_RR)^{-1} the 16 x 16 diagonal inverses.
+// forming the residual V - (K e^Gamma) S first needs no W. T is formed explicitly: the four
+// 16 x 16 diagonal inverses by forward substitution, then the block-inverse identity
+//   [[P, 0], [C, Q]]^{-1} = [[P^{-1}, 0], [-Q^{-1} C P^{-1}, Q^{-1}]]
+// inside each 32-token half and for the two halves, and U = T Diag(beta) (V - Z) is one
+// tensor-core product with Z = (K e^Gamma) S.
 //
 // Bounded decay. Over a block of 64 tokens Gamma can fall to -320, so e^{-Gamma} overflows any
 // floating type and A, P cannot be one product (K e^Gamma)(K e^{-Gamma})^T. With
@@ -20,15 +21,10 @@
 // boundary between its two 16-token sub-blocks (rho_A = Gamma_15, rho_B = Gamma_47):
 //   X[r]   = [k_r ; q_r] e^{Gamma_r - rho(r)}     for every row r        (factor in [e^-80, e^75])
 //   Y_A[j] = k_j e^{rho_A - Gamma_j}              for j < 32             (in [e^-75, e^80])
-//   Y_B[j] = k_j e^{rho_B - Gamma_j}              for j < 64             (<= e^80; for j < 32 it
-//                                                                         may underflow, only where
-//                                                                         every product it enters
-//                                                                         is below e^-12)
+//   Y_B[j] = k_j e^{rho_B - Gamma_j}              for j < 64             (<= e^80)
 // so that one tensor-core product X [Y_B ; Y_A]^T (N = 96) holds every A_rj and P_rj with
 // j <= r: rows of the first half read the Y_A columns, rows of the second half the Y_B columns.
 // Entries above the diagonal may overflow in that product; they are discarded by selection.
-// Every factor is one exponential of its own exponent, so nothing overflows and anything that
-// underflows is below that bound.
 //
 // Layout. One CTA (512 threads) owns one (sequence, head) problem and walks its blocks in
 // order. The state is kept transposed in TMEM: S^T in fp32 (lane = value channel v, column =
@@ -37,24 +33,25 @@
 // TMEM -> registers -> TMEM, so only operands built from the inputs pass through shared memory.
 //
 // Two warp groups work on consecutive blocks at the same time:
-//   group P (warps 0-7), block n + 1: Gamma; X, Y, (K e^Gamma)^T, (Q e^Gamma)^T, Khat^T
-//     ([channel][token] rows, 16-byte stores); the A/P product D = X [Y_B | Y_A]^T; A (fp32)
-//     and P (bf16) out of TMEM; and, once S has finished block n, block n's O out of TMEM.
+//   group P (warps 0-7), block n + 1: X, Y, (K e^Gamma)^T, (Q e^Gamma)^T, Khat^T from transposed
+//     8 x 8 matrix loads of the inputs (running sums of g by warp MMAs), written back by matrix
+//     stores as [channel][token] rows; the A/P product D = X [Y_B | Y_A]^T; A (fp32) and P (bf16)
+//     out of TMEM; the diagonal inverses T_RR; then, once S has finished block n, Khat^T of
+//     block n + 1 and block n's O out of TMEM.
 //   group S (warps 8-15), block n:
-//     tcgen05: [Z^T | O^T] = S^T [(K e^Gamma)^T | (Q e^Gamma)^T]; meanwhile S^T <- S^T e^{Gamma_L}
-//     SIMT: Z^T -> bf16; T_RR by forward substitution (fp32); M_{R,m} (tf32 warp MMAs) and G_R
-//           as bf16 16 x 16 operand tiles
-//     tcgen05, four steps R: U_R^T = V_R^T G_R^T - Z_R^T G_R^T + sum_{m<R} U_m^T M_{R,m}^T (N 16),
-//           each followed by U_R^T -> bf16 in TMEM
+//     tcgen05: Z^T = S^T (K e^Gamma)^T, O^T = S^T (Q e^Gamma)^T; meanwhile S^T <- S^T e^{Gamma_L}
+//     SIMT: Z^T -> bf16; the off-diagonal blocks of T (tf32 warp MMAs); G = T Diag(beta) (bf16)
+//     tcgen05: U^T = V^T G^T - Z^T G^T, U^T -> bf16
 //     tcgen05: O^T += U^T P^T;  S^T += U^T Khat;  SIMT: bf16 copy of S^T
 // Shared buffers pass between the groups through mbarriers: P may rewrite X and Y once its
 // A/P product of the previous block has completed, (K/Q e^Gamma)^T once S's first product has,
-// and Khat^T (held in registers until then), A and P once S's last product has; S starts a
-// block once P has written that block's operands and the previous block's O. Transposed forms
-// keep every product at M = 128 (TMEM lane = row). Only the bf16 copy of the state feeds the
-// tensor cores; the fp32 state accumulates in TMEM, so rounding does not accumulate in S
-// itself. Every wait is bounded; a timeout latches KDA_ERR_TIMEOUT, lets issued copies and
-// products land, frees TMEM and returns.
+// A (WS) once S has finished its solve, and Khat^T (held in registers until then) once S's last
+// product has; S starts a block once P has written that block's operands and the O of two
+// blocks ago (O^T and P are double-buffered by block parity). Transposed products keep every
+// tcgen05 product at M = 128 (TMEM lane = row). Only the bf16 copy of the state feeds the tensor
+// cores; the fp32 state accumulates in TMEM, so rounding does not accumulate in S itself. Every
+// wait is bounded; a timeout latches KDA_ERR_TIMEOUT, lets issued copies and products land,
+// frees TMEM and returns.
 #pragma once
 
 #include <cuda.h>
