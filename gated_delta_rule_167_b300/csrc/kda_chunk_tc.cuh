@@ -82,9 +82,11 @@ constexpr uint32_t IN_V = 49152;       // v tile (MN-major A of V^T (T Diag beta
 constexpr uint32_t XK = 65536;         // X rows 0..63 (k side), MN-major A panel 0
 constexpr uint32_t XQ = XK + 16384;    // X rows 64..127 (q side), MN-major A panel 1
 constexpr uint32_t YP = XQ + 16384;    // [Y_B | Y_A], N = 96 columns in 2 MN-major B panels
-constexpr uint32_t KG = YP + 32768;    // (K e^Gamma)^T [c][r]: MN-major B panel 0 of [Z^T | O^T]
-constexpr uint32_t QG = KG + 16384;    // (Q e^Gamma)^T [c][r]: MN-major B panel 1 of [Z^T | O^T]
-constexpr uint32_t KH = QG + 16384;    // Khat^T [c][r]: K-major B of S^T += U^T Khat
+// (K e^Gamma)^T and (Q e^Gamma)^T [c][r]: the two MN-major B panels of the product with S, in
+// the order of its TMEM output: even blocks [(Q e^Gamma)^T | (K e^Gamma)^T] -> [O^T | Z^T],
+// odd blocks [(K e^Gamma)^T | (Q e^Gamma)^T] -> [Z^T | O^T]
+constexpr uint32_t KQ = YP + 32768;    // 2 x 16 KB
+constexpr uint32_t KH = KQ + 32768;    // Khat^T [c][r]: K-major B of S^T += U^T Khat
 constexpr uint32_t WS = KH + 16384;    // fp32 A, then T ([64][WLD], 18 KB)
 constexpr uint32_t PT = WS + 18432;    // P [r][j], K-major B of O^T += U^T P^T, 2 x 8 KB by parity
 constexpr uint32_t GB = PT + 16384;    // G = T Diag(beta) [r][j] bf16, K-major B of U^T (8 KB)
@@ -96,9 +98,11 @@ constexpr uint32_t BOX_BYTES = 8192;                // one 64-channel x 64-token
 constexpr uint32_t T_ST = 0;    // S^T fp32 [v][c], 128
 constexpr uint32_t T_SB = 128;  // S^T bf16 (A operand), 64
 constexpr uint32_t T_D = 192;   // X [Y_B | Y_A]^T, 96
-constexpr uint32_t T_ZT = 288;  // Z^T fp32, 64; after its bf16 copy: U^T fp32
-constexpr uint32_t T_OT = 352;  // O^T fp32, 2 x 64 by block parity (P writes one out while S
-                                // accumulates the other)
+// O^T fp32 by block parity at 288 (even) and 416 (odd), Z^T fp32 between them at 352, so that
+// [O^T | Z^T] (even) and [Z^T | O^T] (odd) are one 128-column product; group P writes one O^T
+// out while group S accumulates the other
+constexpr uint32_t T_ZT = 352;  // Z^T fp32, 64; after its bf16 copy: U^T fp32
+__host__ __device__ constexpr uint32_t t_ot_of(int b) { return (b & 1) ? 416u : 288u; }
 constexpr uint32_t T_ZB = 480;  // Z^T bf16 (A operand), 32
 constexpr uint32_t T_UT = T_ZT;  // U^T fp32 once Z^T has its bf16 copy
 constexpr uint32_t T_UB = T_ZB;  // U^T bf16 (A operand), over Z^T bf16 once the U product read it
@@ -239,7 +243,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         uint32_t v[16];
-        tmem_ld16(tl + T_OT + 64u * (uint32_t)(b & 1) + 32 * hh + 16 * part, v);
+        tmem_ld16(tl + t_ot_of(b) + 32 * hh + 16 * part, v);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j)
@@ -331,7 +335,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
 #pragma unroll
         for (int cg = 0; cg < 2; ++cg) {
-          const float s0 = sg[cg][0], s1 = sg[cg][1], s2 = sg[cg][2], s3 = sg[cg][3];
+          // e^{s_R} (<= 1) per sub-block, and e^{-s_R} where a sub-block ends at its reference;
+          // every anchor is a product of these
+          const float e0 = ex2(sg[cg][0]), e1 = ex2(sg[cg][1]), e2 = ex2(sg[cg][2]), e3 = ex2(sg[cg][3]);
+          const float f0 = ex2(-sg[cg][0]), f2 = ex2(-sg[cg][2]);
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {  // tokens 32 hf .. 32 hf + 31: sub-blocks 2 hf, 2 hf + 1
             uint32_t kw[4], qw[4];
@@ -348,12 +355,10 @@ __global__ void __launch_bounds__(THREADS, 1)
               qw[i] &= lv;
               // anchors e^{Gamma_{16R-1}}, e^{Gamma_L - Gamma_{16R+15}}, e^{rho_B - Gamma_{16R+15}},
               // e^{+-(Gamma_{16R+15} - Gamma_{16R-1})}
-              const float before = R == 0 ? 0.f : (R == 1 ? s0 : (R == 2 ? s0 + s1 : s0 + s1 + s2));
-              const float after = R == 0 ? s1 + s2 + s3 : (R == 1 ? s2 + s3 : (R == 2 ? s3 : 0.f));
-              const float tob = R == 0 ? s1 + s2 : s2;
-              const float sR = R == 0 ? s0 : (R == 1 ? s1 : (R == 2 ? s2 : s3));
-              const float eb = R == 0 ? 1.f : ex2(before), ea = R == 3 ? 1.f : ex2(after);
-              const float es = ex2(sR), ef = odd ? 1.f : ex2(-sR);
+              const float eb = R == 0 ? 1.f : (R == 1 ? e0 : (R == 2 ? e0 * e1 : e0 * e1 * e2));
+              const float ea = R == 0 ? e1 * e2 * e3 : (R == 1 ? e2 * e3 : (R == 2 ? e3 : 1.f));
+              const float es = R == 0 ? e0 : (R == 1 ? e1 : (R == 2 ? e2 : e3));
+              const float ef = R == 0 ? f0 : (R == 2 ? f2 : 1.f);
               const float L0 = Lr[R][e][2 * cg] * LOG2E, L1 = Lr[R][e][2 * cg + 1] * LOG2E;
               const float2 u = make_float2(ex2(L0), ex2(L1));
               const float2 wv = make_float2(ex2(-L0), ex2(-L1));
@@ -373,7 +378,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               oqg[i] = pack_bf16(qg2.x, qg2.y);
               kh[cg][m] = pack_bf16(kh2.x, kh2.y);
               if (hf == 0) {
-                const float et = ex2(tob);
+                const float et = R == 0 ? e1 * e2 : e2;
                 const float2 yb2 = mul2(k2, mul2(make_float2(et, et), sfx));  // k e^{rho_B - Gamma}
                 oyb[i] = pack_bf16(yb2.x, yb2.y);
               }
@@ -382,8 +387,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t so = sw128_off((uint32_t)(cw + 8 * cg + lr), (uint32_t)(8 * (4 * hf + li)));
             stsm_x4(sb + XK + so, oxk[0], oxk[1], oxk[2], oxk[3]);
             stsm_x4(sb + XQ + so, oxq[0], oxq[1], oxq[2], oxq[3]);
-            stsm_x4(sb + KG + so, okg[0], okg[1], okg[2], okg[3]);
-            stsm_x4(sb + QG + so, oqg[0], oqg[1], oqg[2], oqg[3]);
+            stsm_x4(sb + KQ + (par ? 0u : 16384u) + so, okg[0], okg[1], okg[2], okg[3]);
+            stsm_x4(sb + KQ + (par ? 16384u : 0u) + so, oqg[0], oqg[1], oqg[2], oqg[3]);
             if (hf == 0) {
               stsm_x4(sb + YP + 16384u + so, oy[0], oy[1], oy[2], oy[3]);  // Y_A (panel 1)
               stsm_x4(sb + YP + so, oyb[0], oyb[1], oyb[2], oyb[3]);       // Y_B (panel 0)
@@ -590,18 +595,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t t_ot = T_OT + 64u * (uint32_t)par;  // this block's O^T columns
-      // ---------------- tcgen05: Z^T = S^T (K e^Gamma)^T, O^T = S^T (Q e^Gamma)^T (N 64, K 128)
+      const uint32_t t_ot = t_ot_of(blk);  // this block's O^T columns
+      // ---------------- tcgen05: [O^T | Z^T] (even) or [Z^T | O^T] (odd) =
+      // S^T [(Q e^Gamma)^T | (K e^Gamma)^T] (or the other order) (N 128, K 128)
       if (leader) {
         tc_fence_after();
-        const uint32_t id_z = idesc_bf16(128, 64, 0, 1, 0);
+        const uint32_t id_zo = idesc_bf16(128, 128, 0, 1, 0);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          umma_bf16_tmem_a(tmem + T_ZT, tmem + T_SB + 8u * kk,
-                           desc_sw128(sb + KG + 2048u * kk, 16384, 1024), id_z, kk > 0);
-          umma_bf16_tmem_a(tmem + t_ot, tmem + T_SB + 8u * kk,
-                           desc_sw128(sb + QG + 2048u * kk, 16384, 1024), id_z, kk > 0);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_tmem_a(tmem + (par ? T_ZT : t_ot), tmem + T_SB + 8u * kk,
+                           desc_sw128(sb + KQ + 2048u * kk, 16384, 1024), id_zo, kk > 0);
         umma_commit(&bar_ZO);
       }
       pend_mma = true; last_mma = &bar_ZO; last_par = ph;
