@@ -220,6 +220,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       load2(IN_K, &maps.k, row, &bar_in);
       load2(IN_Q, &maps.q, row, &bar_in);
       load2(IN_G, &maps.g, row, &bar_in);
+      if (b + 1 < nblocks) {  // the block after it into L2, so that its load finds it there
+        const CUtensorMap* mp[3] = {&maps.k, &maps.q, &maps.g};
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+          tma_prefetch_3d(mp[i], 0, h, row + C);
+          tma_prefetch_3d(mp[i], 64, h, row + C);
+        }
+      }
     };
     bool pend_in = false;
     int in_blk = 0, d_blk = -1;  // block of the last input load / A/P product issued
@@ -552,6 +560,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto issue_v = [&](int b) {
       mbar_arrive_expect_tx(&bar_v, 2 * BOX_BYTES);
       load2(IN_V, &maps.v, (int)(row0 + (size_t)b * C), &bar_v);
+      if (b + 1 < nblocks) {  // the next v tile into L2
+        tma_prefetch_3d(&maps.v, 0, h, (int)(row0 + (size_t)(b + 1) * C));
+        tma_prefetch_3d(&maps.v, 64, h, (int)(row0 + (size_t)(b + 1) * C));
+      }
     };
     // ---- initial state S^T: lane v = c, key channels 64 hh .. 64 hh + 63 (coalesced over v)
     {
@@ -635,9 +647,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_st16(tl + T_ST + c0, v);
         }
       }
-      // ---------------- Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand; group P has written
-      // A and P of this block by bar_ext
-      if (!group_wait2(&bar_ZO, ph, &bar_ext, ph, BAR_S)) { aborted = true; break; }
+      // ---------------- Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand; then wait for group P
+      // to have written A, P and the diagonal inverses of this block (bar_ext)
+      if (!group_wait2(&bar_ZO, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       pend_mma = false;
       tc_fence_after();
       {
@@ -648,6 +660,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int j = 0; j < 16; ++j) zb[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
         tmem_st16(tl + T_ZB + 16 * hh, zb);
       }
+      if (!group_wait2(&bar_ext, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       // ---------------- T = (I + A)^{-1} (unit lower triangular) and G = T Diag(beta) (bf16)
       // From the 16 x 16 diagonal inverses T_RR (group P, in trr) and the block-inverse identity
       // [[P, 0], [C, Q]]^{-1} = [[P^{-1}, 0], [-Q^{-1} C P^{-1}, Q^{-1}]]: the off-diagonal
