@@ -242,12 +242,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(P.out);
     // O of block b: TMEM (lane v = c, tokens 32 hh .. 32 hh + 31) -> bf16 rows [token][128]
     // staged in XK (free: this group's A/P product of the block after b has completed, and the
-    // next operands are written after the group's closing barrier) -> 16-byte global stores,
-    // each warp writing two whole 256-byte rows
-    auto emit_o = [&](int b) {
-      const int tb = b * C;
-      const int nb = min(C, len - tb);
-      uint8_t* stg = sm + XK;
+    // next operands are written after the group's next barrier), then, after a group barrier,
+    // 16-byte global stores, each warp writing two whole 256-byte rows
+    uint8_t* stg = sm + XK;
+    auto stage_o = [&](int b) {
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         uint32_t v[16];
@@ -259,7 +257,11 @@ __global__ void __launch_bounds__(THREADS, 1)
               __float2bfloat16_rn(__uint_as_float(v[j]));
       }
       tc_fence_before();
-      named_sync(BAR_P, GROUP);
+    };
+    // after a group barrier that follows stage_o(b)
+    auto store_o = [&](int b) {
+      const int tb = b * C;
+      const int nb = min(C, len - tb);
       const int q = lt & 15;  // 16-byte chunk of a row; rows lt / 16 + 16 i
       __nv_bfloat16* ob = out + ((row0 + tb + (lt >> 4)) * H + h) * D + 8 * q;
       const uint8_t* sp = stg + (lt >> 4) * 256 + 16 * q;
@@ -410,10 +412,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       fence_proxy_async_smem();
       named_sync(BAR_P, GROUP);
       if (lt == 0) {
-        if (blk + 1 < nblocks) issue_in(blk + 1);  // the k, q and g tiles are dead
-        mbar_arrive(&bar_prep);
         // ---------------- tcgen05: D = X [Y_B | Y_A]^T (M 128, N 96, K 128); this group read the
-        // previous block's D out already
+        // previous block's D out already. Issued before the operands are released, so that it
+        // enters the tensor pipe ahead of the state group's first product.
         tc_fence_after();
         const uint32_t id_d = idesc_bf16(128, 96, 1, 1, 0);
 #pragma unroll
@@ -421,6 +422,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           umma_bf16(tmem + T_D, desc_sw128(sb + XK + 2048u * kk, 16384, 1024),
                     desc_sw128(sb + YP + 2048u * kk, 16384, 1024), id_d, kk > 0);
         umma_commit(&bar_D);
+        mbar_arrive(&bar_prep);
+        if (blk + 1 < nblocks) issue_in(blk + 1);  // the k, q and g tiles are dead
       }
       if (blk + 1 < nblocks) {
         pend_in = true;
@@ -537,14 +540,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           stsm_x4(sb + KH + sw128_off((uint32_t)(16 * warp + 8 * cg + (lane & 7)), (uint32_t)(8 * (4 * hf + (lane >> 3)))),
                   kh[cg][4 * hf], kh[cg][4 * hf + 1], kh[cg][4 * hf + 2], kh[cg][4 * hf + 3]);
       fence_proxy_async_smem();
-      if (blk > 0) emit_o(blk - 1);
+      if (blk > 0) stage_o(blk - 1);
       named_sync(BAR_P, GROUP);
+      // Khat^T is stored and the previous block's O is out of TMEM; its global stores follow (the
+      // release of this arrive does not wait for them)
       if (lt == 0) mbar_arrive(&bar_khr);
+      if (blk > 0) store_o(blk - 1);
     }
     if (!aborted && nblocks > 0) {  // the last block's O
       if (group_wait2(&bar_G3, (nblocks - 1) & 1, nullptr, 0, BAR_P)) {
         tc_fence_after();
-        emit_o(nblocks - 1);
+        stage_o(nblocks - 1);
+        named_sync(BAR_P, GROUP);
+        store_o(nblocks - 1);
       } else {
         aborted = true;
       }
