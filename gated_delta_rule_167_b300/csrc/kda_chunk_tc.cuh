@@ -240,21 +240,36 @@ __global__ void __launch_bounds__(THREADS, 1)
     unsigned short beta_next = 0;
     if (lt < C && lt < len) beta_next = beta_u[(row0 + lt) * H + h];
     __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(P.out);
-    // O of block b: TMEM (lane v = c, tokens 32 hh .. 32 hh + 31) -> bf16 rows [token][128]
-    // staged in XK (free: this group's A/P product of the block after b has completed, and the
-    // next operands are written after the group's next barrier), then, after a group barrier,
-    // 16-byte global stores, each warp writing two whole 256-byte rows
+    // O of block b: TMEM -> bf16 rows [token][128] staged in XK (free: this group's A/P product
+    // of the block after b has completed, and the next operands are written after the group's
+    // next barrier), then, after a group barrier, 16-byte global stores, each warp writing two
+    // whole 256-byte rows. The 16-byte chunks of a staged row are permuted by chunk ^ (token % 8)
+    // so that the eight rows of a matrix store fall in distinct banks.
+    // Warp w reads lanes (value channels) 32 (w % 4) .. + 31, columns (tokens) 32 hh .. + 31 in the
+    // 16 x 256 b shape, whose registers are the m16n8 fragment that a transposed matrix store
+    // writes as [token][channel] rows.
     uint8_t* stg = sm + XK;
+    const uint32_t stg_s = sb + XK;
     auto stage_o = [&](int b) {
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
+      for (int sl = 0; sl < 2; ++sl) {  // lanes 32 q + 16 sl .. + 15
         uint32_t v[16];
-        tmem_ld16(tl + t_ot_of(b) + 32 * hh + 16 * part, v);
+        const int cb = 32 * quarter + 16 * sl;  // first channel of the slab
+        tmem_ld_16x256b_x4(tmem + ((uint32_t)cb << 16) + t_ot_of(b) + 32 * hh, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          *reinterpret_cast<__nv_bfloat16*>(stg + (32 * hh + 16 * part + j) * 256 + 2 * c) =
-              __float2bfloat16_rn(__uint_as_float(v[j]));
+        for (int u = 0; u < 2; ++u) {
+          // matrix i: channels cb + 8 (i & 1) .., tokens 32 hh + 8 (2u + (i >> 1)) ..
+          const int li = lane >> 3, lj = lane & 7;
+          const int tok = 32 * hh + 8 * (2 * u + (li >> 1)) + lj;
+          const int chunk = ((cb + 8 * (li & 1)) >> 3) ^ (tok & 7);
+          const int k0 = 2 * u, k1 = 2 * u + 1;
+          stsm_x4_trans(stg_s + (uint32_t)(tok * 256 + 16 * chunk),
+                        pack_bf16(__uint_as_float(v[4 * k0]), __uint_as_float(v[4 * k0 + 1])),
+                        pack_bf16(__uint_as_float(v[4 * k0 + 2]), __uint_as_float(v[4 * k0 + 3])),
+                        pack_bf16(__uint_as_float(v[4 * k1]), __uint_as_float(v[4 * k1 + 1])),
+                        pack_bf16(__uint_as_float(v[4 * k1 + 2]), __uint_as_float(v[4 * k1 + 3])));
+        }
       }
       tc_fence_before();
     };
@@ -264,12 +279,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int nb = min(C, len - tb);
       const int q = lt & 15;  // 16-byte chunk of a row; rows lt / 16 + 16 i
       __nv_bfloat16* ob = out + ((row0 + tb + (lt >> 4)) * H + h) * D + 8 * q;
-      const uint8_t* sp = stg + (lt >> 4) * 256 + 16 * q;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if ((lt >> 4) + 16 * i < nb)
+      for (int i = 0; i < 4; ++i) {
+        const int r = (lt >> 4) + 16 * i;
+        if (r < nb)
           *reinterpret_cast<uint4*>(ob + (size_t)(16 * i) * H * D) =
-              *reinterpret_cast<const uint4*>(sp + 4096 * i);
+              *reinterpret_cast<const uint4*>(stg + r * 256 + 16 * (q ^ (r & 7)));
+      }
     };
 
     for (int blk = 0; blk < nblocks; ++blk) {

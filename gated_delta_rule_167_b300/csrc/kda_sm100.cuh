@@ -168,6 +168,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+// 16 lanes x 256 bit, repeated over 4 groups of 8 columns: the lane base in `taddr` is the first
+// of 16 lanes of this warp's quarter. Lane (g, t) of the warp receives, for k = 0..3,
+// r[4k], r[4k+1] = lane g, columns 8k + 2t, 8k + 2t + 1 and r[4k+2], r[4k+3] = lane g + 8, the
+// same columns (the m16n8 accumulator fragment layout).
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
 // Stores 32 consecutive columns of this thread's lane (same lane rule as tmem_ld32).
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
@@ -351,6 +365,16 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t saddr, uint32_t (&r)[4]) 
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(saddr)
+               : "memory");
+}
+
+// Four 8 x 8 b16 matrices to shared memory, transposed: register i of lane (g, t) holds row g,
+// columns 2t and 2t + 1 of the transpose of matrix i, i.e. column g, rows 2t and 2t + 1 of the
+// stored matrix; lanes 8i .. 8i + 7 give the addresses of the 8 stored rows of matrix i.
+__device__ __forceinline__ void stsm_x4_trans(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                              uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
                : "memory");
 }
 
