@@ -78,7 +78,7 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint32_t IN_K = 0;           // k tile (two 64-channel boxes of [64 tokens][64])
 constexpr uint32_t IN_Q = 16384;       // q tile
 constexpr uint32_t IN_G = 32768;       // g tile
-constexpr uint32_t IN_V = 49152;       // v tile (MN-major A of V^T (T Diag beta)^T as loaded)
+constexpr uint32_t IN_V = 49152;       // v tile: MN-major A operand V^T of U^T = V^T G^T - Z^T G^T
 constexpr uint32_t XK = 65536;         // X rows 0..63 (k side), MN-major A panel 0
 constexpr uint32_t XQ = XK + 16384;    // X rows 64..127 (q side), MN-major A panel 1
 constexpr uint32_t YP = XQ + 16384;    // [Y_B | Y_A], N = 96 columns in 2 MN-major B panels
@@ -120,17 +120,9 @@ struct TmaMaps {
 
 using namespace sm100;
 
-__device__ __forceinline__ float ld_bf16(const uint8_t* base, uint32_t off) {
-  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + off));
-}
-
 __device__ __forceinline__ void st_pack8(uint32_t saddr, const float (&x)[8]) {
   st_shared_v4(saddr, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
                pack_bf16(x[6], x[7]));
-}
-
-__device__ __forceinline__ void st_words4(uint32_t saddr, const uint32_t (&w)[4]) {
-  st_shared_v4(saddr, w[0], w[1], w[2], w[3]);
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -141,17 +133,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t sb = smem_u32(sm);
   // bar_in: k, q, g tiles landed          bar_v: v tile landed
   // bar_prep: P finished a block's operands (release / acquire for its generic stores)
-  // bar_ext: P has taken A (into WS) and P (into PT) out of the A/P product
+  // bar_ext: P has taken A (into WS) and P (into PT) out of the A/P product, made the diagonal
+  //          inverses T_RR (trr) and rounded the A blocks that S multiplies to tf32
   // bar_wsfree: S has read a block's A out of WS (P may put the next one there)
-  // bar_khr: P has stored a block's Khat^T and written the previous block's O out of TMEM
+  // bar_khr: P has stored a block's Khat^T and read the previous block's O out of TMEM
   // bar_D, bar_ZO, bar_G2, bar_G3: tcgen05 products complete
   __shared__ uint64_t bar_in, bar_v, bar_prep, bar_ext, bar_wsfree, bar_khr, bar_D, bar_ZO, bar_G2,
       bar_G3;
   __shared__ uint32_t tmem_base_s;
   __shared__ __align__(16) float beta_s[2][C];  // by block parity
   __shared__ __align__(16) float gl_s[2][D];    // e^{Gamma_L} per key channel, by block parity
-  // diagonal blocks T_RR of the solve (group S); rows of 20 floats: 16-byte aligned, and the
-  // eight row addresses of a matrix load fall in distinct banks
+  // diagonal blocks T_RR of the solve (written by group P, read by group S); rows of 20 floats:
+  // 16-byte aligned, and the eight row addresses of a matrix load fall in distinct banks
   __shared__ __align__(16) float trr[4][16][TLD];
 
   const int tid = threadIdx.x;
