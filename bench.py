@@ -55,13 +55,17 @@ def _peaks():
         return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
 
 
+# The sources the tensor-core prefill kernel is compiled from (its DRAM counters stay valid while
+# these are unchanged).
+PREFILL_SOURCES = ("kda_chunk_tc.cuh", "kda_chunk_simt.cuh", "kda_sm100.cuh", "kda_common.cuh")
+
+
 def _kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_167_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in PREFILL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 

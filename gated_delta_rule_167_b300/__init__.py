@@ -31,7 +31,7 @@ _DTYPES = {torch.float32: KDA_DTYPE_F32, torch.bfloat16: KDA_DTYPE_BF16}
 
 EXPORTED_SYMBOLS = (
     "kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_recurrent_step", "kda_sync_status",
-    "kda_status_string", "kda_last_error", "kda_version",
+    "kda_wait_selftest", "kda_status_string", "kda_last_error", "kda_version",
 )
 
 
@@ -71,6 +71,8 @@ def load_library(path: str | None = None):
     lib.kda_recurrent_step.argtypes = [V] * 7 + [I] * 4 + [I, V]
     lib.kda_recurrent_step.restype = S
     lib.kda_sync_status.argtypes = [V]
+    lib.kda_wait_selftest.argtypes = [ctypes.c_ulonglong, V]
+    lib.kda_wait_selftest.restype = S
     lib.kda_sync_status.restype = S
     lib.kda_status_string.argtypes = [S]
     lib.kda_status_string.restype = ctypes.c_char_p
@@ -181,6 +183,11 @@ def kda_recurrent_step(q, k, v, g, beta, S, out, stream=None):
 def kda_sync_status(stream=None):
     """Synchronises the stream and raises if a kernel latched a device-side error."""
     _check(load_library().kda_sync_status(_stream_handle(stream)), "kda_sync_status")
+
+
+def kda_wait_selftest(limit_ns: int, stream=None) -> int:
+    """Launches the bounded-wait self-test (see include/kda.h); returns the launch status."""
+    return load_library().kda_wait_selftest(int(limit_ns), _stream_handle(stream))
 
 
 def kda_status_string(status: int) -> str:

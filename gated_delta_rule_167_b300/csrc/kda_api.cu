@@ -11,6 +11,7 @@
 #include "kda_chunk_tc.cuh"
 #include "kda_common.cuh"
 #include "kda_decode.cuh"
+#include "kda_selftest.cuh"
 
 namespace {
 
@@ -184,6 +185,15 @@ kda_status_t kda_recurrent_step(const void* q, const void* k, const void* v, con
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "decode_step launch");
+  return KDA_OK;
+}
+
+kda_status_t kda_wait_selftest(unsigned long long limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull)
+    return fail(KDA_ERR_INVALID_ARG, "limit_ns must be in (0, 1e10] (got %llu)", limit_ns);
+  kda::selftest::unanswered_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "selftest launch: %s", cudaGetErrorString(e));
   return KDA_OK;
 }
 

@@ -97,6 +97,16 @@ kda_status_t kda_recurrent_step(const void* q, const void* k, const void* v, con
  * device (KDA_OK if nothing was latched), or KDA_ERR_CUDA if the synchronisation failed. */
 kda_status_t kda_sync_status(void* stream);
 
+/*
+ * Self-test of the device-side failure report. Launches one thread that waits, for at most
+ * limit_ns nanoseconds of the GPU global timer, on an mbarrier that nothing completes, then
+ * latches KDA_ERR_TIMEOUT in the status word the way a kernel does when one of its bounded
+ * waits gives up, and returns. The next kda_sync_status(stream) reports KDA_ERR_TIMEOUT and
+ * clears it; the context stays usable. Asynchronous on `stream`; returns KDA_ERR_INVALID_ARG
+ * unless 0 < limit_ns <= 1e10, KDA_ERR_CUDA if the launch fails.
+ */
+kda_status_t kda_wait_selftest(unsigned long long limit_ns, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* kda_status_string(kda_status_t status);
 
