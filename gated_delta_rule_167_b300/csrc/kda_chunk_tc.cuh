@@ -617,9 +617,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int n = min(C, len - t0);
       const int par = blk & 1;
       const uint32_t ph = (uint32_t)par;
-      // P's operands of this block are in place, and P has written out the O of two blocks ago,
-      // whose TMEM columns this block's O takes
-      if (!group_wait2(&bar_prep, ph, blk > 0 ? &bar_khr : nullptr, (blk - 1) & 1, BAR_S)) {
+      // P's operands of this block are in place. (P has read the O of two blocks ago out of
+      // TMEM, whose columns this block's O takes: bar_khr of the previous block, waited for
+      // before the previous block's last product. Waiting for it again here could alias: P may
+      // already have completed the next phase of bar_khr, and a parity wait would then look
+      // for the phase after it.)
+      if (!group_wait2(&bar_prep, ph, nullptr, 0, BAR_S)) {
         aborted = true;
         break;
       }
