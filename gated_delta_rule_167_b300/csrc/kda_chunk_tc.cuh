@@ -386,20 +386,19 @@ __global__ void __launch_bounds__(THREADS, 1)
               const float2 Fi = odd ? wv : sfx;                  // e^{rho - Gamma}
               const float2 eG = mul2(make_float2(eb, eb), u);    // e^{Gamma}
               const float2 eH = mul2(make_float2(ea, ea), sfx);  // e^{Gamma_L - Gamma}
-              const float2 k2 = make_float2(__uint_as_float(kw[i] << 16), __uint_as_float(kw[i] & 0xffff0000u));
-              const float2 q2 = make_float2(__uint_as_float(qw[i] << 16), __uint_as_float(qw[i] & 0xffff0000u));
-              const float2 xk2 = mul2(k2, F), xq2 = mul2(q2, F), y2 = mul2(k2, Fi);
-              const float2 kg2 = mul2(k2, eG), qg2 = mul2(q2, eG), kh2 = mul2(k2, eH);
-              oxk[i] = pack_bf16(xk2.x, xk2.y);
-              oxq[i] = pack_bf16(xq2.x, xq2.y);
-              oy[i] = pack_bf16(y2.x, y2.y);
-              okg[i] = pack_bf16(kg2.x, kg2.y);
-              oqg[i] = pack_bf16(qg2.x, qg2.y);
-              kh[cg][m] = pack_bf16(kh2.x, kh2.y);
+              // the factors to bf16 pairs, then products with the bf16 k / q pairs as loaded
+              const uint32_t Fb = pack_bf16(F.x, F.y), Fib = pack_bf16(Fi.x, Fi.y);
+              const uint32_t eGb = pack_bf16(eG.x, eG.y), eHb = pack_bf16(eH.x, eH.y);
+              oxk[i] = mul_bf16x2(kw[i], Fb);
+              oxq[i] = mul_bf16x2(qw[i], Fb);
+              oy[i] = mul_bf16x2(kw[i], Fib);
+              okg[i] = mul_bf16x2(kw[i], eGb);
+              oqg[i] = mul_bf16x2(qw[i], eGb);
+              kh[cg][m] = mul_bf16x2(kw[i], eHb);
               if (hf == 0) {
                 const float et = R == 0 ? e1 * e2 : e2;
-                const float2 yb2 = mul2(k2, mul2(make_float2(et, et), sfx));  // k e^{rho_B - Gamma}
-                oyb[i] = pack_bf16(yb2.x, yb2.y);
+                const float2 eY = mul2(make_float2(et, et), sfx);  // e^{rho_B - Gamma}
+                oyb[i] = mul_bf16x2(kw[i], pack_bf16(eY.x, eY.y));
               }
             }
             // rows: channel cw + 8 cg + lr; 16-byte chunk: 8-token block 4 hf + li

@@ -291,6 +291,13 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// a * b on bf16 pairs, each product rounded to nearest even (PTX mul.rn.bf16x2).
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // Packs two floats into one bf16x2 word (round to nearest even); `lo` is the lower address.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
