@@ -55,15 +55,16 @@ def _peaks():
         return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
 
 
-# The sources the tensor-core prefill kernel is compiled from (its DRAM counters stay valid while
-# these are unchanged).
+# The sources each timed kernel is compiled from (its DRAM counters stay valid while these are
+# unchanged).
 PREFILL_SOURCES = ("kda_chunk_tc.cuh", "kda_chunk_simt.cuh", "kda_sm100.cuh", "kda_common.cuh")
+DECODE_SOURCES = ("kda_decode.cuh", "kda_common.cuh")
 
 
-def _kernel_source_hash():
+def _kernel_source_hash(sources=PREFILL_SOURCES):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_167_b300", "csrc")
-    for name in PREFILL_SOURCES:
+    for name in sources:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
@@ -75,7 +76,8 @@ def _recorded_traffic(kernel_key):
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)
         ent = rec.get(kernel_key)
-        if ent and ent.get("source_hash") == _kernel_source_hash():
+        sources = DECODE_SOURCES if kernel_key.startswith("decode") else PREFILL_SOURCES
+        if ent and ent.get("source_hash") == _kernel_source_hash(sources):
             return float(ent["dram_bytes_per_launch"])
     except Exception:
         pass
