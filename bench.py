@@ -359,9 +359,12 @@ def bench_prefill(kda, args, world, rank, device, stream, peaks):
     out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     st_h = torch.empty(Sf.shape, dtype=Sf.dtype, pin_memory=True)
 
+    pipe = kda.HostPipeline(device)
+
     def e2e_step():
         kda.chunk_fwd_host(hin["q"], hin["k"], hin["v"], hin["g"], hin["beta"], None, C=C,
-                           device=device, stream=stream, out_host=out_h, state_host=st_h)
+                           device=device, stream=stream, out_host=out_h, state_host=st_h,
+                           pipeline=pipe)
 
     e2e_steps = max(1, min(args.steps, 3))
     e2e_ms, _ = _timed(e2e_step, e2e_steps, 1, world, device, stream)
@@ -369,9 +372,70 @@ def bench_prefill(kda, args, world, rank, device, stream, peaks):
                   "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin.values()),
                   "d2h_bytes_per_step": out_h.numel() * 2 + st_h.numel() * 4,
                   "steps": e2e_steps}
-    del inp, q, k, v, g, b, out, hin
+    del inp, q, k, v, g, b, out, hin, pipe
     torch.cuda.empty_cache()
     return res
+
+
+def _timed_flushed(fn, steps, warmup, device, stream):
+    """Per-iteration CUDA-event timing with the L2 flushed (a 256 MiB write, outside the timed
+    span) before every iteration; for workloads smaller than L2. Returns (mean ms, clocks)."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize(device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    with ClockSampler(device) as cs:
+        for e0, e1 in ev:
+            flush.fill_(1)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize(device)
+    del flush
+    return sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps, cs.summary()
+
+
+def bench_small(kda, args, world, rank, device, stream, peaks, steps=20):
+    """B=1, H=8, T=4096: eight (sequence, head) problems, far fewer than the SMs. Timed as the
+    plain prefill (one CTA per problem) and segment-parallel along T (automatic segments)."""
+    w = kda_synth.WORKLOADS[1]
+    B, T, H, C = w["B"], w["T"], w["H"], w["C"]
+    inp = kda_synth.make_prefill_inputs(B, T, H, D, D, "bf16", seed=w["seed"] + rank,
+                                        S0_std=w["S0_std"], device=device)
+    q, k, v, g, b, S0 = (inp[n] for n in ("q", "k", "v", "g", "beta", "S0"))
+    out = torch.empty(B, T, H, D, dtype=torch.bfloat16, device=device)
+    Sf = torch.empty(B, H, D, D, dtype=torch.float32, device=device)
+    n_seg = kda.segments_auto(B, H, T)
+    ws = torch.empty(max(1, kda.segmented_workspace_bytes(B, H, T, D, D, n_seg)),
+                     dtype=torch.uint8, device=device)
+
+    def plain():
+        kda.kda_chunk_fwd(q, k, v, g, b, S0, out, Sf, C=C, stream=stream)
+
+    def seg():
+        kda.kda_chunk_fwd_segmented(q, k, v, g, b, S0, out, Sf, n_seg, ws, C=C, stream=stream)
+
+    ms_plain, _ = _timed_flushed(plain, steps, 3, device, stream)
+    ms_seg, clocks = _timed_flushed(seg, steps, 3, device, stream)
+    kda.kda_sync_status(stream)
+    token_heads = B * T * H
+    alg = token_heads * BYTES_PER_TOKEN_HEAD + 2 * B * H * STATE_BYTES  # S0 read, S_final written
+    gbs = alg / (ms_seg * 1e-3) / 1e9
+    del inp, q, k, v, g, b, S0, out, ws
+    torch.cuda.empty_cache()
+    return {"workload": w["name"], "n_seg": n_seg, "ms_per_step": ms_seg,
+            "ms_per_step_unsegmented": ms_plain, "tokens_per_s": world * B * T / (ms_seg * 1e-3),
+            "tokens_per_s_unsegmented": world * B * T / (ms_plain * 1e-3),
+            "tflops": token_heads * useful_flops_per_token_head(C) / (ms_seg * 1e-3) / 1e12,
+            "l2": "flushed before every timed iteration (256 MiB write outside the timed span)",
+            "clocks": clocks,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm"], "traffic": None,
+                         "algorithmic_bytes_per_launch": alg,
+                         "note": "43 MB moved: far below the size at which HBM bandwidth can be "
+                                 "reached; the fraction shows the latency floor"}}
 
 
 def bench_decode(kda, args, world, rank, device, stream, peaks, steps=64):
@@ -398,7 +462,11 @@ def bench_decode(kda, args, world, rank, device, stream, peaks, steps=64):
             "tokens_per_s": world * N / (ms_step * 1e-3), "clocks": clocks,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm"],
+                         "frac_of_8tbs": gbs / 8000.0,
                          "traffic": _recorded_traffic("decode_bf16_N256_H96"),
+                         "traffic_note": "ncu DRAM bytes of a 32-sequence step scaled by "
+                                         "sequences; writes still held in L2 when the kernel "
+                                         "ends are not counted, so this is a lower bound",
                          "algorithmic_bytes_per_launch": bytes_step}}
 
 
@@ -431,8 +499,51 @@ def bench_varlen(kda, args, world, rank, device, stream, peaks, steps=3):
             "tflops": T * H * useful_flops_per_token_head(block) / (ms * 1e-3) / 1e12,
             "clocks": clocks,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
-                         "frac": gbs / peaks["hbm"], "traffic": None,
+                         "frac": gbs / peaks["hbm"],
+                         "traffic": _recorded_traffic("varlen_bf16_H96_T131072_C128"),
                          "algorithmic_bytes_per_launch": alg}}
+
+
+def cpu_baseline_varlen(budget_s=8.0):
+    """The oracle on a bounded sample of the packed workload: whole (sequence, head) problems of
+    the shortest sequences, timed on all host cores; tokens = token-heads / H."""
+    import oracle
+
+    w = kda_synth.WORKLOADS[3]
+    T, H = w["T"], w["H"]
+    cu = kda_synth.varlen_cu_seqlens(T, w["n_seq"], w["seed"])
+    lens = sorted((cu[1:] - cu[:-1]).tolist())
+    cores = oracle.default_threads()
+    Ls = lens[0]
+    n = cores
+    x = _cpu_sample(Ls, n, seed=1)
+    t0 = time.perf_counter()
+    oracle.recurrent(*x, nthreads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": n * Ls / H / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} complete (sequence, head) problems of {Ls} tokens (the shortest "
+                      f"packed sequence) in {dt:.2f} s; tokens = token-heads / H={H}"}
+
+
+def cpu_baseline_decode(heads=2048, steps=8):
+    """The oracle's decode step on a bounded sample: `heads` (sequence, head) states for `steps`
+    steps, scaled to the 256 x 96 state; tokens/s = 256 sequences per step."""
+    import oracle
+
+    w = kda_synth.WORKLOADS[4]
+    N, H = w["N"], w["H"]
+    dec = kda_synth.make_decode_inputs(heads, 1, D, D, "bf16", seed=2, steps=steps)
+    S = kda_synth.to_f64_numpy(dec["S"])
+    xs = [[kda_synth.to_f64_numpy(st[n]) for n in ("q", "k", "v", "g", "beta")]
+          for st in dec["steps"]]
+    t0 = time.perf_counter()
+    for x in xs:
+        _, S = oracle.decode_step(*x, S)
+    dt = time.perf_counter() - t0
+    per_step = dt / steps * (N * H) / heads
+    return {"value": N / per_step, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{heads} states x {steps} steps in {dt:.2f} s on one thread, scaled to "
+                      f"{N} x {H} states ({per_step * 1e3:.1f} ms per step)"}
 
 
 def run_gpu(args):
@@ -448,12 +559,16 @@ def run_gpu(args):
     pre = bench_prefill(kda, args, world, rank, device, stream, peaks)
     secondary = {}
     if not args.headline_only:
+        secondary["small"] = bench_small(kda, args, world, rank, device, stream, peaks)
         secondary["decode"] = bench_decode(kda, args, world, rank, device, stream, peaks)
         secondary["varlen"] = bench_varlen(kda, args, world, rank, device, stream, peaks)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline()
+        if not args.headline_only:
+            secondary["decode"]["cpu_baseline"] = cpu_baseline_decode()
+            secondary["varlen"]["cpu_baseline"] = cpu_baseline_varlen()
 
     if rank == 0:
         line = {

@@ -11,6 +11,7 @@ dtype: float32 or bfloat16); states fp32 ``[B, H, d_k, d_v]``.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -20,6 +21,8 @@ __all__ = [
     "KdaError", "KdaLibraryError", "kda_chunk_fwd", "kda_chunk_fwd_varlen",
     "kda_recurrent_step", "kda_sync_status", "kda_status_string", "kda_version", "lib_path",
     "load_library", "chunk_fwd", "chunk_fwd_varlen", "recurrent_step", "chunk_fwd_host",
+    "HostPipeline", "kda_segment_transitions", "kda_segment_scan", "kda_chunk_fwd_segmented",
+    "chunk_fwd_segmented", "segmented_workspace_bytes", "segments_auto",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -32,6 +35,8 @@ _DTYPES = {torch.float32: KDA_DTYPE_F32, torch.bfloat16: KDA_DTYPE_BF16}
 EXPORTED_SYMBOLS = (
     "kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_recurrent_step", "kda_sync_status",
     "kda_wait_selftest", "kda_status_string", "kda_last_error", "kda_version",
+    "kda_segment_transitions", "kda_segment_scan", "kda_chunk_fwd_segmented",
+    "kda_chunk_fwd_segmented_workspace", "kda_segments_auto",
 )
 
 
@@ -70,6 +75,17 @@ def load_library(path: str | None = None):
     lib.kda_chunk_fwd_varlen.restype = S
     lib.kda_recurrent_step.argtypes = [V] * 7 + [I] * 4 + [I, V]
     lib.kda_recurrent_step.restype = S
+    Z = ctypes.c_size_t
+    lib.kda_segment_transitions.argtypes = [V] * 6 + [I] * 9 + [V]
+    lib.kda_segment_transitions.restype = S
+    lib.kda_segment_scan.argtypes = [V] * 4 + [I] * 5 + [V]
+    lib.kda_segment_scan.restype = S
+    lib.kda_chunk_fwd_segmented.argtypes = [V] * 8 + [I] * 7 + [V, Z, I, V]
+    lib.kda_chunk_fwd_segmented.restype = S
+    lib.kda_chunk_fwd_segmented_workspace.argtypes = [I] * 6
+    lib.kda_chunk_fwd_segmented_workspace.restype = Z
+    lib.kda_segments_auto.argtypes = [I] * 3
+    lib.kda_segments_auto.restype = I
     lib.kda_sync_status.argtypes = [V]
     lib.kda_wait_selftest.argtypes = [ctypes.c_ulonglong, V]
     lib.kda_wait_selftest.restype = S
@@ -180,6 +196,75 @@ def kda_recurrent_step(q, k, v, g, beta, S, out, stream=None):
     _check(st, "kda_recurrent_step")
 
 
+def kda_segment_transitions(k, v, g, beta, M, S_tilde, seg_len: int, C: int = 64, stream=None):
+    """(M, S~) of segments of ``seg_len`` tokens: M [n_seg, B, H, d_k, d_k] and S_tilde
+    [n_seg, B, H, d_k, d_v] (fp32, written)."""
+    lib = load_library()
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    n_seg = M.shape[0]
+    _check_tensors([("k", k), ("v", v), ("g", g), ("beta", beta)], k.dtype, k.device)
+    _check_tensors([("M", M), ("S_tilde", S_tilde)], torch.float32, k.device)
+    _require(g.shape == k.shape and v.shape == (B, T, H, dv) and beta.shape == (B, T, H),
+             "k, g [B, T, H, d_k]; v [B, T, H, d_v]; beta [B, T, H]")
+    _require(M.shape == (n_seg, B, H, dk, dk), "M must be [n_seg, B, H, d_k, d_k]")
+    _require(S_tilde.shape == (n_seg, B, H, dk, dv), "S_tilde must be [n_seg, B, H, d_k, d_v]")
+    st = lib.kda_segment_transitions(_ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(M),
+                                     _ptr(S_tilde), B, H, T, int(seg_len), n_seg, dk, dv, int(C),
+                                     _dtype_code(k), _stream_handle(stream))
+    _check(st, "kda_segment_transitions")
+
+
+def kda_segment_scan(M, S_tilde, S0, S_in, stream=None):
+    """S_in[0] = S0 (or zeros), S_in[s + 1] = M[s] S_in[s] + S_tilde[s]; S_in is
+    [n_seg, B, H, d_k, d_v] fp32 (written)."""
+    lib = load_library()
+    n_seg, B, H, dk, dv = S_in.shape
+    _check_tensors([("M", M), ("S_tilde", S_tilde), ("S0", S0), ("S_in", S_in)], torch.float32,
+                   S_in.device)
+    if n_seg > 1:
+        _require(M is not None and M.shape == (n_seg - 1, B, H, dk, dk),
+                 "M must be [n_seg - 1, B, H, d_k, d_k]")
+        _require(S_tilde is not None and S_tilde.shape == (n_seg - 1, B, H, dk, dv),
+                 "S_tilde must be [n_seg - 1, B, H, d_k, d_v]")
+    _require(S0 is None or S0.shape == (B, H, dk, dv), "S0 must be [B, H, d_k, d_v]")
+    st = lib.kda_segment_scan(_ptr(M), _ptr(S_tilde), _ptr(S0), _ptr(S_in), n_seg, B, H, dk, dv,
+                              _stream_handle(stream))
+    _check(st, "kda_segment_scan")
+
+
+def segmented_workspace_bytes(B, H, T, d_k, d_v, n_seg) -> int:
+    return int(load_library().kda_chunk_fwd_segmented_workspace(B, H, T, d_k, d_v, n_seg))
+
+
+def segments_auto(B, H, T) -> int:
+    return int(load_library().kda_segments_auto(B, H, T))
+
+
+def kda_chunk_fwd_segmented(q, k, v, g, beta, S0, out, S_final, n_seg: int, workspace,
+                            C: int = 64, stream=None):
+    """Prefill parallel along T (see include/kda.h); ``workspace`` is a device tensor of at least
+    :func:`segmented_workspace_bytes` bytes (or None when one segment suffices)."""
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    _check_tensors([("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out)],
+                   q.dtype, q.device)
+    _check_tensors([("S0", S0), ("S_final", S_final)], torch.float32, q.device)
+    _check_tensors([("workspace", workspace)], None, q.device)
+    _require(k.shape == q.shape and g.shape == q.shape, "q, k, g must share [B, T, H, d_k]")
+    _require(v.shape == (B, T, H, dv) and out.shape == v.shape, "v/out must be [B, T, H, d_v]")
+    _require(beta.shape == (B, T, H), "beta must be [B, T, H]")
+    for name, s in (("S0", S0), ("S_final", S_final)):
+        _require(s is None or s.shape == (B, H, dk, dv), f"{name} must be [B, H, d_k, d_v]")
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.kda_chunk_fwd_segmented(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0),
+                                     _ptr(out), _ptr(S_final), B, H, T, dk, dv, int(C),
+                                     int(n_seg), _ptr(workspace), nbytes, _dtype_code(q),
+                                     _stream_handle(stream))
+    _check(st, "kda_chunk_fwd_segmented")
+
+
 def kda_sync_status(stream=None):
     """Synchronises the stream and raises if a kernel latched a device-side error."""
     _check(load_library().kda_sync_status(_stream_handle(stream)), "kda_sync_status")
@@ -201,13 +286,20 @@ def kda_version() -> int:
 # ------------------------------------------------------------------------- conveniences
 
 
+def _on(stream):
+    """Makes ``stream`` torch's current stream for the allocations and copies of a call, so
+    that the caching allocator records them on the stream the kernel runs on."""
+    return torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext()
+
+
 def chunk_fwd(q, k, v, g, beta, S0=None, C: int = 64, want_state: bool = True, stream=None):
-    """Allocates the outputs with torch and calls :func:`kda_chunk_fwd`."""
+    """Allocates the outputs with torch (on ``stream``) and calls :func:`kda_chunk_fwd`."""
     B, T, H, dk = q.shape
-    out = torch.empty(B, T, H, v.shape[-1], dtype=q.dtype, device=q.device)
-    Sf = (torch.empty(B, H, dk, v.shape[-1], dtype=torch.float32, device=q.device)
-          if want_state else None)
-    kda_chunk_fwd(q, k, v, g, beta, S0, out, Sf, C=C, stream=stream)
+    with _on(stream):
+        out = torch.empty(B, T, H, v.shape[-1], dtype=q.dtype, device=q.device)
+        Sf = (torch.empty(B, H, dk, v.shape[-1], dtype=torch.float32, device=q.device)
+              if want_state else None)
+        kda_chunk_fwd(q, k, v, g, beta, S0, out, Sf, C=C, stream=stream)
     return out, Sf
 
 
@@ -215,33 +307,105 @@ def chunk_fwd_varlen(q, k, v, g, beta, cu_seqlens, S0=None, C: int = 64, want_st
                      stream=None):
     _, T, H, dk = q.shape
     N = cu_seqlens.shape[0] - 1
-    out = torch.empty(1, T, H, v.shape[-1], dtype=q.dtype, device=q.device)
-    Sf = (torch.empty(N, H, dk, v.shape[-1], dtype=torch.float32, device=q.device)
-          if want_state else None)
-    kda_chunk_fwd_varlen(q, k, v, g, beta, S0, out, Sf, cu_seqlens, C=C, stream=stream)
+    with _on(stream):
+        out = torch.empty(1, T, H, v.shape[-1], dtype=q.dtype, device=q.device)
+        Sf = (torch.empty(N, H, dk, v.shape[-1], dtype=torch.float32, device=q.device)
+              if want_state else None)
+        kda_chunk_fwd_varlen(q, k, v, g, beta, S0, out, Sf, cu_seqlens, C=C, stream=stream)
+    return out, Sf
+
+
+def chunk_fwd_segmented(q, k, v, g, beta, S0=None, C: int = 64, n_seg: int | None = None,
+                        want_state: bool = True, workspace=None, stream=None):
+    """Allocates the outputs (and the workspace, unless given) with torch on ``stream`` and
+    calls :func:`kda_chunk_fwd_segmented`; ``n_seg=None`` takes :func:`segments_auto`."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if n_seg is None:
+        n_seg = segments_auto(B, H, T)
+    with _on(stream):
+        out = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
+        Sf = (torch.empty(B, H, dk, dv, dtype=torch.float32, device=q.device)
+              if want_state else None)
+        need = segmented_workspace_bytes(B, H, T, dk, dv, n_seg)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        kda_chunk_fwd_segmented(q, k, v, g, beta, S0, out, Sf, n_seg, workspace, C=C,
+                                stream=stream)
     return out, Sf
 
 
 def recurrent_step(q, k, v, g, beta, S, stream=None):
-    out = torch.empty(q.shape[0], q.shape[1], v.shape[-1], dtype=q.dtype, device=q.device)
-    kda_recurrent_step(q, k, v, g, beta, S, out, stream=stream)
+    with _on(stream):
+        out = torch.empty(q.shape[0], q.shape[1], v.shape[-1], dtype=q.dtype, device=q.device)
+        kda_recurrent_step(q, k, v, g, beta, S, out, stream=stream)
     return out
 
 
+class HostPipeline:
+    """Reusable device buffers and streams for :func:`chunk_fwd_host`.
+
+    The batch is processed one sequence row at a time on two alternating streams, so that the
+    host-to-device copy of row i + 1, the kernel of row i and the device-to-host copy of row
+    i - 1 can run at the same time (PCIe copies in the two directions use separate engines).
+    Every row's copies and its kernel are ordered on that row's stream; the caller's stream
+    waits for both streams before the call returns."""
+
+    def __init__(self, device, n_streams: int = 2):
+        self.device = torch.device(device)
+        self.streams = [torch.cuda.Stream(device=self.device) for _ in range(n_streams)]
+        self.bufs = {}
+
+    def buffer(self, name, shape, dtype):
+        t = self.bufs.get(name)
+        if t is None or t.shape != torch.Size(shape) or t.dtype != dtype:
+            t = torch.empty(shape, dtype=dtype, device=self.device)
+            self.bufs[name] = t
+        return t
+
+
 def chunk_fwd_host(q, k, v, g, beta, S0=None, C: int = 64, device=None, stream=None,
-                   out_host=None, state_host=None):
-    """End-to-end call on HOST tensors: copies the inputs to the device (pinned host memory
-    gives asynchronous copies), runs :func:`kda_chunk_fwd`, and copies the output and final
-    state back into ``out_host`` / ``state_host`` (allocated pinned if not given)."""
-    device = device or torch.device("cuda", torch.cuda.current_device())
-    nb = True
-    dq, dk_, dv_, dg, db = (t.to(device, non_blocking=nb) for t in (q, k, v, g, beta))
-    dS0 = None if S0 is None else S0.to(device, non_blocking=nb)
-    out, Sf = chunk_fwd(dq, dk_, dv_, dg, db, dS0, C=C, stream=stream)
+                   out_host=None, state_host=None, pipeline: HostPipeline | None = None):
+    """End-to-end call on HOST tensors: copies the inputs to the device, runs
+    :func:`kda_chunk_fwd`, and copies the output and final state back into ``out_host`` /
+    ``state_host`` (allocated pinned if not given).
+
+    Rows of the batch are independent problems, so the work is split by batch row over the
+    streams of ``pipeline`` (created if not given): the copies of one row overlap the kernel
+    and the copies of its neighbours. Pinned host tensors make the copies asynchronous. The
+    function returns once the results are in the host tensors."""
+    device = torch.device(device or torch.device("cuda", torch.cuda.current_device()))
+    pl = pipeline or HostPipeline(device)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    caller = stream if stream is not None else torch.cuda.current_stream(device)
     if out_host is None:
-        out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        out_host = torch.empty(B, T, H, dv, dtype=q.dtype, pin_memory=True)
     if state_host is None:
-        state_host = torch.empty(Sf.shape, dtype=Sf.dtype, pin_memory=True)
-    out_host.copy_(out, non_blocking=nb)
-    state_host.copy_(Sf, non_blocking=nb)
+        state_host = torch.empty(B, H, dk, dv, dtype=torch.float32, pin_memory=True)
+    dq = pl.buffer("q", q.shape, q.dtype)
+    dk_ = pl.buffer("k", k.shape, k.dtype)
+    dv_ = pl.buffer("v", v.shape, v.dtype)
+    dg = pl.buffer("g", g.shape, g.dtype)
+    db = pl.buffer("beta", beta.shape, beta.dtype)
+    dS0 = None if S0 is None else pl.buffer("S0", S0.shape, torch.float32)
+    dout = pl.buffer("out", (B, T, H, dv), q.dtype)
+    dSf = pl.buffer("Sf", (B, H, dk, dv), torch.float32)
+    for s in pl.streams:  # earlier work of the caller (e.g. on the buffers) comes first
+        s.wait_stream(caller)
+    for b in range(B):
+        s = pl.streams[b % len(pl.streams)]
+        with torch.cuda.stream(s):
+            for src, dst in ((q, dq), (k, dk_), (v, dv_), (g, dg), (beta, db)):
+                dst[b:b + 1].copy_(src[b:b + 1], non_blocking=True)
+            if S0 is not None:
+                dS0[b:b + 1].copy_(S0[b:b + 1], non_blocking=True)
+            kda_chunk_fwd(dq[b:b + 1], dk_[b:b + 1], dv_[b:b + 1], dg[b:b + 1], db[b:b + 1],
+                          None if S0 is None else dS0[b:b + 1], dout[b:b + 1], dSf[b:b + 1],
+                          C=C, stream=s)
+            out_host[b:b + 1].copy_(dout[b:b + 1], non_blocking=True)
+            state_host[b:b + 1].copy_(dSf[b:b + 1], non_blocking=True)
+    for s in pl.streams:
+        caller.wait_stream(s)
+    caller.synchronize()
     return out_host, state_host

@@ -2,6 +2,7 @@
 // Declarations and the full contract are in include/kda.h.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <string>
@@ -11,6 +12,7 @@
 #include "kda_chunk_tc.cuh"
 #include "kda_common.cuh"
 #include "kda_decode.cuh"
+#include "kda_scan.cuh"
 #include "kda_selftest.cuh"
 
 namespace {
@@ -90,6 +92,36 @@ kda_status_t run_chunk(const kda::SeqParams& P, int n_problems, int d, int C, kd
                   : launch_simt<__nv_bfloat16, 64>(P, n_problems, C, st);
 }
 
+// Launches the scan of segment transitions (see kda_scan.cuh).
+kda_status_t launch_scan(const float* M, const float* St, const float* S0, float* S_in, int n_seg,
+                         int BH, int d, int d_v, cudaStream_t st) {
+  (void)d_v;
+  dim3 grid(BH, d / (d == 128 ? kda::scan::ScanSmem<128>::NC : kda::scan::ScanSmem<64>::NC));
+  cudaError_t e;
+  if (d == 128) {
+    auto kern = kda::scan::segment_scan_kernel<128, 128>;
+    const int bytes = (int)kda::scan::ScanSmem<128>::bytes;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(segment_scan)");
+    kern<<<grid, kda::scan::THREADS, bytes, st>>>(M, St, S0, S_in, n_seg, BH);
+  } else {
+    auto kern = kda::scan::segment_scan_kernel<64, 64>;
+    const int bytes = (int)kda::scan::ScanSmem<64>::bytes;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(segment_scan)");
+    kern<<<grid, kda::scan::THREADS, bytes, st>>>(M, St, S0, S_in, n_seg, BH);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "segment_scan launch");
+  return KDA_OK;
+}
+
+// Tokens per segment when T is split into (at most) n_seg segments of whole 64-token blocks.
+long long segment_tokens(int T, int n_seg) {
+  const long long blocks = ((long long)T + 63) / 64;
+  return ((blocks + n_seg - 1) / n_seg) * 64;
+}
+
 }  // namespace
 
 extern "C" {
@@ -104,7 +136,8 @@ kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const vo
   if (B < 0 || T < 0) return fail(KDA_ERR_INVALID_ARG, "B and T must be >= 0 (got %d, %d)", B, T);
   if (!(C == 16 || C == 32 || C == 64 || C == 128))
     return fail(KDA_ERR_UNSUPPORTED, "C must be 16, 32, 64 or 128 (got %d)", C);
-  if ((long long)B * T * H * d_k >= (1ll << 40))
+  if ((long long)B * T * H * d_k >= (1ll << 40) || (long long)B * H >= (1ll << 31) ||
+      (long long)B * T >= (1ll << 31))
     return fail(KDA_ERR_UNSUPPORTED, "problem too large");
   const bool tokens = (long long)B * T > 0;
   if ((s = check_ptr(q, "q", tokens)) || (s = check_ptr(k, "k", tokens)) ||
@@ -129,7 +162,8 @@ kda_status_t kda_chunk_fwd_varlen(const void* q, const void* k, const void* v, c
     return fail(KDA_ERR_INVALID_ARG, "N and T_total must be >= 0 (got %d, %d)", N, T_total);
   if (!(C == 16 || C == 32 || C == 64 || C == 128))
     return fail(KDA_ERR_UNSUPPORTED, "C must be 16, 32, 64 or 128 (got %d)", C);
-  if ((long long)T_total * H * d_k >= (1ll << 40))
+  if ((long long)T_total * H * d_k >= (1ll << 40) || (long long)N * H >= (1ll << 31) ||
+      N >= (1 << 30))
     return fail(KDA_ERR_UNSUPPORTED, "problem too large");
   if (cu_seqlens == nullptr) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is NULL");
   if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
@@ -188,6 +222,141 @@ kda_status_t kda_recurrent_step(const void* q, const void* k, const void* v, con
   return KDA_OK;
 }
 
+kda_status_t kda_segment_transitions(const void* k, const void* v, const void* g,
+                                     const void* beta, float* M, float* S_tilde, int B, int H,
+                                     int T, int seg_len, int n_seg, int d_k, int d_v, int C,
+                                     kda_dtype_t dtype, void* stream) {
+  t_last_error.clear();
+  kda_status_t s = check_common(H, d_k, d_v, dtype);
+  if (s != KDA_OK) return s;
+  if (B < 0 || T < 0 || n_seg < 0)
+    return fail(KDA_ERR_INVALID_ARG, "B, T and n_seg must be >= 0 (got %d, %d, %d)", B, T, n_seg);
+  if (seg_len < 1) return fail(KDA_ERR_INVALID_ARG, "seg_len must be >= 1 (got %d)", seg_len);
+  if (!(C == 16 || C == 32 || C == 64 || C == 128))
+    return fail(KDA_ERR_UNSUPPORTED, "C must be 16, 32, 64 or 128 (got %d)", C);
+  if ((long long)B * T * H * d_k >= (1ll << 40) || 2ll * n_seg * B * H >= (1ll << 31) ||
+      (long long)B * T >= (1ll << 31))
+    return fail(KDA_ERR_UNSUPPORTED, "problem too large");
+  const long long work = (long long)n_seg * B * H;
+  if (work == 0) return KDA_OK;
+  const bool tokens = (long long)B * T > 0;
+  if ((s = check_ptr(k, "k", tokens)) || (s = check_ptr(v, "v", tokens)) ||
+      (s = check_ptr(g, "g", tokens)) || (s = check_ptr(beta, "beta", tokens)) ||
+      (s = check_ptr(M, "M", true)) || (s = check_ptr(S_tilde, "S_tilde", true)))
+    return s;
+  // q is never read for its outputs here (none are written); k stands in for it
+  kda::SeqParams P{k, k, v, g, beta, nullptr, nullptr, S_tilde, nullptr, B, H, T};
+  P.seg_len = seg_len;
+  P.n_seg = n_seg;
+  P.n_ident = (int)work;
+  P.M_out = M;
+  return run_chunk(P, (int)(2 * work), d_k, C, dtype, static_cast<cudaStream_t>(stream));
+}
+
+kda_status_t kda_segment_scan(const float* M, const float* S_tilde, const float* S0, float* S_in,
+                              int n_seg, int B, int H, int d_k, int d_v, void* stream) {
+  t_last_error.clear();
+  kda_status_t s = check_common(H, d_k, d_v, KDA_DTYPE_F32);
+  if (s != KDA_OK) return s;
+  if (n_seg < 1 || B < 0)
+    return fail(KDA_ERR_INVALID_ARG, "n_seg must be >= 1 and B >= 0 (got %d, %d)", n_seg, B);
+  if ((long long)B * H >= (1ll << 31) || (long long)n_seg * B * H * d_k * d_v >= (1ll << 40))
+    return fail(KDA_ERR_UNSUPPORTED, "problem too large");
+  if (B == 0) return KDA_OK;
+  if ((s = check_ptr(M, "M", n_seg > 1)) || (s = check_ptr(S_tilde, "S_tilde", n_seg > 1)) ||
+      (s = check_ptr(S0, "S0", false)) || (s = check_ptr(S_in, "S_in", true)))
+    return s;
+  return launch_scan(M, S_tilde, S0, S_in, n_seg, B * H, d_k, d_v,
+                     static_cast<cudaStream_t>(stream));
+}
+
+size_t kda_chunk_fwd_segmented_workspace(int B, int H, int T, int d_k, int d_v, int n_seg) {
+  if (B < 0 || H < 1 || T < 1 || n_seg < 1 || d_k < 1 || d_v < 1) return 0;
+  if (n_seg == 1) return 0;
+  const long long n = ((long long)T + segment_tokens(T, n_seg) - 1) / segment_tokens(T, n_seg);
+  const long long segs = n < 1 ? 1 : n;
+  // M and S~ of the first segs - 1 segments, then S_in of every segment
+  return (size_t)4 * (size_t)B * H * ((size_t)(segs - 1) * ((size_t)d_k * d_k + (size_t)d_k * d_v) +
+                                      (size_t)segs * d_k * d_v);
+}
+
+kda_status_t kda_chunk_fwd_segmented(const void* q, const void* k, const void* v, const void* g,
+                                     const void* beta, const float* S0, void* out,
+                                     float* S_final, int B, int H, int T, int d_k, int d_v, int C,
+                                     int n_seg, void* workspace, size_t workspace_bytes,
+                                     kda_dtype_t dtype, void* stream) {
+  t_last_error.clear();
+  if (n_seg < 1) return fail(KDA_ERR_INVALID_ARG, "n_seg must be >= 1 (got %d)", n_seg);
+  const long long seg = segment_tokens(T, n_seg);
+  const int segs = T > 0 ? (int)(((long long)T + seg - 1) / seg) : 1;
+  if (segs <= 1)
+    return kda_chunk_fwd(q, k, v, g, beta, S0, out, S_final, B, H, T, d_k, d_v, C, dtype, stream);
+  kda_status_t s = check_common(H, d_k, d_v, dtype);
+  if (s != KDA_OK) return s;
+  if (B < 0) return fail(KDA_ERR_INVALID_ARG, "B must be >= 0 (got %d)", B);
+  if (!(C == 16 || C == 32 || C == 64 || C == 128))
+    return fail(KDA_ERR_UNSUPPORTED, "C must be 16, 32, 64 or 128 (got %d)", C);
+  if ((long long)B * T * H * d_k >= (1ll << 40) || 2ll * segs * B * H >= (1ll << 31) ||
+      (long long)B * T >= (1ll << 31))
+    return fail(KDA_ERR_UNSUPPORTED, "problem too large");
+  if (B == 0) return KDA_OK;
+  const size_t need = kda_chunk_fwd_segmented_workspace(B, H, T, d_k, d_v, n_seg);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(KDA_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu%s)", need,
+                workspace_bytes, workspace ? "" : ", NULL");
+  if ((s = check_ptr(q, "q", true)) || (s = check_ptr(k, "k", true)) ||
+      (s = check_ptr(v, "v", true)) || (s = check_ptr(g, "g", true)) ||
+      (s = check_ptr(beta, "beta", true)) || (s = check_ptr(out, "out", true)) ||
+      (s = check_ptr(S0, "S0", false)) || (s = check_ptr(S_final, "S_final", false)) ||
+      (s = check_ptr(workspace, "workspace", true)))
+    return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t BH = (size_t)B * H;
+  float* M = static_cast<float*>(workspace);
+  float* St = M + (size_t)(segs - 1) * BH * d_k * d_k;
+  float* S_in = St + (size_t)(segs - 1) * BH * d_k * d_v;
+  // 1. (M, S~) of every segment but the last
+  kda::SeqParams P1{k, k, v, g, beta, nullptr, nullptr, St, nullptr, B, H, T};
+  P1.seg_len = (int)seg;
+  P1.n_seg = segs - 1;
+  P1.n_ident = (int)((segs - 1) * BH);
+  P1.M_out = M;
+  if ((s = run_chunk(P1, 2 * P1.n_ident, d_k, C, dtype, st)) != KDA_OK) return s;
+  // 2. incoming state of every segment
+  if ((s = launch_scan(M, St, S0, S_in, segs, (int)BH, d_k, d_v, st)) != KDA_OK) return s;
+  // 3. every segment from its incoming state: outputs, and the final state of the last one
+  kda::SeqParams P2{q, k, v, g, beta, S_in, out, S_final, nullptr, B, H, T};
+  P2.seg_len = (int)seg;
+  P2.n_seg = segs;
+  P2.sf_last_only = 1;
+  return run_chunk(P2, (int)(segs * BH), d_k, C, dtype, st);
+}
+
+int kda_segments_auto(int B, int H, int T) {
+  if (B < 1 || H < 1 || T < 1) return 1;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    (void)cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long P = (long long)B * H;
+  const long long nb = ((long long)T + 63) / 64;
+  // cost in 64-token block times: transitions (two problems per segment but the last), the
+  // scan (about a quarter block per segment) and the outputs pass; two extra launches
+  auto waves = [&](long long n) { return (n + sms - 1) / sms; };
+  double best = (double)waves(P) * nb;
+  int best_n = 1;
+  for (int n = 2; n <= 64 && n <= nb; ++n) {
+    const long long L = (nb + n - 1) / n;
+    const int segs = (int)((nb + L - 1) / L);
+    const double cost = (double)waves(2 * P * (segs - 1)) * L + 0.25 * (segs - 1) +
+                        (double)waves(P * segs) * L + 1.0;
+    if (cost < best * 0.97) {
+      best = cost;
+      best_n = segs;
+    }
+  }
+  return best_n;
+}
+
 kda_status_t kda_wait_selftest(unsigned long long limit_ns, void* stream) {
   if (limit_ns == 0 || limit_ns > 10000000000ull)
     return fail(KDA_ERR_INVALID_ARG, "limit_ns must be in (0, 1e10] (got %llu)", limit_ns);
@@ -198,17 +367,24 @@ kda_status_t kda_wait_selftest(unsigned long long limit_ns, void* stream) {
 }
 
 kda_status_t kda_sync_status(void* stream) {
+  static std::atomic<unsigned int> next_slot{0};
   t_last_error.clear();
-  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  unsigned int word = 0, zero = 0;
-  e = cudaMemcpyFromSymbol(&word, kda::g_status, sizeof(word));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Everything queued on `stream` before this call finishes first; then one thread takes the
+  // word and clears it in a single atomic exchange, so a code latched by a kernel on another
+  // stream is either taken here or left for the next call, never lost.
+  const int slot = (int)(next_slot.fetch_add(1u) % (unsigned)kda::kStatusSlots);
+  kda::take_status_kernel<<<1, 1, 0, st>>>(slot);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "status read launch");
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbolAsync(&word, kda::g_status_taken, sizeof(word),
+                                sizeof(word) * (size_t)slot, cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
-  if (word != 0) {
-    e = cudaMemcpyToSymbol(kda::g_status, &zero, sizeof(zero));
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  if (word != 0)
     return fail((kda_status_t)word, "device reported %s", kda_status_string((kda_status_t)word));
-  }
   return KDA_OK;
 }
 

@@ -33,24 +33,65 @@ struct SeqParams {
   const void* g;
   const void* beta;
   const float* S0;
-  void* out;
+  void* out;                  // null: outputs are not written
   float* S_final;
   const int32_t* cu_seqlens;  // null for a dense batch
   int n_seq;                  // dense: B; packed: N
   int H;
   int T;  // dense: tokens per sequence; packed: T_total
+  // Segments of dense sequences (seg_len > 0): problem (s, h) with s = sigma * n_seq + b covers
+  // tokens [sigma * seg_len, min((sigma + 1) * seg_len, T)) of sequence b, sigma < n_seg.
+  int seg_len;
+  int n_seg;
+  // Transition launches (n_ident > 0): problems p < n_ident start from the identity with v = 0,
+  // so their final state is the product of the segment's M_t (written to M_out); problems
+  // p >= n_ident cover the same segments from S0 (or zero) with the real v (final state to
+  // S_final).
+  int n_ident;
+  float* M_out;
+  // Nonzero: only the last segment of a sequence writes its final state, at (sequence, head).
+  int sf_last_only;
 };
 
-// Resolves problem p = (sequence, head) to its token range [t0, t1) and the index of its
-// first token row in the [B, T, H] token grid. Returns false (and records the error) for
-// inconsistent packed offsets.
-__device__ __forceinline__ bool resolve_problem(const SeqParams& P, int p, int& h, size_t& row0,
-                                                int& len) {
-  const int s = p / P.H;
-  h = p % P.H;
+// One (sequence or segment, head) problem of a launch.
+struct Problem {
+  int h;
+  size_t row0;     // first token row in the [rows, H] token grid
+  int len;         // tokens
+  bool ident;      // initial state I and v = 0; S0 is not read
+  long long s0;    // index of the initial state in S0
+  float* sf;       // array the final state goes to (S_final or M_out), or null
+  long long sf_i;  // index in it
+};
+
+// Resolves problem p to its token range and state slots. Returns false (and records the
+// error) for inconsistent packed offsets.
+__device__ __forceinline__ bool resolve_problem(const SeqParams& P, int p, Problem& pr) {
+  int q = p;
+  pr.ident = false;
+  if (P.n_ident > 0) {
+    pr.ident = p < P.n_ident;
+    if (!pr.ident) q = p - P.n_ident;
+  }
+  const int s = q / P.H;
+  pr.h = q % P.H;
+  pr.s0 = q;
+  pr.sf = pr.ident ? P.M_out : P.S_final;
+  pr.sf_i = q;
+  if (P.seg_len > 0) {
+    const int b = s % P.n_seq, sigma = s / P.n_seq;
+    const long long a = (long long)sigma * P.seg_len;
+    pr.row0 = (size_t)b * P.T + (size_t)a;
+    pr.len = (int)max(0ll, min((long long)P.seg_len, (long long)P.T - a));
+    if (P.sf_last_only) {
+      pr.sf = sigma == P.n_seg - 1 ? P.S_final : nullptr;
+      pr.sf_i = (long long)b * P.H + pr.h;
+    }
+    return true;
+  }
   if (P.cu_seqlens == nullptr) {
-    row0 = (size_t)s * P.T;
-    len = P.T;
+    pr.row0 = (size_t)s * P.T;
+    pr.len = P.T;
     return true;
   }
   const int a = P.cu_seqlens[s], b = P.cu_seqlens[s + 1];
@@ -59,8 +100,8 @@ __device__ __forceinline__ bool resolve_problem(const SeqParams& P, int p, int& 
     record_status(1u /* KDA_ERR_INVALID_ARG */);
     return false;
   }
-  row0 = (size_t)a;
-  len = b - a;
+  pr.row0 = (size_t)a;
+  pr.len = b - a;
   return true;
 }
 
@@ -100,13 +141,17 @@ __global__ void __launch_bounds__(THREADS) chunk_simt_kernel(SeqParams P) {
 
   const int p = blockIdx.x;
   const int tid = threadIdx.x;
-  int h, len;
-  size_t row0;
-  if (!resolve_problem(P, p, h, row0, len)) return;
-  const int H = P.H;
+  Problem pr;
+  if (!resolve_problem(P, p, pr)) return;
+  const int H = P.H, h = pr.h, len = pr.len;
+  const size_t row0 = pr.row0;
 
-  for (int i = tid; i < DK * DV; i += THREADS)
-    S[i] = P.S0 ? P.S0[(size_t)p * DK * DV + i] : 0.f;
+  for (int i = tid; i < DK * DV; i += THREADS) {
+    if (pr.ident)
+      S[i] = (i / DV == i % DV) ? 1.f : 0.f;
+    else
+      S[i] = P.S0 ? P.S0[(size_t)pr.s0 * DK * DV + i] : 0.f;
+  }
 
   for (int t0 = 0; t0 < len; t0 += L) {
     const int n = min(L, len - t0);
@@ -127,7 +172,7 @@ __global__ void __launch_bounds__(THREADS) chunk_simt_kernel(SeqParams P) {
     }
     for (int i = tid; i < L * DV; i += THREADS) {
       const int r = i / DV, c = i % DV;
-      Vc[r * DV + c] = r < n ? to_f32(v[((row0 + t0 + r) * H + h) * DV + c]) : 0.f;
+      Vc[r * DV + c] = (r < n && !pr.ident) ? to_f32(v[((row0 + t0 + r) * H + h) * DV + c]) : 0.f;
     }
     for (int r = tid; r < L; r += THREADS) bt[r] = r < n ? to_f32(beta[(row0 + t0 + r) * H + h]) : 0.f;
     __syncthreads();
@@ -211,7 +256,7 @@ __global__ void __launch_bounds__(THREADS) chunk_simt_kernel(SeqParams P) {
     }
     __syncthreads();
     // ---- O = (Q exp Gamma) S + P U, written straight out
-    for (int i = tid; i < n * DV; i += THREADS) {
+    for (int i = tid; out != nullptr && i < n * DV; i += THREADS) {
       const int r = i / DV, c = i % DV;
       float acc = 0.f;
       const float* qr = Qc + r * KP;
@@ -234,8 +279,8 @@ __global__ void __launch_bounds__(THREADS) chunk_simt_kernel(SeqParams P) {
     }
   }
   __syncthreads();
-  if (P.S_final)
-    for (int i = tid; i < DK * DV; i += THREADS) P.S_final[(size_t)p * DK * DV + i] = S[i];
+  if (pr.sf)
+    for (int i = tid; i < DK * DV; i += THREADS) pr.sf[(size_t)pr.sf_i * DK * DV + i] = S[i];
 }
 
 }  // namespace kda

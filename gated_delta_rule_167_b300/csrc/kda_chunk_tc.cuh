@@ -57,6 +57,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <string>
 
 #include "../../include/kda.h"
@@ -115,10 +116,30 @@ constexpr int Y_A = 64;
 constexpr int WLD = 72;
 constexpr int TLD = 20;  // row stride (floats) of the diagonal inverses
 struct TmaMaps {
-  CUtensorMap q, k, v, g;
+  CUtensorMap q, k, v, g, o;  // o: the output, for the stores of whole blocks (unused if out is null)
 };
 
 using namespace sm100;
+
+// 16 x 8 tile of acc += A B over K = 8 nk (nk <= 4) with tf32 warp MMAs on fp32 values already
+// rounded to tf32: A as four 8 x 8 b16 matrix loads (8 rows x 4 fp32 each: rows 0-7 / 8-15 x
+// columns 0-3 / 4-7, which is the tf32 A fragment; Ab has 16-byte aligned rows), B as two
+// 32-bit loads per k step.
+__device__ __forceinline__ void tile_mma(float (&acc)[4], const float* Ab, int lda, const float* Bb,
+                                         int ldb, int nk) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const uint32_t ar = smem_u32(Ab) + 4u * (uint32_t)(((lane & 7) + 8 * ((lane >> 3) & 1)) * lda + 4 * (lane >> 4));
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) {
+    if (ks < nk) {
+      uint32_t a[4];
+      ldsm_x4(ar + 32u * (uint32_t)ks, a);
+      const uint32_t b[2] = {__float_as_uint(Bb[(8 * ks + t) * ldb + g]),
+                             __float_as_uint(Bb[(8 * ks + t + 4) * ldb + g])};
+      mma_tf32(acc, a, b);
+    }
+  }
+}
 
 __device__ __forceinline__ void st_pack8(uint32_t saddr, const float (&x)[8]) {
   st_shared_v4(saddr, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
@@ -137,9 +158,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   //          inverses T_RR (trr) and rounded the A blocks that S multiplies to tf32
   // bar_wsfree: S has read a block's A out of WS (P may put the next one there)
   // bar_khr: P has stored a block's Khat^T and read the previous block's O out of TMEM
-  // bar_D, bar_ZO, bar_G2, bar_G3: tcgen05 products complete
-  __shared__ uint64_t bar_in, bar_v, bar_prep, bar_ext, bar_wsfree, bar_khr, bar_D, bar_ZO, bar_G2,
-      bar_G3;
+  // bar_D, bar_Z (Z^T), bar_ZO (Z^T and O^T), bar_G2, bar_G3: tcgen05 products complete
+  __shared__ uint64_t bar_in, bar_v, bar_prep, bar_ext, bar_wsfree, bar_khr, bar_D, bar_Z, bar_ZO,
+      bar_G2, bar_G3;
   __shared__ uint32_t tmem_base_s;
   __shared__ __align__(16) float beta_s[2][C];  // by block parity
   __shared__ __align__(16) float gl_s[2][D];    // e^{Gamma_L} per key channel, by block parity
@@ -157,11 +178,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;  // mma fragment coordinates
 
-  int h, len;
-  size_t row0;
   const int p = blockIdx.x;
-  if (!resolve_problem(P, p, h, row0, len)) return;
-  const int H = P.H;
+  Problem pr;
+  if (!resolve_problem(P, p, pr)) return;
+  const int H = P.H, h = pr.h, len = pr.len;
+  const size_t row0 = pr.row0;
+  const bool vzero = pr.ident;              // v = 0: no v tile, U^T = -Z^T G^T
+  const bool write_out = P.out != nullptr;  // outputs wanted
   const int nblocks = (len + C - 1) / C;
 
   if (tid == 0) {
@@ -172,6 +195,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bar_wsfree, 1);
     mbar_init(&bar_khr, 1);
     mbar_init(&bar_D, 1);
+    mbar_init(&bar_Z, 1);
     mbar_init(&bar_ZO, 1);
     mbar_init(&bar_G2, 1);
     mbar_init(&bar_G3, 1);
@@ -233,11 +257,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     unsigned short beta_next = 0;
     if (lt < C && lt < len) beta_next = beta_u[(row0 + lt) * H + h];
     __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(P.out);
-    // O of block b: TMEM -> bf16 rows [token][128] staged in XK (free: this group's A/P product
-    // of the block after b has completed, and the next operands are written after the group's
-    // next barrier), then, after a group barrier, 16-byte global stores, each warp writing two
-    // whole 256-byte rows. The 16-byte chunks of a staged row are permuted by chunk ^ (token % 8)
-    // so that the eight rows of a matrix store fall in distinct banks.
+    // O of block b: TMEM -> bf16 staged in XK (free: this group's A/P product of the block after b
+    // has completed, and the next operands are written after the bulk store has read it) as two
+    // 64-channel boxes of [64 tokens][128 B] in the 128-byte swizzle of the TMA map (16-byte chunk
+    // c of token row r at c ^ (r % 8), which also puts the eight rows of a matrix store in
+    // distinct banks); then, after a group barrier, one thread stores a whole block with two TMA
+    // stores, and a partial block is written with 16-byte stores of the rows that exist.
     // Warp w reads lanes (value channels) 32 (w % 4) .. + 31, columns (tokens) 32 hh .. + 31 in the
     // 16 x 256 b shape, whose registers are the m16n8 fragment that a transposed matrix store
     // writes as [token][channel] rows.
@@ -255,29 +280,42 @@ __global__ void __launch_bounds__(THREADS, 1)
           // matrix i: channels cb + 8 (i & 1) .., tokens 32 hh + 8 (2u + (i >> 1)) ..
           const int li = lane >> 3, lj = lane & 7;
           const int tok = 32 * hh + 8 * (2 * u + (li >> 1)) + lj;
-          const int chunk = ((cb + 8 * (li & 1)) >> 3) ^ (tok & 7);
+          const int ch = (cb + 8 * (li & 1)) >> 3;  // 16-byte chunk of the 256-byte row
+          const uint32_t so = (uint32_t)((ch >> 3) * BOX_BYTES + tok * 128 + 16 * ((ch & 7) ^ (tok & 7)));
           const int k0 = 2 * u, k1 = 2 * u + 1;
-          stsm_x4_trans(stg_s + (uint32_t)(tok * 256 + 16 * chunk),
+          stsm_x4_trans(stg_s + so,
                         pack_bf16(__uint_as_float(v[4 * k0]), __uint_as_float(v[4 * k0 + 1])),
                         pack_bf16(__uint_as_float(v[4 * k0 + 2]), __uint_as_float(v[4 * k0 + 3])),
                         pack_bf16(__uint_as_float(v[4 * k1]), __uint_as_float(v[4 * k1 + 1])),
                         pack_bf16(__uint_as_float(v[4 * k1 + 2]), __uint_as_float(v[4 * k1 + 3])));
         }
       }
+      fence_proxy_async_smem();  // the TMA store reads the staged rows
       tc_fence_before();
     };
     // after a group barrier that follows stage_o(b)
+    bool pend_store = false;  // a bulk store of this group's thread 0 may still read XK
     auto store_o = [&](int b) {
       const int tb = b * C;
       const int nb = min(C, len - tb);
+      if (nb == C) {
+        if (lt == 0) {
+          const int row = (int)(row0 + (size_t)tb);
+          tma_store_3d(&maps.o, sm + XK, 0, h, row);
+          tma_store_3d(&maps.o, sm + XK + BOX_BYTES, 64, h, row);
+          bulk_commit();
+          pend_store = true;
+        }
+        return;
+      }
       const int q = lt & 15;  // 16-byte chunk of a row; rows lt / 16 + 16 i
       __nv_bfloat16* ob = out + ((row0 + tb + (lt >> 4)) * H + h) * D + 8 * q;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = (lt >> 4) + 16 * i;
         if (r < nb)
-          *reinterpret_cast<uint4*>(ob + (size_t)(16 * i) * H * D) =
-              *reinterpret_cast<const uint4*>(stg + r * 256 + 16 * (q ^ (r & 7)));
+          *reinterpret_cast<uint4*>(ob + (size_t)(16 * i) * H * D) = *reinterpret_cast<const uint4*>(
+              stg + (q >> 3) * BOX_BYTES + r * 128 + 16 * ((q & 7) ^ (r & 7)));
       }
     };
 
@@ -288,6 +326,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       // S has started the previous block (its first product read (K/Q e^Gamma)^T and the
       // per-parity arrays of two blocks ago are no longer read) and the previous A/P product
       // has released X and Y.
+      if (pend_store) {  // (thread 0 only) the previous block's bulk store has read XK
+        bulk_wait_read();
+        pend_store = false;
+      }
       if (blk > 0 && !group_wait2(&bar_ZO, (blk - 1) & 1, &bar_D, (blk - 1) & 1, BAR_P)) {
         aborted = true;
         break;
@@ -495,9 +537,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       fence_proxy_async_smem();  // P is a tensor-core operand of S's last product
       named_sync(BAR_P, GROUP);
       // ---------------- first step of the solve of T = (I + A)^{-1}, which needs A only: the
-      // 16 x 16 diagonal inverses T_RR (fp32, rounded to tf32 into trr; the state group reads trr
-      // from bar_ext until it releases WS), and the blocks of A that the state group uses as MMA
-      // A operands rounded to tf32 in place
+      // 16 x 16 diagonal inverses T_RR (fp32, rounded to tf32 into trr), and the blocks of A that
+      // the warp MMAs of the later steps take as A operands rounded to tf32 in place
       {
         float* ws = reinterpret_cast<float*>(sm + WS);
         if (lt >= GROUP - 64) {
@@ -534,6 +575,41 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       named_sync(BAR_P, GROUP);
+      // ---------------- second step: the off-diagonal 16 x 16 block of each 32-token half,
+      // T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22 (block-inverse identity), by warps
+      // 0-3 as tf32 warp MMAs; warps 4-7 copy the diagonal inverses into the diagonal blocks of
+      // WS, where A_RR is no longer read. Warp (h, n) of warps 0-3 (h = half, n = 8-column
+      // half) makes columns 8n .. 8n + 7 of Y = A_10 T_00 (into the scratch qs: rows 0..31,
+      // columns 32..63 of WS, where A is zero and T keeps nothing), then of T_10 = -T_11 Y.
+      {
+        float* ws = reinterpret_cast<float*>(sm + WS);
+        float* qs = ws + 32;
+        if (warp < 4) {
+          const int tile = warp >> 1, nh = warp & 1;
+          float* y = qs + 16 * tile + 8 * nh;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma(acc, ws + (16 + 32 * tile) * WLD + 32 * tile, WLD, &trr[2 * tile][0][8 * nh], TLD, 2);
+          float* yo = y + 2 * t;
+          yo[g * WLD] = tf32r(acc[0]);
+          yo[g * WLD + 1] = tf32r(acc[1]);
+          yo[(g + 8) * WLD] = tf32r(acc[2]);
+          yo[(g + 8) * WLD + 1] = tf32r(acc[3]);
+          __syncwarp();
+          float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma(acc2, &trr[2 * tile + 1][0][0], TLD, y, WLD, 2);
+          float* o = ws + (16 + 32 * tile) * WLD + 32 * tile + 8 * nh + 2 * t;
+          o[g * WLD] = tf32r(-acc2[0]);
+          o[g * WLD + 1] = tf32r(-acc2[1]);
+          o[(g + 8) * WLD] = tf32r(-acc2[2]);
+          o[(g + 8) * WLD + 1] = tf32r(-acc2[3]);
+        } else {
+          for (int e = lt - 128; e < 1024; e += 128) {
+            const int R = e >> 8, i = (e >> 4) & 15, j = e & 15;
+            ws[(16 * R + i) * WLD + 16 * R + j] = trr[R][i][j];
+          }
+        }
+      }
+      named_sync(BAR_P, GROUP);
       if (lt == 0) mbar_arrive(&bar_ext);
       // ---------------- once S's last product of the previous block is complete: Khat^T of this
       // block (that product read the previous one) and the previous block's O
@@ -548,24 +624,31 @@ __global__ void __launch_bounds__(THREADS, 1)
           stsm_x4(sb + KH + sw128_off((uint32_t)(16 * warp + 8 * cg + (lane & 7)), (uint32_t)(8 * (4 * hf + (lane >> 3)))),
                   kh[cg][4 * hf], kh[cg][4 * hf + 1], kh[cg][4 * hf + 2], kh[cg][4 * hf + 3]);
       fence_proxy_async_smem();
-      if (blk > 0) stage_o(blk - 1);
+      if (blk > 0 && write_out) stage_o(blk - 1);
       named_sync(BAR_P, GROUP);
       // Khat^T is stored and the previous block's O is out of TMEM; its global stores follow (the
       // release of this arrive does not wait for them)
       if (lt == 0) mbar_arrive(&bar_khr);
-      if (blk > 0) store_o(blk - 1);
+      if (blk > 0 && write_out) store_o(blk - 1);
     }
     if (!aborted && nblocks > 0) {  // the last block's O
+      if (pend_store) {  // (thread 0 only) the previous block's bulk store has read XK
+        bulk_wait_read();
+        pend_store = false;
+      }
       if (group_wait2(&bar_G3, (nblocks - 1) & 1, nullptr, 0, BAR_P)) {
         tc_fence_after();
-        stage_o(nblocks - 1);
-        named_sync(BAR_P, GROUP);
-        store_o(nblocks - 1);
+        if (write_out) {
+          stage_o(nblocks - 1);
+          named_sync(BAR_P, GROUP);
+          store_o(nblocks - 1);
+        }
       } else {
         aborted = true;
       }
     }
     if (aborted) record_status(4u /* KDA_ERR_TIMEOUT */);
+    if (pend_store) bulk_wait_all();  // (thread 0) the output stores have completed
     if (lt == 0) {  // let anything already issued land before the CTA's memory goes away
       if (aborted && pend_in) (void)mbar_wait(&bar_in, in_blk & 1);
       if (d_blk >= 0) (void)mbar_wait(&bar_D, d_blk & 1);
@@ -583,13 +666,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     // ---- initial state S^T: lane v = c, key channels 64 hh .. 64 hh + 63 (coalesced over v)
     {
-      const float* s0 = P.S0 ? P.S0 + (size_t)p * D * D + c : nullptr;
+      const float* s0 = (P.S0 && !pr.ident) ? P.S0 + (size_t)pr.s0 * D * D + c : nullptr;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t sv[32], sbf[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          sv[j] = s0 ? __float_as_uint(s0[(size_t)(64 * hh + 32 * half + j) * D]) : 0u;
+        for (int j = 0; j < 32; ++j) {
+          const int cc = 64 * hh + 32 * half + j;  // key channel
+          sv[j] = s0 ? __float_as_uint(s0[(size_t)cc * D]) : ((pr.ident && cc == c) ? 0x3F800000u : 0u);
+        }
         tmem_st32(tl + T_ST + 64 * hh + 32 * half, sv);
 #pragma unroll
         for (int j = 0; j < 16; ++j) sbf[j] = pack_bf16(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]));
@@ -602,7 +687,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int v_blk = 0;  // block of the last v load issued
     uint64_t* last_mma = &bar_ZO;
     uint32_t last_par = 0;
-    if (nblocks > 0) {
+    if (nblocks > 0 && !vzero) {
       if (leader) issue_v(0);
       pend_v = true;
     }
@@ -627,15 +712,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_after();
       const uint32_t t_ot = t_ot_of(blk);  // this block's O^T columns
-      // ---------------- tcgen05: [O^T | Z^T] (even) or [Z^T | O^T] (odd) =
-      // S^T [(Q e^Gamma)^T | (K e^Gamma)^T] (or the other order) (N 128, K 128)
+      // ---------------- tcgen05: Z^T = S^T (K e^Gamma)^T, then O^T = S^T (Q e^Gamma)^T (N 64 each,
+      // K 128), committed separately so that Z^T can be converted while O^T is computed
       if (leader) {
         tc_fence_after();
-        const uint32_t id_zo = idesc_bf16(128, 128, 0, 1, 0);
+        const uint32_t id_h = idesc_bf16(128, 64, 0, 1, 0);
+        const uint32_t kg = sb + KQ + (par ? 0u : 16384u), qg = sb + KQ + (par ? 16384u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_tmem_a(tmem + (par ? T_ZT : t_ot), tmem + T_SB + 8u * kk,
-                           desc_sw128(sb + KQ + 2048u * kk, 16384, 1024), id_zo, kk > 0);
+          umma_bf16_tmem_a(tmem + T_ZT, tmem + T_SB + 8u * kk, desc_sw128(kg + 2048u * kk, 16384, 1024),
+                           id_h, kk > 0);
+        umma_commit(&bar_Z);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_tmem_a(tmem + t_ot, tmem + T_SB + 8u * kk, desc_sw128(qg + 2048u * kk, 16384, 1024),
+                           id_h, kk > 0);
         umma_commit(&bar_ZO);
       }
       pend_mma = true; last_mma = &bar_ZO; last_par = ph;
@@ -668,8 +759,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       // ---------------- Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand; then wait for group P
       // to have written A, P and the diagonal inverses of this block (bar_ext)
-      if (!group_wait2(&bar_ZO, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
-      pend_mma = false;
+      if (!group_wait2(&bar_Z, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       tc_fence_after();
       {
         uint32_t v[32], zb[16];
@@ -681,102 +771,60 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!group_wait2(&bar_ext, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       // ---------------- T = (I + A)^{-1} (unit lower triangular) and G = T Diag(beta) (bf16)
-      // From the 16 x 16 diagonal inverses T_RR (group P, in trr) and the block-inverse identity
-      // [[P, 0], [C, Q]]^{-1} = [[P^{-1}, 0], [-Q^{-1} C P^{-1}, Q^{-1}]]: the off-diagonal
-      // 16 x 16 block of each 32 x 32 half and then the off-diagonal 32 x 32 block, as tf32 warp
-      // MMAs on fp32 blocks in WS (T overwrites A where A is no longer read).
+      // Group P has placed the diagonal inverses T_RR and the off-diagonal blocks T_10, T_32 of
+      // each 32-token half in WS. The block-inverse identity
+      // [[P, 0], [C, Q]]^{-1} = [[P^{-1}, 0], [-Q^{-1} C P^{-1}, Q^{-1}]] for the two halves gives
+      // the off-diagonal 32 x 32 block T_(32)10 = -T_(32)11 A_(32)10 T_(32)00 (tf32 warp MMAs).
       {
         float* ws = reinterpret_cast<float*>(sm + WS);
-        // scratch: rows 0..31, columns 32..63 of WS, where A is zero and no block of T is kept
-        float* qs = ws + 32;
+        float* qs = ws + 32;  // scratch: rows 0..31, columns 32..63 of WS
         const int sw = warp - GROUP / 32;  // warp index inside the group
         const float* bt = beta_s[par];
-        // 16 x 8 tile: acc += A B over K = 8 nk. Every value of the solve is rounded to tf32 where
-        // it is written, so operands load as they are: A as four 8 x 8 b16 matrices (8 rows x 4 fp32 each: rows 0-7 / 8-15 x columns
-        // 0-3 / 4-7, which is the tf32 A fragment), B as two 32-bit loads. Ab: 16-byte aligned rows.
-        auto tile_mma = [&](float (&acc)[4], const float* Ab, int lda, const float* Bb, int ldb,
-                            int nk) {
-          const uint32_t ar = smem_u32(Ab) + 4u * (uint32_t)(((lane & 7) + 8 * ((lane >> 3) & 1)) * lda + 4 * (lane >> 4));
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            if (ks < nk) {
-              uint32_t a[4];
-              ldsm_x4(ar + 32u * (uint32_t)ks, a);
-              const uint32_t b[2] = {__float_as_uint(Bb[(8 * ks + t) * ldb + g]),
-                                     __float_as_uint(Bb[(8 * ks + t + 4) * ldb + g])};
-              mma_tf32(acc, a, b);
-            }
-          }
-        };
         // two adjacent entries of G = T Diag(beta): row r, columns j and j + 1 (j even)
         auto g_store = [&](int r, int j, float x0, float x1) {
           *reinterpret_cast<uint32_t*>(sm + GB + sw128_off((uint32_t)r, (uint32_t)j)) =
               pack_bf16(x0 * bt[j], x1 * bt[j + 1]);
         };
-        // (2) warp (h, n) of warps 0-3, h = 32-row half, n = 8-column half: columns 8n .. 8n + 7
-        //     of Y = A_10 T_00 (into qs), then of T_10 = -T_11 Y (into WS), which need no other
-        //     columns of Y (h = 1: A_32, T_22, T_33, T_32); warps 4-7: the T_RR into the diagonal
-        //     blocks of WS, where A_RR is no longer read, and G of the diagonal blocks
-        if (sw < 4) {
-          const int tile = sw >> 1, nh = sw & 1;
-          float* y = qs + 16 * tile + 8 * nh;
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          tile_mma(acc, ws + (16 + 32 * tile) * WLD + 32 * tile, WLD, &trr[2 * tile][0][8 * nh], TLD, 2);
-          float* yo = y + 2 * t;
-          yo[g * WLD] = tf32r(acc[0]);
-          yo[g * WLD + 1] = tf32r(acc[1]);
-          yo[(g + 8) * WLD] = tf32r(acc[2]);
-          yo[(g + 8) * WLD + 1] = tf32r(acc[3]);
-          __syncwarp();
-          float acc2[4] = {0.f, 0.f, 0.f, 0.f};
-          tile_mma(acc2, &trr[2 * tile + 1][0][0], TLD, y, WLD, 2);
-          float* o = ws + (16 + 32 * tile) * WLD + 32 * tile + 8 * nh + 2 * t;
-          o[g * WLD] = tf32r(-acc2[0]);
-          o[g * WLD + 1] = tf32r(-acc2[1]);
-          o[(g + 8) * WLD] = tf32r(-acc2[2]);
-          o[(g + 8) * WLD + 1] = tf32r(-acc2[3]);
-        } else {
-          for (int e = lt - 128; e < 1024; e += 128) {
-            const int R = e >> 8, i = (e >> 4) & 15, j = e & 15;
-            ws[(16 * R + i) * WLD + 16 * R + j] = trr[R][i][j];
-          }
-          for (int e = lt - 128; e < 512; e += 128) {
+        // warp (n, m), n = sw & 3, m = sw >> 2: tile (m, n) of Q = A_(32)10 T_(32)00 (rows
+        // 32 + 16 m .., columns 8 n .., K 32; into qs); the two warps of column block n meet at
+        // their own barrier; then tile (m, n) of G rows 32..63: T_(32)10 = -T_(32)11 Q. Every
+        // thread also writes three pairs of G from the blocks group P placed in WS.
+        const int nt = sw & 3, mt = sw >> 2;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma(acc, ws + (32 + 16 * mt) * WLD, WLD, ws + 8 * nt, WLD, 4);
+        float* o = qs + 16 * mt * WLD + 8 * nt + 2 * t;
+        o[g * WLD] = tf32r(acc[0]);
+        o[g * WLD + 1] = tf32r(acc[1]);
+        o[(g + 8) * WLD] = tf32r(acc[2]);
+        o[(g + 8) * WLD + 1] = tf32r(acc[3]);
+#pragma unroll
+        for (int e = lt; e < 768; e += GROUP) {
+          int r, j;
+          if (e < 512) {  // diagonal blocks
             const int R = e >> 7, i = (e >> 3) & 15, jp = 2 * (e & 7);
-            g_store(16 * R + i, 16 * R + jp, trr[R][i][jp], trr[R][i][jp + 1]);
+            r = 16 * R + i;
+            j = 16 * R + jp;
+          } else {  // T_10 and T_32
+            const int e2 = e - 512, tile = e2 >> 7, i = (e2 >> 3) & 15, jp = 2 * (e2 & 7);
+            r = 16 + 32 * tile + i;
+            j = 32 * tile + jp;
           }
+          g_store(r, j, ws[r * WLD + j], ws[r * WLD + j + 1]);
         }
-        named_sync(BAR_S, GROUP);
-        // (3) warp (n, m), n = sw & 3, m = sw >> 2: tile (m, n) of Q = A_(32)10 T_(32)00 (rows
-        //     32 + 16 m .., columns 8 n .., K 32; into qs); the two warps of column block n meet
-        //     at their own barrier; then tile (m, n) of G rows 32..63: T_(32)10 = -T_(32)11 Q.
-        //     Every thread also writes one pair of G of T_10 and T_32.
-        {
-          const int nt = sw & 3, mt = sw >> 2;
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          tile_mma(acc, ws + (32 + 16 * mt) * WLD, WLD, ws + 8 * nt, WLD, 4);
-          float* o = qs + 16 * mt * WLD + 8 * nt + 2 * t;
-          o[g * WLD] = tf32r(acc[0]);
-          o[g * WLD + 1] = tf32r(acc[1]);
-          o[(g + 8) * WLD] = tf32r(acc[2]);
-          o[(g + 8) * WLD + 1] = tf32r(acc[3]);
-          {
-            const int tile = lt >> 7, i = (lt >> 3) & 15, jp = 2 * (lt & 7);
-            const int r = 16 + 32 * tile + i, j = 32 * tile + jp;
-            g_store(r, j, ws[r * WLD + j], ws[r * WLD + j + 1]);
-          }
-          named_sync(BAR_PAIR0 + nt, 64);
-          float acc2[4] = {0.f, 0.f, 0.f, 0.f};
-          tile_mma(acc2, ws + (32 + 16 * mt) * WLD + 32, WLD, qs + 8 * nt, WLD, 4);
-          const int r = 32 + 16 * mt + g, j = 8 * nt + 2 * t;
-          g_store(r, j, -acc2[0], -acc2[1]);
-          g_store(r + 8, j, -acc2[2], -acc2[3]);
-        }
+        named_sync(BAR_PAIR0 + nt, 64);
+        float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma(acc2, ws + (32 + 16 * mt) * WLD + 32, WLD, qs + 8 * nt, WLD, 4);
+        const int r = 32 + 16 * mt + g, j = 8 * nt + 2 * t;
+        g_store(r, j, -acc2[0], -acc2[1]);
+        g_store(r + 8, j, -acc2[2], -acc2[3]);
       }
       fence_proxy_async_smem();  // G is a tensor-core operand
       tmem_st_wait();
       tc_fence_before();
-      if (!group_wait2(&bar_v, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
-      pend_v = false;
+      if (!vzero) {
+        if (!group_wait2(&bar_v, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
+        pend_v = false;
+      }
       if (leader) mbar_arrive(&bar_wsfree);  // WS is no longer read
       // ---------------- tcgen05: U^T = V^T G^T - Z^T G^T (M 128, N 64, K 64), which is
       // U = T Diag(beta) (V - Z), the solution of (I + A) U = Diag(beta) (V - Z)
@@ -787,8 +835,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t bg = desc_sw128(sb + GB + 32u * kk, 16, 1024);
-          umma_bf16(tmem + T_UT, desc_sw128(sb + IN_V + 2048u * kk, BOX_BYTES, 1024), bg, id_v, kk > 0);
-          umma_bf16_tmem_a(tmem + T_UT, tmem + T_ZB + 8u * kk, bg, id_z, 1);
+          if (!vzero)
+            umma_bf16(tmem + T_UT, desc_sw128(sb + IN_V + 2048u * kk, BOX_BYTES, 1024), bg, id_v, kk > 0);
+          umma_bf16_tmem_a(tmem + T_UT, tmem + T_ZB + 8u * kk, bg, id_z, (kk > 0 || !vzero) ? 1u : 0u);
         }
         umma_commit(&bar_G2);
       }
@@ -808,7 +857,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       named_sync(BAR_S, GROUP);
       if (aborted) break;
-      if (blk + 1 < nblocks) {  // the v tile is dead
+      if (blk + 1 < nblocks && !vzero) {  // the v tile is dead
         if (leader) issue_v(blk + 1);
         pend_v = true;
         v_blk = blk + 1;
@@ -855,8 +904,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (pend_mma) (void)mbar_wait(last_mma, last_par);
         if (pend_v) (void)mbar_wait(&bar_v, v_blk & 1);
       }
-    } else if (P.S_final) {  // S_final[c'][v] from S^T (lane v): coalesced over v
-      float* sf = P.S_final + (size_t)p * D * D + c;
+    } else if (pr.sf) {  // S_final[c'][v] from S^T (lane v): coalesced over v
+      float* sf = pr.sf + (size_t)pr.sf_i * D * D + c;
       uint32_t v[32];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -896,6 +945,10 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 inline bool encode_token_map(CUtensorMap* m, const void* base, long long rows, int H) {
   auto fn = encode_fn();
   if (!fn) return false;
+  if (base == nullptr) {  // an unused map (no output): keep it zero
+    memset(m, 0, sizeof(*m));
+    return true;
+  }
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
   cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
@@ -915,7 +968,8 @@ inline kda_status_t launch_chunk_tc(const SeqParams& P, int n_problems, int C, c
   tc::TmaMaps maps;
   const long long rows = P.cu_seqlens ? (long long)P.T : (long long)P.n_seq * P.T;
   if (!tc::encode_token_map(&maps.q, P.q, rows, P.H) || !tc::encode_token_map(&maps.k, P.k, rows, P.H) ||
-      !tc::encode_token_map(&maps.v, P.v, rows, P.H) || !tc::encode_token_map(&maps.g, P.g, rows, P.H)) {
+      !tc::encode_token_map(&maps.v, P.v, rows, P.H) || !tc::encode_token_map(&maps.g, P.g, rows, P.H) ||
+      !tc::encode_token_map(&maps.o, P.out, rows, P.H)) {
     err = "cuTensorMapEncodeTiled failed";
     return KDA_ERR_CUDA;
   }

@@ -8,9 +8,18 @@
 namespace kda {
 
 // Device-side status word of the library (one per device, in the library's own image; the
-// library is a single translation unit). Kernels record the first error they meet;
-// kda_sync_status() reads and clears it.
+// library is a single translation unit). Kernels on every stream record the first error they
+// meet into the same word; kda_sync_status() takes it and clears it in one atomic exchange.
 __device__ unsigned int g_status = 0u;
+
+// Slots into which kda_sync_status() moves the status word (one slot per call in flight, so
+// that overlapping calls from several host threads do not read each other's result).
+constexpr int kStatusSlots = 64;
+__device__ unsigned int g_status_taken[kStatusSlots];
+
+__global__ void take_status_kernel(int slot) {
+  g_status_taken[slot] = atomicExch(&g_status, 0u);
+}
 
 __device__ __forceinline__ void record_status(unsigned int code) {
   atomicCAS(&g_status, 0u, code);

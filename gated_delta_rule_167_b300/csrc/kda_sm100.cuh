@@ -394,47 +394,8 @@ __device__ __forceinline__ void stsm_x4(uint32_t saddr, uint32_t r0, uint32_t r1
                : "memory");
 }
 
-// d += A B for one 8-wide k step, with each operand split into a tf32 head and a tf32 tail
-// (x = hi + lo); the three products hi*hi + hi*lo + lo*hi carry about fp32 accuracy.
-__device__ __forceinline__ void mma_3xtf32(float (&d)[4], const float (&a)[4], const float (&b)[2]) {
-  uint32_t ah[4], al[4], bh[2], bl[2];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    ah[i] = to_tf32(a[i]);
-    al[i] = to_tf32(a[i] - __uint_as_float(ah[i]));
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    bh[i] = to_tf32(b[i]);
-    bl[i] = to_tf32(b[i] - __uint_as_float(bh[i]));
-  }
-  mma_tf32(d, al, bh);
-  mma_tf32(d, ah, bl);
-  mma_tf32(d, ah, bh);
-}
-
-// Same three products as mma_3xtf32, each into its own accumulator (acc[0] + acc[1] + acc[2]
-// is the result) so that consecutive k steps do not wait on one another.
-__device__ __forceinline__ void mma_3xtf32_split(float (&acc)[3][4], const float (&a)[4],
-                                                 const float (&b)[2]) {
-  uint32_t ah[4], al[4], bh[2], bl[2];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    ah[i] = to_tf32(a[i]);
-    al[i] = to_tf32(a[i] - __uint_as_float(ah[i]));
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    bh[i] = to_tf32(b[i]);
-    bl[i] = to_tf32(b[i] - __uint_as_float(bh[i]));
-  }
-  mma_tf32(acc[2], al, bh);
-  mma_tf32(acc[1], ah, bl);
-  mma_tf32(acc[0], ah, bh);
-}
-
-// ---------------------------------------------------------------- TMA stores
-// 3-D tiled TMA store from shared memory; completion is tracked with bulk groups.
+// 3-D tiled TMA store from shared memory to global; completion is tracked with bulk groups of
+// the issuing thread.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1,
                                              int c2) {
   asm volatile(
@@ -448,12 +409,12 @@ __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-// Waits until every committed bulk store has finished reading its shared-memory source.
+// Waits until every committed bulk store of this thread has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-// Waits until every committed bulk store has completed.
+// Waits until every committed bulk store of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }

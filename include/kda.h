@@ -32,6 +32,7 @@
 #ifndef KDA_H_
 #define KDA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -93,8 +94,72 @@ kda_status_t kda_recurrent_step(const void* q, const void* k, const void* v, con
                                 const void* beta, float* S, void* out, int N, int H, int d_k,
                                 int d_v, kda_dtype_t dtype, void* stream);
 
-/* Synchronises `stream`, then returns and clears the device-side status word of the current
- * device (KDA_OK if nothing was latched), or KDA_ERR_CUDA if the synchronisation failed. */
+/*
+ * Segment transitions (Kimi K3 wiki, "Notations mathématiques", table "Attention et KDA": the
+ * transition M_t and S~, the state computed from S = 0; "Glossaire", entry "KCP": the pair
+ * (cumulative M, local S~) of a stretch of tokens composes associatively and exactly).
+ * Segment sigma (0 <= sigma < n_seg) of sequence b covers its tokens
+ * [sigma * seg_len, min((sigma + 1) * seg_len, T)); for every (sigma, b, h) this writes
+ *   M       [n_seg, B, H, d_k, d_k] fp32 : the product M_{last} ... M_{first} of the segment
+ *   S_tilde [n_seg, B, H, d_k, d_v] fp32 : the state the segment reaches from S = 0
+ * so that S_after = M S_before + S~ for any incoming state. An empty segment gives (I, 0).
+ *   k, g : [B, T, H, d_k] dtype   v : [B, T, H, d_v] dtype   beta : [B, T, H] dtype
+ * Requires d_k = d_v (supported head sizes as above); seg_len >= 1. Computed by the prefill
+ * kernels themselves (M as the final state of a run from S0 = I with v = 0, S~ as that of a run
+ * from S0 = 0), so the precision is that of kda_chunk_fwd for the same dtype.
+ */
+kda_status_t kda_segment_transitions(const void* k, const void* v, const void* g,
+                                     const void* beta, float* M, float* S_tilde, int B, int H,
+                                     int T, int seg_len, int n_seg, int d_k, int d_v, int C,
+                                     kda_dtype_t dtype, void* stream);
+
+/*
+ * Incoming state of every segment from the segments' transitions (same references):
+ *   S_in[0] = S0 (zeros if S0 is NULL),  S_in[s + 1] = M[s] S_in[s] + S_tilde[s]
+ *   M [n_seg - 1, B, H, d_k, d_k], S_tilde [n_seg - 1, B, H, d_k, d_v] (both unused and
+ *   may be NULL when n_seg = 1), S0 [B, H, d_k, d_v] or NULL, S_in [n_seg, B, H, d_k, d_v]:
+ * all fp32 device arrays. fp32 arithmetic; the segments of one (b, h) are composed in order,
+ * different (b, h) and value columns in parallel. n_seg >= 1.
+ */
+kda_status_t kda_segment_scan(const float* M, const float* S_tilde, const float* S0, float* S_in,
+                              int n_seg, int B, int H, int d_k, int d_v, void* stream);
+
+/*
+ * Chunkwise prefill of a dense batch, parallel along T: the same contract and results (up to
+ * rounding) as kda_chunk_fwd, for batches with too few (sequence, head) problems to fill the
+ * GPU. T is cut into at most n_seg segments of whole 64-token blocks (seg_len =
+ * ceil(ceil(T / 64) / n_seg) * 64 tokens); the call runs kda_segment_transitions over every
+ * segment but the last, kda_segment_scan from S0, then every segment from its incoming state
+ * (outputs, and S_final from the last segment). With one segment it is kda_chunk_fwd.
+ *   workspace : caller-owned DEVICE scratch of at least
+ *               kda_chunk_fwd_segmented_workspace(B, H, T, d_k, d_v, n_seg) bytes, 16-byte
+ *               aligned; its contents on entry are ignored and on return unspecified. Two calls
+ *               in flight at the same time need distinct workspaces.
+ * Returns KDA_ERR_INVALID_ARG if the workspace is missing or too small.
+ */
+kda_status_t kda_chunk_fwd_segmented(const void* q, const void* k, const void* v, const void* g,
+                                     const void* beta, const float* S0, void* out,
+                                     float* S_final, int B, int H, int T, int d_k, int d_v, int C,
+                                     int n_seg, void* workspace, size_t workspace_bytes,
+                                     kda_dtype_t dtype, void* stream);
+
+/* Bytes of workspace kda_chunk_fwd_segmented needs (0 when it needs none or the sizes are
+ * invalid). Host-only; touches no device. */
+size_t kda_chunk_fwd_segmented_workspace(int B, int H, int T, int d_k, int d_v, int n_seg);
+
+/* A segment count for kda_chunk_fwd_segmented on the current device (1 when the (B, H)
+ * problems alone fill its SMs), from a cost model of the three passes in 64-token block times.
+ * Host-only apart from reading the device's SM count (148 if no device is visible). */
+int kda_segments_auto(int B, int H, int T);
+
+/*
+ * Waits for the work queued on `stream` so far, then takes and clears the device-side status
+ * word of the current device in one atomic exchange: returns the code latched there (KDA_OK if
+ * nothing was latched), or KDA_ERR_CUDA if the wait failed. The word is one per device and is
+ * shared by every stream: a code latched by a kernel on another stream is reported by whichever
+ * call takes the word first (it is never lost, but it may be reported on another stream), and a
+ * kernel still running on another stream may latch a code after this call returns.
+ */
 kda_status_t kda_sync_status(void* stream);
 
 /*

@@ -288,3 +288,41 @@ def test_prefill_then_decode_continues_the_sequence(kda):
     o_ref, S_ref = oracle_dense(inp)
     check(o_last.cpu().double().numpy(), o_ref[:, -1], "f32", "o_last")
     check(Sf.cpu().double().numpy(), S_ref, "f32", "S")
+
+
+# ------------------------------------------------------------------ streams and host buffers
+
+
+def test_nondefault_stream_matches_default(kda):
+    """A call on a side stream allocates and writes on that stream; its result is bit-identical
+    to the same call on the current stream, and both match the oracle."""
+    inp = kda_synth.make_prefill_inputs(2, 300, 4, 128, 128, "bf16", seed=77, S0_std=0.05)
+    x = to_dev(inp)
+    S0 = inp["S0"].to(DEV)
+    ref_out, ref_S = kda.chunk_fwd(*x, S0, C=64)
+    side = torch.cuda.Stream(device=DEV)
+    side.wait_stream(torch.cuda.current_stream(DEV))
+    out, Sf = kda.chunk_fwd(*x, S0, C=64, stream=side)
+    kda.kda_sync_status(side)
+    torch.cuda.current_stream(DEV).wait_stream(side)
+    assert torch.equal(out, ref_out) and torch.equal(Sf, ref_S)
+    o_ref, S_ref = oracle_dense(inp)
+    check(out.float().cpu().double().numpy(), o_ref, "bf16", "out")
+    check(Sf.cpu().double().numpy(), S_ref, "bf16", "S_final")
+
+
+def test_host_pipeline_matches_device_call(kda):
+    """chunk_fwd_host splits the batch by row over two streams; its host results equal the
+    device call's bits, including a caller stream that is not the current one."""
+    inp = kda_synth.make_prefill_inputs(5, 200, 3, 128, 128, "bf16", seed=78, S0_std=0.05)
+    hin = {n: inp[n].pin_memory() for n in ("q", "k", "v", "g", "beta")}
+    S0h = inp["S0"].pin_memory()
+    ref_out, ref_S = kda.chunk_fwd(*to_dev(inp), inp["S0"].to(DEV), C=64)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(device=DEV)
+    pl = kda.HostPipeline(DEV)
+    for _ in range(2):  # the pipeline's buffers are reused on the second call
+        oh, sh = kda.chunk_fwd_host(hin["q"], hin["k"], hin["v"], hin["g"], hin["beta"], S0h,
+                                    C=64, device=DEV, stream=side, pipeline=pl)
+        assert torch.equal(oh, ref_out.cpu()) and torch.equal(sh, ref_S.cpu())
+    kda.kda_sync_status(side)

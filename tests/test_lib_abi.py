@@ -99,3 +99,35 @@ def test_varlen_and_decode_reject_bad_arguments(lib):
     assert st == 2  # unsupported head size
     assert lib.kda_recurrent_step(None, None, None, None, None, None, None, 0, 2, 128, 128, 1,
                                   None) == 0  # N = 0 is a no-op
+
+
+def test_segmented_workspace_size_and_validation(lib):
+    # 4 segments of 64 tokens (T = 256), one (b, h): 3 x (M + S~) + 4 x S_in, 64 KiB each
+    assert lib.kda_chunk_fwd_segmented_workspace(1, 1, 256, 128, 128, 4) == 4 * 128 * 128 * (3 * 2 + 4)
+    assert lib.kda_chunk_fwd_segmented_workspace(2, 3, 256, 128, 128, 4) == 6 * 4 * 128 * 128 * 10
+    assert lib.kda_chunk_fwd_segmented_workspace(1, 1, 256, 128, 128, 1) == 0
+    # more segments than 64-token blocks: one segment per block
+    assert lib.kda_chunk_fwd_segmented_workspace(1, 1, 130, 128, 128, 8) == 4 * 128 * 128 * (2 * 2 + 3)
+    assert lib.kda_chunk_fwd_segmented_workspace(1, 1, 256, 128, 128, 0) == 0
+    # workspace missing / too small: rejected before anything is launched
+    a = [_fake()] * 5 + [None, _fake(), None]
+    assert lib.kda_chunk_fwd_segmented(*a, 1, 1, 256, 128, 128, 64, 4, None, 0, 1, None) == 1
+    assert lib.kda_chunk_fwd_segmented(*a, 1, 1, 256, 128, 128, 64, 4, _fake(), 100, 1, None) == 1
+    assert b"workspace" in lib.kda_last_error()
+    assert lib.kda_chunk_fwd_segmented(*a, 1, 1, 256, 128, 128, 64, 0, _fake(), 0, 1, None) == 1
+    # transitions and scan: host validation
+    assert lib.kda_segment_transitions(_fake(), _fake(), _fake(), _fake(), None, _fake(), 1, 1,
+                                       256, 64, 4, 128, 128, 64, 1, None) == 1
+    assert lib.kda_segment_transitions(_fake(), _fake(), _fake(), _fake(), _fake(), _fake(), 1, 1,
+                                       256, 0, 4, 128, 128, 64, 1, None) == 1
+    assert lib.kda_segment_scan(None, None, None, _fake(), 0, 1, 1, 128, 128, None) == 1
+    assert lib.kda_segment_scan(None, None, None, _fake(), 3, 1, 1, 128, 128, None) == 1
+
+
+def test_segments_auto_is_sane(lib):
+    # a batch that fills the SMs stays whole; few problems over long T are split
+    assert lib.kda_segments_auto(4, 96, 8192) == 1
+    assert lib.kda_segments_auto(1, 8, 4096) > 1
+    assert lib.kda_segments_auto(1, 1, 65536) > 8
+    assert lib.kda_segments_auto(1, 1, 64) == 1
+    assert lib.kda_segments_auto(0, 1, 64) == 1
