@@ -57,7 +57,6 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include <cstring>
 #include <string>
 
 #include "../../include/kda.h"
@@ -116,7 +115,7 @@ constexpr int Y_A = 64;
 constexpr int WLD = 72;
 constexpr int TLD = 20;  // row stride (floats) of the diagonal inverses
 struct TmaMaps {
-  CUtensorMap q, k, v, g, o;  // o: the output, for the stores of whole blocks (unused if out is null)
+  CUtensorMap q, k, v, g;
 };
 
 using namespace sm100;
@@ -158,9 +157,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   //          inverses T_RR (trr) and rounded the A blocks that S multiplies to tf32
   // bar_wsfree: S has read a block's A out of WS (P may put the next one there)
   // bar_khr: P has stored a block's Khat^T and read the previous block's O out of TMEM
-  // bar_D, bar_Z (Z^T), bar_ZO (Z^T and O^T), bar_G2, bar_G3: tcgen05 products complete
-  __shared__ uint64_t bar_in, bar_v, bar_prep, bar_ext, bar_wsfree, bar_khr, bar_D, bar_Z, bar_ZO,
-      bar_G2, bar_G3;
+  // bar_D, bar_ZO, bar_G2, bar_G3: tcgen05 products complete
+  __shared__ uint64_t bar_in, bar_v, bar_prep, bar_ext, bar_wsfree, bar_khr, bar_D, bar_ZO, bar_G2,
+      bar_G3;
   __shared__ uint32_t tmem_base_s;
   __shared__ __align__(16) float beta_s[2][C];  // by block parity
   __shared__ __align__(16) float gl_s[2][D];    // e^{Gamma_L} per key channel, by block parity
@@ -195,7 +194,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bar_wsfree, 1);
     mbar_init(&bar_khr, 1);
     mbar_init(&bar_D, 1);
-    mbar_init(&bar_Z, 1);
     mbar_init(&bar_ZO, 1);
     mbar_init(&bar_G2, 1);
     mbar_init(&bar_G3, 1);
@@ -257,12 +255,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     unsigned short beta_next = 0;
     if (lt < C && lt < len) beta_next = beta_u[(row0 + lt) * H + h];
     __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(P.out);
-    // O of block b: TMEM -> bf16 staged in XK (free: this group's A/P product of the block after b
-    // has completed, and the next operands are written after the bulk store has read it) as two
-    // 64-channel boxes of [64 tokens][128 B] in the 128-byte swizzle of the TMA map (16-byte chunk
-    // c of token row r at c ^ (r % 8), which also puts the eight rows of a matrix store in
-    // distinct banks); then, after a group barrier, one thread stores a whole block with two TMA
-    // stores, and a partial block is written with 16-byte stores of the rows that exist.
+    // O of block b: TMEM -> bf16 rows [token][128] staged in XK (free: this group's A/P product
+    // of the block after b has completed, and the next operands are written after the group's
+    // next barrier), then, after a group barrier, 16-byte global stores, each warp writing two
+    // whole 256-byte rows. The 16-byte chunks of a staged row are permuted by chunk ^ (token % 8)
+    // so that the eight rows of a matrix store fall in distinct banks.
     // Warp w reads lanes (value channels) 32 (w % 4) .. + 31, columns (tokens) 32 hh .. + 31 in the
     // 16 x 256 b shape, whose registers are the m16n8 fragment that a transposed matrix store
     // writes as [token][channel] rows.
@@ -280,42 +277,29 @@ __global__ void __launch_bounds__(THREADS, 1)
           // matrix i: channels cb + 8 (i & 1) .., tokens 32 hh + 8 (2u + (i >> 1)) ..
           const int li = lane >> 3, lj = lane & 7;
           const int tok = 32 * hh + 8 * (2 * u + (li >> 1)) + lj;
-          const int ch = (cb + 8 * (li & 1)) >> 3;  // 16-byte chunk of the 256-byte row
-          const uint32_t so = (uint32_t)((ch >> 3) * BOX_BYTES + tok * 128 + 16 * ((ch & 7) ^ (tok & 7)));
+          const int chunk = ((cb + 8 * (li & 1)) >> 3) ^ (tok & 7);
           const int k0 = 2 * u, k1 = 2 * u + 1;
-          stsm_x4_trans(stg_s + so,
+          stsm_x4_trans(stg_s + (uint32_t)(tok * 256 + 16 * chunk),
                         pack_bf16(__uint_as_float(v[4 * k0]), __uint_as_float(v[4 * k0 + 1])),
                         pack_bf16(__uint_as_float(v[4 * k0 + 2]), __uint_as_float(v[4 * k0 + 3])),
                         pack_bf16(__uint_as_float(v[4 * k1]), __uint_as_float(v[4 * k1 + 1])),
                         pack_bf16(__uint_as_float(v[4 * k1 + 2]), __uint_as_float(v[4 * k1 + 3])));
         }
       }
-      fence_proxy_async_smem();  // the TMA store reads the staged rows
       tc_fence_before();
     };
     // after a group barrier that follows stage_o(b)
-    bool pend_store = false;  // a bulk store of this group's thread 0 may still read XK
     auto store_o = [&](int b) {
       const int tb = b * C;
       const int nb = min(C, len - tb);
-      if (nb == C) {
-        if (lt == 0) {
-          const int row = (int)(row0 + (size_t)tb);
-          tma_store_3d(&maps.o, sm + XK, 0, h, row);
-          tma_store_3d(&maps.o, sm + XK + BOX_BYTES, 64, h, row);
-          bulk_commit();
-          pend_store = true;
-        }
-        return;
-      }
       const int q = lt & 15;  // 16-byte chunk of a row; rows lt / 16 + 16 i
       __nv_bfloat16* ob = out + ((row0 + tb + (lt >> 4)) * H + h) * D + 8 * q;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = (lt >> 4) + 16 * i;
         if (r < nb)
-          *reinterpret_cast<uint4*>(ob + (size_t)(16 * i) * H * D) = *reinterpret_cast<const uint4*>(
-              stg + (q >> 3) * BOX_BYTES + r * 128 + 16 * ((q & 7) ^ (r & 7)));
+          *reinterpret_cast<uint4*>(ob + (size_t)(16 * i) * H * D) =
+              *reinterpret_cast<const uint4*>(stg + r * 256 + 16 * (q ^ (r & 7)));
       }
     };
 
@@ -326,10 +310,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       // S has started the previous block (its first product read (K/Q e^Gamma)^T and the
       // per-parity arrays of two blocks ago are no longer read) and the previous A/P product
       // has released X and Y.
-      if (pend_store) {  // (thread 0 only) the previous block's bulk store has read XK
-        bulk_wait_read();
-        pend_store = false;
-      }
       if (blk > 0 && !group_wait2(&bar_ZO, (blk - 1) & 1, &bar_D, (blk - 1) & 1, BAR_P)) {
         aborted = true;
         break;
@@ -537,8 +517,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       fence_proxy_async_smem();  // P is a tensor-core operand of S's last product
       named_sync(BAR_P, GROUP);
       // ---------------- first step of the solve of T = (I + A)^{-1}, which needs A only: the
-      // 16 x 16 diagonal inverses T_RR (fp32, rounded to tf32 into trr), and the blocks of A that
-      // the warp MMAs of the later steps take as A operands rounded to tf32 in place
+      // 16 x 16 diagonal inverses T_RR (fp32, rounded to tf32 into trr; the state group reads trr
+      // from bar_ext until it releases WS), and the blocks of A that the state group uses as MMA
+      // A operands rounded to tf32 in place
       {
         float* ws = reinterpret_cast<float*>(sm + WS);
         if (lt >= GROUP - 64) {
@@ -575,40 +556,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       named_sync(BAR_P, GROUP);
-      // ---------------- second step: the off-diagonal 16 x 16 block of each 32-token half,
-      // T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22 (block-inverse identity), by warps
-      // 0-3 as tf32 warp MMAs; warps 4-7 copy the diagonal inverses into the diagonal blocks of
-      // WS, where A_RR is no longer read. Warp (h, n) of warps 0-3 (h = half, n = 8-column
-      // half) makes columns 8n .. 8n + 7 of Y = A_10 T_00 (into the scratch qs: rows 0..31,
-      // columns 32..63 of WS, where A is zero and T keeps nothing), then of T_10 = -T_11 Y.
-      {
-        float* ws = reinterpret_cast<float*>(sm + WS);
-        float* qs = ws + 32;
-        if (warp < 4) {
-          const int tile = warp >> 1, nh = warp & 1;
-          float* y = qs + 16 * tile + 8 * nh;
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          tile_mma(acc, ws + (16 + 32 * tile) * WLD + 32 * tile, WLD, &trr[2 * tile][0][8 * nh], TLD, 2);
-          float* yo = y + 2 * t;
-          yo[g * WLD] = tf32r(acc[0]);
-          yo[g * WLD + 1] = tf32r(acc[1]);
-          yo[(g + 8) * WLD] = tf32r(acc[2]);
-          yo[(g + 8) * WLD + 1] = tf32r(acc[3]);
-          __syncwarp();
-          float acc2[4] = {0.f, 0.f, 0.f, 0.f};
-          tile_mma(acc2, &trr[2 * tile + 1][0][0], TLD, y, WLD, 2);
-          float* o = ws + (16 + 32 * tile) * WLD + 32 * tile + 8 * nh + 2 * t;
-          o[g * WLD] = tf32r(-acc2[0]);
-          o[g * WLD + 1] = tf32r(-acc2[1]);
-          o[(g + 8) * WLD] = tf32r(-acc2[2]);
-          o[(g + 8) * WLD + 1] = tf32r(-acc2[3]);
-        } else {
-          for (int e = lt - 128; e < 1024; e += 128) {
-            const int R = e >> 8, i = (e >> 4) & 15, j = e & 15;
-            ws[(16 * R + i) * WLD + 16 * R + j] = trr[R][i][j];
-          }
-        }
-      }
       named_sync(BAR_P, GROUP);
       if (lt == 0) mbar_arrive(&bar_ext);
       // ---------------- once S's last product of the previous block is complete: Khat^T of this
@@ -632,10 +579,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (blk > 0 && write_out) store_o(blk - 1);
     }
     if (!aborted && nblocks > 0) {  // the last block's O
-      if (pend_store) {  // (thread 0 only) the previous block's bulk store has read XK
-        bulk_wait_read();
-        pend_store = false;
-      }
       if (group_wait2(&bar_G3, (nblocks - 1) & 1, nullptr, 0, BAR_P)) {
         tc_fence_after();
         if (write_out) {
@@ -648,7 +591,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     if (aborted) record_status(4u /* KDA_ERR_TIMEOUT */);
-    if (pend_store) bulk_wait_all();  // (thread 0) the output stores have completed
     if (lt == 0) {  // let anything already issued land before the CTA's memory goes away
       if (aborted && pend_in) (void)mbar_wait(&bar_in, in_blk & 1);
       if (d_blk >= 0) (void)mbar_wait(&bar_D, d_blk & 1);
@@ -712,21 +654,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_after();
       const uint32_t t_ot = t_ot_of(blk);  // this block's O^T columns
-      // ---------------- tcgen05: Z^T = S^T (K e^Gamma)^T, then O^T = S^T (Q e^Gamma)^T (N 64 each,
-      // K 128), committed separately so that Z^T can be converted while O^T is computed
+      // ---------------- tcgen05: [O^T | Z^T] (even) or [Z^T | O^T] (odd) =
+      // S^T [(Q e^Gamma)^T | (K e^Gamma)^T] (or the other order) (N 128, K 128)
       if (leader) {
         tc_fence_after();
-        const uint32_t id_h = idesc_bf16(128, 64, 0, 1, 0);
-        const uint32_t kg = sb + KQ + (par ? 0u : 16384u), qg = sb + KQ + (par ? 16384u : 0u);
+        const uint32_t id_zo = idesc_bf16(128, 128, 0, 1, 0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_tmem_a(tmem + T_ZT, tmem + T_SB + 8u * kk, desc_sw128(kg + 2048u * kk, 16384, 1024),
-                           id_h, kk > 0);
-        umma_commit(&bar_Z);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_tmem_a(tmem + t_ot, tmem + T_SB + 8u * kk, desc_sw128(qg + 2048u * kk, 16384, 1024),
-                           id_h, kk > 0);
+          umma_bf16_tmem_a(tmem + (par ? T_ZT : t_ot), tmem + T_SB + 8u * kk,
+                           desc_sw128(sb + KQ + 2048u * kk, 16384, 1024), id_zo, kk > 0);
         umma_commit(&bar_ZO);
       }
       pend_mma = true; last_mma = &bar_ZO; last_par = ph;
@@ -759,7 +695,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       // ---------------- Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand; then wait for group P
       // to have written A, P and the diagonal inverses of this block (bar_ext)
-      if (!group_wait2(&bar_Z, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
+      if (!group_wait2(&bar_ZO, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
+      pend_mma = false;
       tc_fence_after();
       {
         uint32_t v[32], zb[16];
@@ -771,13 +708,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!group_wait2(&bar_ext, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       // ---------------- T = (I + A)^{-1} (unit lower triangular) and G = T Diag(beta) (bf16)
-      // Group P has placed the diagonal inverses T_RR and the off-diagonal blocks T_10, T_32 of
-      // each 32-token half in WS. The block-inverse identity
-      // [[P, 0], [C, Q]]^{-1} = [[P^{-1}, 0], [-Q^{-1} C P^{-1}, Q^{-1}]] for the two halves gives
-      // the off-diagonal 32 x 32 block T_(32)10 = -T_(32)11 A_(32)10 T_(32)00 (tf32 warp MMAs).
+      // From the 16 x 16 diagonal inverses T_RR (group P, in trr) and the block-inverse identity
+      // [[P, 0], [C, Q]]^{-1} = [[P^{-1}, 0], [-Q^{-1} C P^{-1}, Q^{-1}]]: the off-diagonal
+      // 16 x 16 block of each 32 x 32 half and then the off-diagonal 32 x 32 block, as tf32 warp
+      // MMAs on fp32 blocks in WS (T overwrites A where A is no longer read).
       {
         float* ws = reinterpret_cast<float*>(sm + WS);
-        float* qs = ws + 32;  // scratch: rows 0..31, columns 32..63 of WS
+        // scratch: rows 0..31, columns 32..63 of WS, where A is zero and no block of T is kept
+        float* qs = ws + 32;
         const int sw = warp - GROUP / 32;  // warp index inside the group
         const float* bt = beta_s[par];
         // two adjacent entries of G = T Diag(beta): row r, columns j and j + 1 (j even)
@@ -785,38 +723,64 @@ __global__ void __launch_bounds__(THREADS, 1)
           *reinterpret_cast<uint32_t*>(sm + GB + sw128_off((uint32_t)r, (uint32_t)j)) =
               pack_bf16(x0 * bt[j], x1 * bt[j + 1]);
         };
-        // warp (n, m), n = sw & 3, m = sw >> 2: tile (m, n) of Q = A_(32)10 T_(32)00 (rows
-        // 32 + 16 m .., columns 8 n .., K 32; into qs); the two warps of column block n meet at
-        // their own barrier; then tile (m, n) of G rows 32..63: T_(32)10 = -T_(32)11 Q. Every
-        // thread also writes three pairs of G from the blocks group P placed in WS.
-        const int nt = sw & 3, mt = sw >> 2;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mma(acc, ws + (32 + 16 * mt) * WLD, WLD, ws + 8 * nt, WLD, 4);
-        float* o = qs + 16 * mt * WLD + 8 * nt + 2 * t;
-        o[g * WLD] = tf32r(acc[0]);
-        o[g * WLD + 1] = tf32r(acc[1]);
-        o[(g + 8) * WLD] = tf32r(acc[2]);
-        o[(g + 8) * WLD + 1] = tf32r(acc[3]);
-#pragma unroll
-        for (int e = lt; e < 768; e += GROUP) {
-          int r, j;
-          if (e < 512) {  // diagonal blocks
-            const int R = e >> 7, i = (e >> 3) & 15, jp = 2 * (e & 7);
-            r = 16 * R + i;
-            j = 16 * R + jp;
-          } else {  // T_10 and T_32
-            const int e2 = e - 512, tile = e2 >> 7, i = (e2 >> 3) & 15, jp = 2 * (e2 & 7);
-            r = 16 + 32 * tile + i;
-            j = 32 * tile + jp;
+        // (2) warp (h, n) of warps 0-3, h = 32-row half, n = 8-column half: columns 8n .. 8n + 7
+        //     of Y = A_10 T_00 (into qs), then of T_10 = -T_11 Y (into WS), which need no other
+        //     columns of Y (h = 1: A_32, T_22, T_33, T_32); warps 4-7: the T_RR into the diagonal
+        //     blocks of WS, where A_RR is no longer read, and G of the diagonal blocks
+        if (sw < 4) {
+          const int tile = sw >> 1, nh = sw & 1;
+          float* y = qs + 16 * tile + 8 * nh;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma(acc, ws + (16 + 32 * tile) * WLD + 32 * tile, WLD, &trr[2 * tile][0][8 * nh], TLD, 2);
+          float* yo = y + 2 * t;
+          yo[g * WLD] = tf32r(acc[0]);
+          yo[g * WLD + 1] = tf32r(acc[1]);
+          yo[(g + 8) * WLD] = tf32r(acc[2]);
+          yo[(g + 8) * WLD + 1] = tf32r(acc[3]);
+          __syncwarp();
+          float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma(acc2, &trr[2 * tile + 1][0][0], TLD, y, WLD, 2);
+          float* o = ws + (16 + 32 * tile) * WLD + 32 * tile + 8 * nh + 2 * t;
+          o[g * WLD] = tf32r(-acc2[0]);
+          o[g * WLD + 1] = tf32r(-acc2[1]);
+          o[(g + 8) * WLD] = tf32r(-acc2[2]);
+          o[(g + 8) * WLD + 1] = tf32r(-acc2[3]);
+        } else {
+          for (int e = lt - 128; e < 1024; e += 128) {
+            const int R = e >> 8, i = (e >> 4) & 15, j = e & 15;
+            ws[(16 * R + i) * WLD + 16 * R + j] = trr[R][i][j];
           }
-          g_store(r, j, ws[r * WLD + j], ws[r * WLD + j + 1]);
+          for (int e = lt - 128; e < 512; e += 128) {
+            const int R = e >> 7, i = (e >> 3) & 15, jp = 2 * (e & 7);
+            g_store(16 * R + i, 16 * R + jp, trr[R][i][jp], trr[R][i][jp + 1]);
+          }
         }
-        named_sync(BAR_PAIR0 + nt, 64);
-        float acc2[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mma(acc2, ws + (32 + 16 * mt) * WLD + 32, WLD, qs + 8 * nt, WLD, 4);
-        const int r = 32 + 16 * mt + g, j = 8 * nt + 2 * t;
-        g_store(r, j, -acc2[0], -acc2[1]);
-        g_store(r + 8, j, -acc2[2], -acc2[3]);
+        named_sync(BAR_S, GROUP);
+        // (3) warp (n, m), n = sw & 3, m = sw >> 2: tile (m, n) of Q = A_(32)10 T_(32)00 (rows
+        //     32 + 16 m .., columns 8 n .., K 32; into qs); the two warps of column block n meet
+        //     at their own barrier; then tile (m, n) of G rows 32..63: T_(32)10 = -T_(32)11 Q.
+        //     Every thread also writes one pair of G of T_10 and T_32.
+        {
+          const int nt = sw & 3, mt = sw >> 2;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma(acc, ws + (32 + 16 * mt) * WLD, WLD, ws + 8 * nt, WLD, 4);
+          float* o = qs + 16 * mt * WLD + 8 * nt + 2 * t;
+          o[g * WLD] = tf32r(acc[0]);
+          o[g * WLD + 1] = tf32r(acc[1]);
+          o[(g + 8) * WLD] = tf32r(acc[2]);
+          o[(g + 8) * WLD + 1] = tf32r(acc[3]);
+          {
+            const int tile = lt >> 7, i = (lt >> 3) & 15, jp = 2 * (lt & 7);
+            const int r = 16 + 32 * tile + i, j = 32 * tile + jp;
+            g_store(r, j, ws[r * WLD + j], ws[r * WLD + j + 1]);
+          }
+          named_sync(BAR_PAIR0 + nt, 64);
+          float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma(acc2, ws + (32 + 16 * mt) * WLD + 32, WLD, qs + 8 * nt, WLD, 4);
+          const int r = 32 + 16 * mt + g, j = 8 * nt + 2 * t;
+          g_store(r, j, -acc2[0], -acc2[1]);
+          g_store(r + 8, j, -acc2[2], -acc2[3]);
+        }
       }
       fence_proxy_async_smem();  // G is a tensor-core operand
       tmem_st_wait();
@@ -945,10 +909,6 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 inline bool encode_token_map(CUtensorMap* m, const void* base, long long rows, int H) {
   auto fn = encode_fn();
   if (!fn) return false;
-  if (base == nullptr) {  // an unused map (no output): keep it zero
-    memset(m, 0, sizeof(*m));
-    return true;
-  }
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
   cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
@@ -968,8 +928,7 @@ inline kda_status_t launch_chunk_tc(const SeqParams& P, int n_problems, int C, c
   tc::TmaMaps maps;
   const long long rows = P.cu_seqlens ? (long long)P.T : (long long)P.n_seq * P.T;
   if (!tc::encode_token_map(&maps.q, P.q, rows, P.H) || !tc::encode_token_map(&maps.k, P.k, rows, P.H) ||
-      !tc::encode_token_map(&maps.v, P.v, rows, P.H) || !tc::encode_token_map(&maps.g, P.g, rows, P.H) ||
-      !tc::encode_token_map(&maps.o, P.out, rows, P.H)) {
+      !tc::encode_token_map(&maps.v, P.v, rows, P.H) || !tc::encode_token_map(&maps.g, P.g, rows, P.H)) {
     err = "cuTensorMapEncodeTiled failed";
     return KDA_ERR_CUDA;
   }

@@ -394,31 +394,6 @@ __device__ __forceinline__ void stsm_x4(uint32_t saddr, uint32_t r0, uint32_t r1
                : "memory");
 }
 
-// 3-D tiled TMA store from shared memory to global; completion is tracked with bulk groups of
-// the issuing thread.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1,
-                                             int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Waits until every committed bulk store of this thread has finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// Waits until every committed bulk store of this thread has completed.
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // Byte offset of element (row, col) inside a 128-byte-swizzled panel of 64 bf16 per row
 // (rows stacked every 128 bytes, 8-row atoms of 1024 bytes): the 16-byte chunk index is
 // XOR-ed with the row index modulo 8.
