@@ -23,6 +23,7 @@ __all__ = [
     "load_library", "chunk_fwd", "chunk_fwd_varlen", "recurrent_step", "chunk_fwd_host",
     "HostPipeline", "kda_segment_transitions", "kda_segment_scan", "kda_chunk_fwd_segmented",
     "chunk_fwd_segmented", "segmented_workspace_bytes", "segments_auto",
+    "kda_chunk_fwd_segmented_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -36,8 +37,11 @@ EXPORTED_SYMBOLS = (
     "kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_recurrent_step", "kda_sync_status",
     "kda_wait_selftest", "kda_status_string", "kda_last_error", "kda_version",
     "kda_segment_transitions", "kda_segment_scan", "kda_chunk_fwd_segmented",
-    "kda_chunk_fwd_segmented_workspace", "kda_segments_auto",
+    "kda_chunk_fwd_segmented_workspace", "kda_segments_auto", "kda_chunk_fwd_segmented_noalloc",
 )
+
+# Bytes of the fixed device scratch behind kda_chunk_fwd_segmented_noalloc (include/kda.h).
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class KdaError(RuntimeError):
@@ -86,6 +90,8 @@ def load_library(path: str | None = None):
     lib.kda_chunk_fwd_segmented_workspace.restype = Z
     lib.kda_segments_auto.argtypes = [I] * 3
     lib.kda_segments_auto.restype = I
+    lib.kda_chunk_fwd_segmented_noalloc.argtypes = [V] * 8 + [I] * 7 + [I, V]
+    lib.kda_chunk_fwd_segmented_noalloc.restype = S
     lib.kda_sync_status.argtypes = [V]
     lib.kda_wait_selftest.argtypes = [ctypes.c_ulonglong, V]
     lib.kda_wait_selftest.restype = S
@@ -263,6 +269,30 @@ def kda_chunk_fwd_segmented(q, k, v, g, beta, S0, out, S_final, n_seg: int, work
                                      int(n_seg), _ptr(workspace), nbytes, _dtype_code(q),
                                      _stream_handle(stream))
     _check(st, "kda_chunk_fwd_segmented")
+
+
+def kda_chunk_fwd_segmented_noalloc(q, k, v, g, beta, S0, out, S_final, n_seg: int,
+                                    C: int = 64, stream=None):
+    """:func:`kda_chunk_fwd_segmented` without a workspace: the library's fixed device scratch
+    (``NOALLOC_SCRATCH_BYTES``) serves instead, and nothing is allocated. For callers that cannot
+    allocate device memory at the point of the call; calls that overlap on the GPU share that
+    scratch and must be ordered on one stream (see include/kda.h)."""
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    _check_tensors([("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out)],
+                   q.dtype, q.device)
+    _check_tensors([("S0", S0), ("S_final", S_final)], torch.float32, q.device)
+    _require(k.shape == q.shape and g.shape == q.shape, "q, k, g must share [B, T, H, d_k]")
+    _require(v.shape == (B, T, H, dv) and out.shape == v.shape, "v/out must be [B, T, H, d_v]")
+    _require(beta.shape == (B, T, H), "beta must be [B, T, H]")
+    for name, s in (("S0", S0), ("S_final", S_final)):
+        _require(s is None or s.shape == (B, H, dk, dv), f"{name} must be [B, H, d_k, d_v]")
+    st = lib.kda_chunk_fwd_segmented_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                             _ptr(S0), _ptr(out), _ptr(S_final), B, H, T, dk, dv,
+                                             int(C), int(n_seg), _dtype_code(q),
+                                             _stream_handle(stream))
+    _check(st, "kda_chunk_fwd_segmented_noalloc")
 
 
 def kda_sync_status(stream=None):

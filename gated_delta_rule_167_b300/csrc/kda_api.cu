@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "../../include/kda.h"
@@ -330,6 +331,67 @@ kda_status_t kda_chunk_fwd_segmented(const void* q, const void* k, const void* v
   P2.n_seg = segs;
   P2.sf_last_only = 1;
   return run_chunk(P2, (int)(segs * BH), d_k, C, dtype, st);
+}
+
+}  // extern "C"
+
+// Scratch of kda_chunk_fwd_segmented_noalloc: a fixed array in the library's device image, so
+// that the call needs no allocation. Every device that loads the library holds it until the
+// process exits. In host code the name stands for a host-side shadow, not a device address; the
+// device address comes from cudaGetSymbolAddress, once per device, in noalloc_scratch().
+static __device__ __align__(256) unsigned char kda_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the static scratch on the current device (looked up on the first call there).
+kda_status_t noalloc_scratch(void** addr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(KDA_ERR_UNSUPPORTED, "device ordinal %d is beyond the %d devices tracked", dev,
+                kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, kda_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(kda_noalloc_scratch)");
+    g_noalloc_addr[dev] = p;
+  }
+  *addr = g_noalloc_addr[dev];
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const void* v,
+                                             const void* g, const void* beta, const float* S0,
+                                             void* out, float* S_final, int B, int H, int T,
+                                             int d_k, int d_v, int C, int n_seg,
+                                             kda_dtype_t dtype, void* stream) {
+  t_last_error.clear();
+  if (n_seg < 1) return fail(KDA_ERR_INVALID_ARG, "n_seg must be >= 1 (got %d)", n_seg);
+  const size_t need = kda_chunk_fwd_segmented_workspace(B, H, T, d_k, d_v, n_seg);
+  if (need > (size_t)KDA_NOALLOC_SCRATCH_BYTES)
+    return fail(KDA_ERR_UNSUPPORTED,
+                "this request needs %zu bytes of scratch; the library's fixed scratch holds %zu "
+                "(use fewer segments, or kda_chunk_fwd_segmented with a caller workspace)",
+                need, (size_t)KDA_NOALLOC_SCRATCH_BYTES);
+  void* ws = nullptr;
+  if (need > 0) {
+    kda_status_t s = noalloc_scratch(&ws);
+    if (s != KDA_OK) return s;
+  }
+  // The segmented path writes every byte of scratch it reads (transitions, then the scan), so
+  // nothing in the array has to start at zero.
+  return kda_chunk_fwd_segmented(q, k, v, g, beta, S0, out, S_final, B, H, T, d_k, d_v, C, n_seg,
+                                 ws, need, dtype, stream);
 }
 
 int kda_segments_auto(int B, int H, int T) {

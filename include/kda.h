@@ -152,6 +152,35 @@ size_t kda_chunk_fwd_segmented_workspace(int B, int H, int T, int d_k, int d_v, 
  * Host-only apart from reading the device's SM count (148 if no device is visible). */
 int kda_segments_auto(int B, int H, int T);
 
+/* Bytes of the fixed device scratch behind kda_chunk_fwd_segmented_noalloc (32 MiB). */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * kda_chunk_fwd_segmented without a caller workspace and without any allocation. The pages have
+ * no counterpart to this entry point; it exists for callers that cannot allocate device memory
+ * at the point of the call: runtimes whose device memory is all owned by a fixed arena or pool,
+ * plug-ins whose host hands them tensors but no allocator, and loops that cannot afford the
+ * synchronisation and unpredictable latency of cudaMalloc / cudaFree.
+ *
+ * Same arguments, results and errors as kda_chunk_fwd_segmented, minus the workspace. The scratch
+ * is one array of KDA_NOALLOC_SCRATCH_BYTES in the library's device image, held on every device
+ * that loads the library until the process exits. A request whose scratch
+ * (kda_chunk_fwd_segmented_workspace(B, H, T, d_k, d_v, n_seg)) exceeds that size is rejected with
+ * KDA_ERR_UNSUPPORTED before anything is launched. The call makes no cudaMalloc, cudaFree or
+ * other allocating call.
+ *  - The first call on a device looks up the array's device address there (cudaGetSymbolAddress,
+ *    with that device current); make that first call before any stream capture on the device.
+ *  - All calls on a device share the one array, and it keeps the contents of the last call.
+ *    Every byte a call reads from it is written earlier in the same call, so nothing needs
+ *    clearing, but calls whose work overlaps on the GPU (different streams, or host threads
+ *    without ordering) race on the array and give wrong results: order them on one stream.
+ */
+kda_status_t kda_chunk_fwd_segmented_noalloc(const void* q, const void* k, const void* v,
+                                             const void* g, const void* beta, const float* S0,
+                                             void* out, float* S_final, int B, int H, int T,
+                                             int d_k, int d_v, int C, int n_seg,
+                                             kda_dtype_t dtype, void* stream);
+
 /*
  * Waits for the work queued on `stream` so far, then takes and clears the device-side status
  * word of the current device in one atomic exchange: returns the code latched there (KDA_OK if

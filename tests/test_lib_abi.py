@@ -131,3 +131,12 @@ def test_segments_auto_is_sane(lib):
     assert lib.kda_segments_auto(1, 1, 65536) > 8
     assert lib.kda_segments_auto(1, 1, 64) == 1
     assert lib.kda_segments_auto(0, 1, 64) == 1
+
+
+def test_noalloc_entry_point_refuses_oversized_requests_on_the_host(lib):
+    # 96 heads x 8192 tokens in 8 segments needs ~138 MB of scratch, beyond the fixed 32 MiB:
+    # refused before the device is touched
+    a = [_fake()] * 5 + [None, _fake(), None]
+    assert lib.kda_chunk_fwd_segmented_noalloc(*a, 1, 96, 8192, 128, 128, 64, 8, 1, None) == 2
+    assert b"scratch" in lib.kda_last_error()
+    assert lib.kda_chunk_fwd_segmented_noalloc(*a, 1, 96, 8192, 128, 128, 64, 0, 1, None) == 1
