@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bar_D, 1);
     mbar_init(&bar_ZO, 1);
     mbar_init(&bar_G2, 1);
-    mbar_init(&bar_G3, 1);
+    mbar_init(&bar_G3, 2);  // the two issuers of the last product commit to it
     fence_mbar_init();
     prefetch_tensormap(&maps.q);
     prefetch_tensormap(&maps.k);
@@ -785,9 +785,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       fence_proxy_async_smem();  // G is a tensor-core operand
       tmem_st_wait();
       tc_fence_before();
+      // every thread of the group is done with WS (the v wait's group barrier, else a plain one)
       if (!vzero) {
         if (!group_wait2(&bar_v, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
         pend_v = false;
+      } else {
+        named_sync(BAR_S, GROUP);
       }
       if (leader) mbar_arrive(&bar_wsfree);  // WS is no longer read
       // ---------------- tcgen05: U^T = V^T G^T - Z^T G^T (M 128, N 64, K 64), which is
@@ -827,19 +830,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         v_blk = blk + 1;
       }
       // ---------------- tcgen05: O^T += U^T P^T (N 64) ; S^T += U^T Khat (N 128), K 64; P has
-      // stored this block's Khat^T by bar_khr
+      // stored this block's Khat^T by bar_khr. The two products have their own accumulators, so
+      // two threads in different warps issue them at the same time (a thread issues one MMA about
+      // every 120 cycles, whatever its size); both commit to bar_G3.
       if (!group_wait2(&bar_khr, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       if (leader) {
         tc_fence_after();
-        const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
         const uint32_t id_s = idesc_bf16(128, 128, 0, 0, 0);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          umma_bf16_tmem_a(tmem + t_ot, tmem + T_UB + 8u * kk,
-                           desc_sw128(sb + PT + 8192u * (uint32_t)par + 32u * kk, 16, 1024), id_o, 1);
+        for (int kk = 0; kk < 4; ++kk)
           umma_bf16_tmem_a(tmem + T_ST, tmem + T_UB + 8u * kk,
                            desc_sw128(sb + KH + 32u * kk, 16, 1024), id_s, 1);
-        }
+        umma_commit(&bar_G3);
+      } else if (lt == 128) {
+        tc_fence_after();
+        const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_tmem_a(tmem + t_ot, tmem + T_UB + 8u * kk,
+                           desc_sw128(sb + PT + 8192u * (uint32_t)par + 32u * kk, 16, 1024), id_o, 1);
         umma_commit(&bar_G3);
       }
       pend_mma = true; last_mma = &bar_G3; last_par = ph;
