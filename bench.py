@@ -57,7 +57,8 @@ def _peaks():
 
 # The sources each timed kernel is compiled from (its DRAM counters stay valid while these are
 # unchanged).
-PREFILL_SOURCES = ("kda_chunk_tc.cuh", "kda_chunk_simt.cuh", "kda_sm100.cuh", "kda_common.cuh")
+PREFILL_SOURCES = ("kda_chunk_tc.cuh", "kda_chunk_simt.cuh", "kda_sm100.cuh", "kda_common.cuh",
+                   "kda_pre.cuh", "kda_post.cuh")
 DECODE_SOURCES = ("kda_decode.cuh", "kda_common.cuh")
 
 
@@ -504,6 +505,112 @@ def bench_varlen(kda, args, world, rank, device, stream, peaks, steps=3):
                          "algorithmic_bytes_per_launch": alg}}
 
 
+def bench_layer_sides(kda, args, world, rank, device, stream, peaks, steps=5):
+    """The layers around the core at the B=4, H=96, T=8192 shape: the output side (RMSNorm of the
+    raw output times the sigmoid gate) fused into the prefill's epilogue vs the plain prefill
+    plus the standalone gate pass; the input side (ShortConv, L2Norm, decay gate) fused into the
+    prefill vs the standalone input pass plus the plain prefill."""
+    w = kda_synth.WORKLOADS[2]
+    B, T, H, C = w["B"], w["T"], w["H"], w["C"]
+    inp = kda_synth.make_prefill_inputs(B, T, H, D, D, "bf16", seed=w["seed"] + rank,
+                                        g_bias=True, device=device)
+    x = [inp[n] for n in ("q", "k", "v", "g", "beta")]
+    gen = torch.Generator(device=device).manual_seed(1234 + rank)
+    u = torch.randn(B, T, H, D, generator=gen, device=device).to(torch.bfloat16)
+    nw = 1.0 + 0.1 * torch.randn(D, generator=gen, device=device)
+    conv = [0.5 * torch.randn(H, 4, D, generator=gen, device=device) for _ in range(3)]
+    A_log = 0.1 * torch.randn(H, generator=gen, device=device)
+    b_dec = torch.rand(H, D, generator=gen, device=device) * 4 - 2
+    out = torch.empty(B, T, H, D, dtype=torch.bfloat16, device=device)
+    Sf = torch.empty(B, H, D, D, dtype=torch.float32, device=device)
+    qkvg = [torch.empty_like(x[0]) for _ in range(4)]
+    prm = conv + [A_log, b_dec]
+
+    def t(fn):
+        ms, _ = _timed(fn, steps, 2, world, device, stream)
+        return ms / steps
+
+    core = t(lambda: kda.kda_chunk_fwd(*x, None, out, Sf, C=C, stream=stream))
+    gated = t(lambda: kda.kda_chunk_fwd_gated(*x, None, u, nw, out, Sf, C=C, stream=stream))
+    gate_alone = t(lambda: kda.kda_output_gate(out, u, nw, out, stream=stream))
+    pre_alone = t(lambda: kda.kda_pre_core(x[0], x[1], x[2], x[3], *prm, *qkvg, stream=stream))
+    fused_in = t(lambda: kda.kda_chunk_fwd_fused(x[0], x[1], x[2], x[3], x[4], *prm, None, out, Sf,
+                                                 C=C, stream=stream))
+    fused_both = t(lambda: kda.kda_chunk_fwd_fused(x[0], x[1], x[2], x[3], x[4], *prm, None, out,
+                                                   Sf, gate_u=u, norm_w=nw, C=C, stream=stream))
+    kda.kda_sync_status(stream)
+    th = B * T * H
+    gate_bytes = th * D * 2 * 3  # o~ and u in, y out
+    pre_bytes = th * D * 2 * 8   # q~, k~, v~, z in; q, k, v, g out
+    del inp, x, u, out, qkvg, conv
+    torch.cuda.empty_cache()
+    return {"workload": w["name"], "ms_core": core,
+            "output_side": {"ms_fused_in_epilogue": gated, "ms_core_plus_standalone_gate": core + gate_alone,
+                            "ms_standalone_gate": gate_alone,
+                            "standalone_gate_gbs": gate_bytes / (gate_alone * 1e-3) / 1e9},
+            "input_side": {"ms_fused_in_prefill": fused_in,
+                           "ms_standalone_pass_plus_core": pre_alone + core,
+                           "ms_standalone_pass": pre_alone,
+                           "standalone_pass_gbs": pre_bytes / (pre_alone * 1e-3) / 1e9},
+            "ms_fused_both_sides": fused_both,
+            "tokens_per_s_fused_both_sides": world * B * T / (fused_both * 1e-3)}
+
+
+def bench_decode_tokens(kda, args, world, rank, device, stream, peaks, K=4, calls=16):
+    """K = 4 decode tokens per (sequence, head) per call for the 256 x 96 state: the state
+    crosses HBM once per call whatever K is."""
+    w = kda_synth.WORKLOADS[4]
+    N, H = w["N"], w["H"]
+    dec = kda_synth.make_decode_inputs(N, H, D, D, "bf16", seed=w["seed"] + rank,
+                                       S0_std=w["S0_std"], steps=K, device=device)
+    stack = [torch.stack([st[n] for st in dec["steps"]], dim=1).contiguous()
+             for n in ("q", "k", "v", "g", "beta")]
+    S = dec["S"]
+    out = torch.empty(N, K, H, D, dtype=torch.bfloat16, device=device)
+
+    def run():
+        for _ in range(calls):
+            kda.kda_recurrent_steps(*stack, S, out, stream=stream)
+
+    total_ms, clocks = _timed(run, 1, 1, world, device, stream)
+    kda.kda_sync_status(stream)
+    ms = total_ms / calls
+    bytes_call = N * H * (2 * D * D * 4 + K * ((3 * D + D) * 2 + 2 + D * 2))
+    gbs = bytes_call / (ms * 1e-3) / 1e9
+    del dec, stack, S, out
+    torch.cuda.empty_cache()
+    return {"workload": f"decode_bf16_N{N}_H{H}_K{K}", "K": K, "ms_per_call": ms,
+            "tokens_per_s": world * N * K / (ms * 1e-3), "clocks": clocks,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm"], "traffic": None,
+                         "algorithmic_bytes_per_launch": bytes_call}}
+
+
+def bench_nano(kda, args, world, rank, device, stream, peaks, steps=5):
+    """The nano-K3 head shape (8 heads x 64 channels, context 2048), 64 sequences, bf16: the
+    d = 64 path (CUDA cores)."""
+    B, T, H, d, C = 64, 2048, 8, 64, 64
+    inp = kda_synth.make_prefill_inputs(B, T, H, d, d, "bf16", seed=rank, device=device)
+    x = [inp[n] for n in ("q", "k", "v", "g", "beta")]
+    out = torch.empty(B, T, H, d, dtype=torch.bfloat16, device=device)
+    Sf = torch.empty(B, H, d, d, dtype=torch.float32, device=device)
+    total_ms, clocks = _timed(lambda: kda.kda_chunk_fwd(*x, None, out, Sf, C=C, stream=stream),
+                              steps, 2, world, device, stream)
+    kda.kda_sync_status(stream)
+    ms = total_ms / steps
+    alg = B * T * H * (3 * d * 2 + d * 2 + 2 + d * 2) + B * H * d * d * 4
+    gbs = alg / (ms * 1e-3) / 1e9
+    del inp, x, out
+    torch.cuda.empty_cache()
+    return {"workload": f"kda_bf16_B{B}_H{H}_T{T}_d{d}_C{C}", "ms_per_step": ms,
+            "tokens_per_s": world * B * T / (ms * 1e-3),
+            "tflops": B * T * H * useful_flops_per_token_head(C, d, d) / (ms * 1e-3) / 1e12,
+            "clocks": clocks,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm"], "traffic": None,
+                         "algorithmic_bytes_per_launch": alg}}
+
+
 def cpu_baseline_varlen(budget_s=8.0):
     """The oracle on a bounded sample of the packed workload: whole (sequence, head) problems of
     the shortest sequences, timed on all host cores; tokens = token-heads / H."""
@@ -562,6 +669,9 @@ def run_gpu(args):
         secondary["small"] = bench_small(kda, args, world, rank, device, stream, peaks)
         secondary["decode"] = bench_decode(kda, args, world, rank, device, stream, peaks)
         secondary["varlen"] = bench_varlen(kda, args, world, rank, device, stream, peaks)
+        secondary["decode_tokens"] = bench_decode_tokens(kda, args, world, rank, device, stream, peaks)
+        secondary["layer_sides"] = bench_layer_sides(kda, args, world, rank, device, stream, peaks)
+        secondary["nano_d64"] = bench_nano(kda, args, world, rank, device, stream, peaks)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -23,7 +23,8 @@ __all__ = [
     "load_library", "chunk_fwd", "chunk_fwd_varlen", "recurrent_step", "chunk_fwd_host",
     "HostPipeline", "kda_segment_transitions", "kda_segment_scan", "kda_chunk_fwd_segmented",
     "chunk_fwd_segmented", "segmented_workspace_bytes", "segments_auto",
-    "kda_chunk_fwd_segmented_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "kda_chunk_fwd_segmented_noalloc", "NOALLOC_SCRATCH_BYTES", "kda_chunk_fwd_gated",
+    "kda_output_gate", "kda_pre_core", "kda_chunk_fwd_fused", "kda_recurrent_steps",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -38,6 +39,8 @@ EXPORTED_SYMBOLS = (
     "kda_wait_selftest", "kda_status_string", "kda_last_error", "kda_version",
     "kda_segment_transitions", "kda_segment_scan", "kda_chunk_fwd_segmented",
     "kda_chunk_fwd_segmented_workspace", "kda_segments_auto", "kda_chunk_fwd_segmented_noalloc",
+    "kda_chunk_fwd_gated", "kda_output_gate", "kda_pre_core", "kda_chunk_fwd_fused",
+    "kda_recurrent_steps",
 )
 
 # Bytes of the fixed device scratch behind kda_chunk_fwd_segmented_noalloc (include/kda.h).
@@ -92,6 +95,17 @@ def load_library(path: str | None = None):
     lib.kda_segments_auto.restype = I
     lib.kda_chunk_fwd_segmented_noalloc.argtypes = [V] * 8 + [I] * 7 + [I, V]
     lib.kda_chunk_fwd_segmented_noalloc.restype = S
+    F = ctypes.c_float
+    lib.kda_chunk_fwd_gated.argtypes = [V] * 8 + [F, V, V, V] + [I] * 6 + [I, V]
+    lib.kda_chunk_fwd_gated.restype = S
+    lib.kda_output_gate.argtypes = [V, V, V, F, V, ctypes.c_longlong, I, I, V]
+    lib.kda_output_gate.restype = S
+    lib.kda_pre_core.argtypes = [V] * 14 + [I] * 4 + [I, V]
+    lib.kda_pre_core.restype = S
+    lib.kda_chunk_fwd_fused.argtypes = [V] * 13 + [F, V, V, V] + [I] * 6 + [I, V]
+    lib.kda_chunk_fwd_fused.restype = S
+    lib.kda_recurrent_steps.argtypes = [V] * 7 + [I] * 5 + [I, V]
+    lib.kda_recurrent_steps.restype = S
     lib.kda_sync_status.argtypes = [V]
     lib.kda_wait_selftest.argtypes = [ctypes.c_ulonglong, V]
     lib.kda_wait_selftest.restype = S
@@ -293,6 +307,129 @@ def kda_chunk_fwd_segmented_noalloc(q, k, v, g, beta, S0, out, S_final, n_seg: i
                                              int(C), int(n_seg), _dtype_code(q),
                                              _stream_handle(stream))
     _check(st, "kda_chunk_fwd_segmented_noalloc")
+
+
+def kda_chunk_fwd_gated(q, k, v, g, beta, S0, gate_u, norm_w, out, S_final, cu_seqlens=None,
+                        norm_eps: float = 1e-5, C: int = 64, stream=None):
+    """Prefill plus the output side: ``out`` = RMSNorm(o~) * norm_w * sigma(gate_u) (see
+    include/kda.h). Dense [B, T, H, d] tensors, or a packed batch with ``cu_seqlens``."""
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    _check_tensors([("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out),
+                    ("gate_u", gate_u)], q.dtype, q.device)
+    _check_tensors([("S0", S0), ("S_final", S_final), ("norm_w", norm_w)], torch.float32,
+                   q.device)
+    _require(k.shape == q.shape and g.shape == q.shape, "q, k, g must share [B, T, H, d_k]")
+    _require(v.shape == (B, T, H, dv) and out.shape == v.shape and gate_u.shape == v.shape,
+             "v, out, gate_u must be [B, T, H, d_v]")
+    _require(beta.shape == (B, T, H), "beta must be [B, T, H]")
+    _require(norm_w.shape == (dv,), "norm_w must be [d_v]")
+    if cu_seqlens is not None:
+        _check_tensors([("cu_seqlens", cu_seqlens)], torch.int32, q.device)
+        _require(B == 1, "packed batches have a leading dimension of 1")
+        n_seq = cu_seqlens.shape[0] - 1
+    else:
+        n_seq = B
+    for name, s in (("S0", S0), ("S_final", S_final)):
+        _require(s is None or s.shape == (n_seq, H, dk, dv), f"{name} must be [n_seq, H, d_k, d_v]")
+    st = lib.kda_chunk_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0),
+                                 _ptr(gate_u), _ptr(norm_w), float(norm_eps), _ptr(out),
+                                 _ptr(S_final), _ptr(cu_seqlens), n_seq, H, T, dk, dv, int(C),
+                                 _dtype_code(q), _stream_handle(stream))
+    _check(st, "kda_chunk_fwd_gated")
+
+
+def kda_output_gate(o, gate_u, norm_w, y, norm_eps: float = 1e-5, stream=None):
+    """y = RMSNorm(o) * norm_w * sigma(gate_u) over the last axis (d_v in {64, 128})."""
+    lib = load_library()
+    dv = o.shape[-1]
+    _check_tensors([("o", o), ("gate_u", gate_u), ("y", y)], o.dtype, o.device)
+    _check_tensors([("norm_w", norm_w)], torch.float32, o.device)
+    _require(gate_u.shape == o.shape and y.shape == o.shape, "o, gate_u, y must share a shape")
+    _require(norm_w.shape == (dv,), "norm_w must be [d_v]")
+    st = lib.kda_output_gate(_ptr(o), _ptr(gate_u), _ptr(norm_w), float(norm_eps), _ptr(y),
+                             o.numel() // dv, dv, _dtype_code(o), _stream_handle(stream))
+    _check(st, "kda_output_gate")
+
+
+def _layer_n_seq(q, cu_seqlens):
+    if cu_seqlens is None:
+        return q.shape[0]
+    _check_tensors([("cu_seqlens", cu_seqlens)], torch.int32, q.device)
+    _require(q.shape[0] == 1, "packed batches have a leading dimension of 1")
+    return cu_seqlens.shape[0] - 1
+
+
+def _check_pre_params(H, d, conv_q, conv_k, conv_v, A_log, b_decay, device):
+    _check_tensors([("conv_q", conv_q), ("conv_k", conv_k), ("conv_v", conv_v),
+                    ("A_log", A_log), ("b_decay", b_decay)], torch.float32, device)
+    for name, c in (("conv_q", conv_q), ("conv_k", conv_k), ("conv_v", conv_v)):
+        _require(c.shape == (H, 4, d), f"{name} must be tap-major [H, 4, d]")
+    _require(A_log.shape == (H,) and b_decay.shape == (H, d), "A_log [H], b_decay [H, d]")
+
+
+def kda_pre_core(q_raw, k_raw, v_raw, z, conv_q, conv_k, conv_v, A_log, b_decay, q, k, v, g,
+                 cu_seqlens=None, stream=None):
+    """The inputs of the recurrence from the raw projections (see include/kda.h)."""
+    lib = load_library()
+    B, T, H, d = q_raw.shape
+    _check_tensors([(n, t) for n, t in (("q_raw", q_raw), ("k_raw", k_raw), ("v_raw", v_raw),
+                                        ("z", z), ("q", q), ("k", k), ("v", v), ("g", g))],
+                   q_raw.dtype, q_raw.device)
+    for n, t in (("k_raw", k_raw), ("v_raw", v_raw), ("z", z), ("q", q), ("k", k), ("v", v),
+                 ("g", g)):
+        _require(t.shape == q_raw.shape, f"{n} must be [B, T, H, d] like q_raw")
+    _check_pre_params(H, d, conv_q, conv_k, conv_v, A_log, b_decay, q_raw.device)
+    n_seq = _layer_n_seq(q_raw, cu_seqlens)
+    st = lib.kda_pre_core(*(_ptr(t) for t in (q_raw, k_raw, v_raw, z, conv_q, conv_k, conv_v,
+                                              A_log, b_decay, q, k, v, g, cu_seqlens)),
+                          n_seq, H, T, d, _dtype_code(q_raw), _stream_handle(stream))
+    _check(st, "kda_pre_core")
+
+
+def kda_chunk_fwd_fused(q_raw, k_raw, v_raw, z, beta, conv_q, conv_k, conv_v, A_log, b_decay,
+                        S0, out, S_final, gate_u=None, norm_w=None, cu_seqlens=None,
+                        norm_eps: float = 1e-5, C: int = 64, stream=None):
+    """The layer from the raw projections in one kernel (input side fused; output side fused
+    when ``gate_u`` is given). See include/kda.h."""
+    lib = load_library()
+    B, T, H, d = q_raw.shape
+    _check_tensors([(n, t) for n, t in (("q_raw", q_raw), ("k_raw", k_raw), ("v_raw", v_raw),
+                                        ("z", z), ("beta", beta), ("out", out),
+                                        ("gate_u", gate_u))], q_raw.dtype, q_raw.device)
+    for n, t in (("k_raw", k_raw), ("v_raw", v_raw), ("z", z), ("out", out)):
+        _require(t.shape == q_raw.shape, f"{n} must be [B, T, H, d] like q_raw")
+    _require(beta.shape == (B, T, H), "beta must be [B, T, H]")
+    _require(gate_u is None or gate_u.shape == out.shape, "gate_u must be shaped like out")
+    _check_pre_params(H, d, conv_q, conv_k, conv_v, A_log, b_decay, q_raw.device)
+    _check_tensors([("S0", S0), ("S_final", S_final), ("norm_w", norm_w)], torch.float32,
+                   q_raw.device)
+    n_seq = _layer_n_seq(q_raw, cu_seqlens)
+    st = lib.kda_chunk_fwd_fused(*(_ptr(t) for t in (q_raw, k_raw, v_raw, z, beta, conv_q, conv_k,
+                                                     conv_v, A_log, b_decay, S0, gate_u, norm_w)),
+                                 float(norm_eps), _ptr(out), _ptr(S_final), _ptr(cu_seqlens),
+                                 n_seq, H, T, d, d, int(C), _dtype_code(q_raw),
+                                 _stream_handle(stream))
+    _check(st, "kda_chunk_fwd_fused")
+
+
+def kda_recurrent_steps(q, k, v, g, beta, S, out, stream=None):
+    """K decode tokens per (sequence, head): q, k, g [N, K, H, d_k]; v, out [N, K, H, d_v];
+    beta [N, K, H]; S (fp32 [N, H, d_k, d_v]) updated in place."""
+    lib = load_library()
+    N, K, H, dk = q.shape
+    dv = v.shape[-1]
+    _check_tensors([("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out)],
+                   q.dtype, q.device)
+    _check_tensors([("S", S)], torch.float32, q.device)
+    _require(k.shape == q.shape and g.shape == q.shape, "q, k, g must share [N, K, H, d_k]")
+    _require(v.shape == (N, K, H, dv) and out.shape == v.shape, "v/out must be [N, K, H, d_v]")
+    _require(beta.shape == (N, K, H), "beta must be [N, K, H]")
+    _require(S.shape == (N, H, dk, dv), "S must be [N, H, d_k, d_v]")
+    st = lib.kda_recurrent_steps(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S),
+                                 _ptr(out), N, K, H, dk, dv, _dtype_code(q), _stream_handle(stream))
+    _check(st, "kda_recurrent_steps")
 
 
 def kda_sync_status(stream=None):

@@ -13,6 +13,8 @@
 #include "kda_chunk_tc.cuh"
 #include "kda_common.cuh"
 #include "kda_decode.cuh"
+#include "kda_post.cuh"
+#include "kda_pre.cuh"
 #include "kda_scan.cuh"
 #include "kda_selftest.cuh"
 
@@ -114,6 +116,33 @@ kda_status_t launch_scan(const float* M, const float* St, const float* S0, float
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "segment_scan launch");
+  return KDA_OK;
+}
+
+// Launches the standalone output gate over n_rows rows of d_v channels (y may alias o).
+kda_status_t launch_output_gate(const void* o, const void* u, const float* w, float eps, void* y,
+                                long long n_rows, int d_v, kda_dtype_t dtype, cudaStream_t st) {
+  if (n_rows == 0) return KDA_OK;
+  using bf = __nv_bfloat16;
+  if (d_v == 128) {
+    const unsigned grid = (unsigned)((n_rows + 15) / 16);
+    if (dtype == KDA_DTYPE_BF16)
+      kda::post::output_gate_kernel<bf><<<grid, 256, 0, st>>>((const bf*)o, (const bf*)u, w, eps,
+                                                              (bf*)y, n_rows);
+    else
+      kda::post::output_gate_kernel<float><<<grid, 256, 0, st>>>((const float*)o, (const float*)u,
+                                                                 w, eps, (float*)y, n_rows);
+  } else {
+    const unsigned grid = (unsigned)((n_rows + 31) / 32);
+    if (dtype == KDA_DTYPE_BF16)
+      kda::post::output_gate64_kernel<bf><<<grid, 256, 0, st>>>((const bf*)o, (const bf*)u, w, eps,
+                                                                (bf*)y, n_rows);
+    else
+      kda::post::output_gate64_kernel<float><<<grid, 256, 0, st>>>(
+          (const float*)o, (const float*)u, w, eps, (float*)y, n_rows);
+  }
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "output_gate launch");
   return KDA_OK;
 }
 
@@ -221,6 +250,155 @@ kda_status_t kda_recurrent_step(const void* q, const void* k, const void* v, con
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "decode_step launch");
   return KDA_OK;
+}
+
+kda_status_t kda_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* g,
+                                 const void* beta, const float* S0, const void* gate_u,
+                                 const float* norm_w, float norm_eps, void* out, float* S_final,
+                                 const int32_t* cu_seqlens, int n_seq, int H, int T, int d_k,
+                                 int d_v, int C, kda_dtype_t dtype, void* stream) {
+  t_last_error.clear();
+  kda_status_t s = check_common(H, d_k, d_v, dtype);
+  if (s != KDA_OK) return s;
+  if (n_seq < 0 || T < 0) return fail(KDA_ERR_INVALID_ARG, "n_seq and T must be >= 0 (got %d, %d)", n_seq, T);
+  if (!(C == 16 || C == 32 || C == 64 || C == 128))
+    return fail(KDA_ERR_UNSUPPORTED, "C must be 16, 32, 64 or 128 (got %d)", C);
+  if (!(norm_eps >= 0.f) || !(norm_eps < 1e30f))
+    return fail(KDA_ERR_INVALID_ARG, "norm_eps must be finite and >= 0");
+  const bool packed = cu_seqlens != nullptr;
+  const long long rows = packed ? (long long)T : (long long)n_seq * T;
+  if (rows * H * d_k >= (1ll << 40) || (long long)n_seq * H >= (1ll << 31) || rows >= (1ll << 31) ||
+      n_seq >= (1 << 30))
+    return fail(KDA_ERR_UNSUPPORTED, "problem too large");
+  if (packed && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
+    return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is not 4-byte aligned");
+  const bool tokens = rows > 0;
+  if ((s = check_ptr(q, "q", tokens)) || (s = check_ptr(k, "k", tokens)) ||
+      (s = check_ptr(v, "v", tokens)) || (s = check_ptr(g, "g", tokens)) ||
+      (s = check_ptr(beta, "beta", tokens)) || (s = check_ptr(out, "out", tokens)) ||
+      (s = check_ptr(gate_u, "gate_u", tokens)) || (s = check_ptr(norm_w, "norm_w", tokens)) ||
+      (s = check_ptr(S0, "S0", false)) || (s = check_ptr(S_final, "S_final", false)))
+    return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  kda::SeqParams P{q, k, v, g, beta, S0, out, S_final, cu_seqlens, n_seq, H, T};
+  const int n_problems = n_seq * H;
+  if (dtype == KDA_DTYPE_BF16 && d_k == 128 && kda::tc_supports(C)) {
+    // the tensor-core kernel gates each block's output on its way out
+    P.gate_u = gate_u;
+    P.norm_w = norm_w;
+    P.norm_eps = norm_eps;
+    return run_chunk(P, n_problems, d_k, C, dtype, st);
+  }
+  // other shapes: the raw output, then the standalone gate over it in place
+  if ((s = run_chunk(P, n_problems, d_k, C, dtype, st)) != KDA_OK) return s;
+  return launch_output_gate(out, gate_u, norm_w, norm_eps, out, rows * H, d_v, dtype, st);
+}
+
+kda_status_t kda_output_gate(const void* o, const void* gate_u, const float* norm_w,
+                             float norm_eps, void* y, long long n_rows, int d_v,
+                             kda_dtype_t dtype, void* stream) {
+  t_last_error.clear();
+  kda_status_t s = check_common(1, d_v, d_v, dtype);
+  if (s != KDA_OK) return s;
+  if (n_rows < 0) return fail(KDA_ERR_INVALID_ARG, "n_rows must be >= 0");
+  if (n_rows >= (1ll << 36)) return fail(KDA_ERR_UNSUPPORTED, "problem too large");
+  if (!(norm_eps >= 0.f) || !(norm_eps < 1e30f))
+    return fail(KDA_ERR_INVALID_ARG, "norm_eps must be finite and >= 0");
+  const bool any = n_rows > 0;
+  if ((s = check_ptr(o, "o", any)) || (s = check_ptr(gate_u, "gate_u", any)) ||
+      (s = check_ptr(norm_w, "norm_w", any)) || (s = check_ptr(y, "y", any)))
+    return s;
+  return launch_output_gate(o, gate_u, norm_w, norm_eps, y, n_rows, d_v, dtype,
+                            static_cast<cudaStream_t>(stream));
+}
+
+kda_status_t kda_pre_core(const void* q_raw, const void* k_raw, const void* v_raw,
+                          const void* z, const float* conv_q, const float* conv_k,
+                          const float* conv_v, const float* A_log, const float* b_decay, void* q,
+                          void* k, void* v, void* g, const int32_t* cu_seqlens, int n_seq, int H,
+                          int T, int d, kda_dtype_t dtype, void* stream) {
+  t_last_error.clear();
+  kda_status_t s = check_common(H, d, d, dtype);
+  if (s != KDA_OK) return s;
+  if (n_seq < 0 || T < 0) return fail(KDA_ERR_INVALID_ARG, "n_seq and T must be >= 0 (got %d, %d)", n_seq, T);
+  const bool packed = cu_seqlens != nullptr;
+  const long long rows = packed ? (long long)T : (long long)n_seq * T;
+  if (rows * H * d >= (1ll << 40) || rows >= (1ll << 31) || n_seq >= (1 << 30))
+    return fail(KDA_ERR_UNSUPPORTED, "problem too large");
+  if (packed && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
+    return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is not 4-byte aligned");
+  const bool any = rows > 0;
+  if ((s = check_ptr(q_raw, "q_raw", any)) || (s = check_ptr(k_raw, "k_raw", any)) ||
+      (s = check_ptr(v_raw, "v_raw", any)) || (s = check_ptr(z, "z", any)) ||
+      (s = check_ptr(conv_q, "conv_q", any)) || (s = check_ptr(conv_k, "conv_k", any)) ||
+      (s = check_ptr(conv_v, "conv_v", any)) || (s = check_ptr(A_log, "A_log", any)) ||
+      (s = check_ptr(b_decay, "b_decay", any)) || (s = check_ptr(q, "q", any)) ||
+      (s = check_ptr(k, "k", any)) || (s = check_ptr(v, "v", any)) || (s = check_ptr(g, "g", any)))
+    return s;
+  if (!any) return KDA_OK;
+  kda::pre::PreParams P{q_raw, k_raw, v_raw, z, conv_q, conv_k, conv_v, A_log, b_decay,
+                        q, k, v, g, cu_seqlens, n_seq, H, T};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int tok_per_cta = 4 * (256 / (d / 8));
+  const long long tiles = (rows + tok_per_cta - 1) / tok_per_cta;
+  const dim3 grid((unsigned)H, (unsigned)(tiles < 65535 ? tiles : 65535));  // the kernel strides over tiles
+  using bf = __nv_bfloat16;
+  if (d == 128) {
+    if (dtype == KDA_DTYPE_BF16) kda::pre::pre_core_kernel<bf, 128><<<grid, 256, 0, st>>>(P, rows);
+    else kda::pre::pre_core_kernel<float, 128><<<grid, 256, 0, st>>>(P, rows);
+  } else {
+    if (dtype == KDA_DTYPE_BF16) kda::pre::pre_core_kernel<bf, 64><<<grid, 256, 0, st>>>(P, rows);
+    else kda::pre::pre_core_kernel<float, 64><<<grid, 256, 0, st>>>(P, rows);
+  }
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "pre_core launch");
+  return KDA_OK;
+}
+
+kda_status_t kda_chunk_fwd_fused(const void* q_raw, const void* k_raw, const void* v_raw,
+                                 const void* z, const void* beta, const float* conv_q,
+                                 const float* conv_k, const float* conv_v, const float* A_log,
+                                 const float* b_decay, const float* S0, const void* gate_u,
+                                 const float* norm_w, float norm_eps, void* out, float* S_final,
+                                 const int32_t* cu_seqlens, int n_seq, int H, int T, int d_k,
+                                 int d_v, int C, kda_dtype_t dtype, void* stream) {
+  t_last_error.clear();
+  kda_status_t s = check_common(H, d_k, d_v, dtype);
+  if (s != KDA_OK) return s;
+  if (!(dtype == KDA_DTYPE_BF16 && d_k == 128 && (C == 64 || C == 128)))
+    return fail(KDA_ERR_UNSUPPORTED,
+                "the fused input side runs on the bf16 tensor-core path (d = 128, C = 64 or 128); "
+                "for other shapes use kda_pre_core, then kda_chunk_fwd or kda_chunk_fwd_gated");
+  if (n_seq < 0 || T < 0) return fail(KDA_ERR_INVALID_ARG, "n_seq and T must be >= 0 (got %d, %d)", n_seq, T);
+  if (gate_u != nullptr && (!(norm_eps >= 0.f) || !(norm_eps < 1e30f)))
+    return fail(KDA_ERR_INVALID_ARG, "norm_eps must be finite and >= 0");
+  const bool packed = cu_seqlens != nullptr;
+  const long long rows = packed ? (long long)T : (long long)n_seq * T;
+  if (rows * H * d_k >= (1ll << 40) || (long long)n_seq * H >= (1ll << 31) || rows >= (1ll << 31) ||
+      n_seq >= (1 << 30))
+    return fail(KDA_ERR_UNSUPPORTED, "problem too large");
+  if (packed && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
+    return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is not 4-byte aligned");
+  const bool tokens = rows > 0;
+  if ((s = check_ptr(q_raw, "q_raw", tokens)) || (s = check_ptr(k_raw, "k_raw", tokens)) ||
+      (s = check_ptr(v_raw, "v_raw", tokens)) || (s = check_ptr(z, "z", tokens)) ||
+      (s = check_ptr(beta, "beta", tokens)) || (s = check_ptr(out, "out", tokens)) ||
+      (s = check_ptr(conv_q, "conv_q", tokens)) || (s = check_ptr(conv_k, "conv_k", tokens)) ||
+      (s = check_ptr(conv_v, "conv_v", tokens)) || (s = check_ptr(A_log, "A_log", tokens)) ||
+      (s = check_ptr(b_decay, "b_decay", tokens)) || (s = check_ptr(gate_u, "gate_u", false)) ||
+      (s = check_ptr(norm_w, "norm_w", gate_u != nullptr && tokens)) ||
+      (s = check_ptr(S0, "S0", false)) || (s = check_ptr(S_final, "S_final", false)))
+    return s;
+  kda::SeqParams P{q_raw, k_raw, v_raw, z, beta, S0, out, S_final, cu_seqlens, n_seq, H, T};
+  P.conv_q = conv_q;
+  P.conv_k = conv_k;
+  P.conv_v = conv_v;
+  P.A_log = A_log;
+  P.b_decay = b_decay;
+  P.gate_u = gate_u;
+  P.norm_w = norm_w;
+  P.norm_eps = norm_eps;
+  return run_chunk(P, n_seq * H, d_k, C, dtype, static_cast<cudaStream_t>(stream));
 }
 
 kda_status_t kda_segment_transitions(const void* k, const void* v, const void* g,
@@ -417,6 +595,44 @@ int kda_segments_auto(int B, int H, int T) {
     }
   }
   return best_n;
+}
+
+kda_status_t kda_recurrent_steps(const void* q, const void* k, const void* v, const void* g,
+                                 const void* beta, float* S, void* out, int N, int K, int H,
+                                 int d_k, int d_v, kda_dtype_t dtype, void* stream) {
+  t_last_error.clear();
+  kda_status_t s = check_common(H, d_k, d_v, dtype);
+  if (s != KDA_OK) return s;
+  if (N < 0 || K < 0) return fail(KDA_ERR_INVALID_ARG, "N and K must be >= 0 (got %d, %d)", N, K);
+  if (N == 0 || K == 0) return KDA_OK;
+  if ((long long)N * H >= (1ll << 31) || (long long)N * K * H * d_k >= (1ll << 40))
+    return fail(KDA_ERR_UNSUPPORTED, "problem too large");
+  if ((s = check_ptr(q, "q", true)) || (s = check_ptr(k, "k", true)) ||
+      (s = check_ptr(v, "v", true)) || (s = check_ptr(g, "g", true)) ||
+      (s = check_ptr(beta, "beta", true)) || (s = check_ptr(S, "S", true)) ||
+      (s = check_ptr(out, "out", true)))
+    return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int grid = N * H;
+  using bf = __nv_bfloat16;
+  if (dtype == KDA_DTYPE_F32) {
+    const float *qq = (const float*)q, *kk = (const float*)k, *vv = (const float*)v,
+                *gg = (const float*)g, *bb = (const float*)beta;
+    if (d_k == 128)
+      kda::decode_tokens_kernel<float, 128, 128, 256><<<grid, 256, 0, st>>>(qq, kk, vv, gg, bb, S, (float*)out, K, H);
+    else
+      kda::decode_tokens_kernel<float, 64, 64, 128><<<grid, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (float*)out, K, H);
+  } else {
+    const bf *qq = (const bf*)q, *kk = (const bf*)k, *vv = (const bf*)v, *gg = (const bf*)g,
+             *bb = (const bf*)beta;
+    if (d_k == 128)
+      kda::decode_tokens_kernel<bf, 128, 128, 256><<<grid, 256, 0, st>>>(qq, kk, vv, gg, bb, S, (bf*)out, K, H);
+    else
+      kda::decode_tokens_kernel<bf, 64, 64, 128><<<grid, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (bf*)out, K, H);
+  }
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "decode_tokens launch");
+  return KDA_OK;
 }
 
 kda_status_t kda_wait_selftest(unsigned long long limit_ns, void* stream) {

@@ -51,6 +51,20 @@ struct SeqParams {
   float* M_out;
   // Nonzero: only the last segment of a sequence writes its final state, at (sequence, head).
   int sf_last_only;
+  // Output side (null gate_u: out receives the raw output o~): out receives
+  // RMSNorm(o~) * norm_w * sigma(gate_u), gate_u shaped like out, norm_w [d_v] fp32.
+  const void* gate_u;
+  const float* norm_w;
+  float norm_eps;
+  // Input side (null conv_q: q, k, v, g are the inputs of the recurrence). Otherwise q, k, v, g
+  // hold the raw projections q~, k~, v~ and the decay logit z, and the kernel forms
+  // q = L2Norm(ShortConv(q~)), k = L2Norm(ShortConv(k~)), v = ShortConv(v~) and
+  // g = g_min sigma(e^{A_h} z + b_h): conv_* [H, d, 4], A_log [H], b_decay [H, d], fp32.
+  const float* conv_q;
+  const float* conv_k;
+  const float* conv_v;
+  const float* A_log;
+  const float* b_decay;
 };
 
 // One (sequence or segment, head) problem of a launch.
@@ -59,6 +73,7 @@ struct Problem {
   size_t row0;     // first token row in the [rows, H] token grid
   int len;         // tokens
   bool ident;      // initial state I and v = 0; S0 is not read
+  int pos0;        // position of the first token inside its sequence (segments start inside)
   long long s0;    // index of the initial state in S0
   float* sf;       // array the final state goes to (S_final or M_out), or null
   long long sf_i;  // index in it
@@ -78,11 +93,13 @@ __device__ __forceinline__ bool resolve_problem(const SeqParams& P, int p, Probl
   pr.s0 = q;
   pr.sf = pr.ident ? P.M_out : P.S_final;
   pr.sf_i = q;
+  pr.pos0 = 0;
   if (P.seg_len > 0) {
     const int b = s % P.n_seq, sigma = s / P.n_seq;
     const long long a = (long long)sigma * P.seg_len;
     pr.row0 = (size_t)b * P.T + (size_t)a;
     pr.len = (int)max(0ll, min((long long)P.seg_len, (long long)P.T - a));
+    pr.pos0 = (int)a;
     if (P.sf_last_only) {
       pr.sf = sigma == P.n_seg - 1 ? P.S_final : nullptr;
       pr.sf_i = (long long)b * P.H + pr.h;

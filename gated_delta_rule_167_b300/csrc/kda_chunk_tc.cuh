@@ -61,6 +61,8 @@
 
 #include "../../include/kda.h"
 #include "kda_chunk_simt.cuh"
+#include "kda_post.cuh"
+#include "kda_pre.cuh"
 #include "kda_sm100.cuh"
 
 namespace kda {
@@ -140,11 +142,72 @@ __device__ __forceinline__ void tile_mma(float (&acc)[4], const float* Ab, int l
   }
 }
 
+// Input side, fused. Thread (cg, rg) of a group handles channels [8 cg, 8 cg + 8) of rows
+// 4 rg .. 4 rg + 3 of a staged [64 tokens][128] bf16 tile (two 128-byte-swizzled 64-channel
+// boxes); the 16 threads of a row are the lanes of a half-warp. Chunk address of row r:
+__device__ __forceinline__ uint32_t tile_chunk(int cg, int r) {
+  return (uint32_t)((cg >> 3) * BOX_BYTES + r * 128 + 16 * ((cg & 7) ^ (r & 7)));
+}
+
+// The causal 4-tap convolution of this thread's 4 rows (tap-major weights w[h][j][c], all 32 of
+// this thread's taps loaded in one batch before they are needed, so that their latency is paid
+// once). Taps before row 0 come from the previous block's last three raw rows, which that block's
+// pass left in a stash (halo(hr) = address of this thread's chunk of raw row 61 + hr);
+// `first_pos` is the position of row 0 inside its sequence, so that no tap reaches before a
+// sequence start. The 7 input rows stay packed (bf16 pairs) until used.
+template <typename Halo>
+__device__ __forceinline__ void conv_rows4(const uint8_t* tile, const float* w, int h, int cg, int rg,
+                                           int first_pos, Halo halo, float (&y)[4][8]) {
+  float t[4][8];
+  pre::load_taps<D>(w, h, 8 * cg, t);
+  uint32_t xr[7][4];
+#pragma unroll
+  for (int m = 0; m < 7; ++m) {
+    const int r = 4 * rg + m - 3;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r >= 0) v = *reinterpret_cast<const uint4*>(tile + tile_chunk(cg, r));
+    else if (first_pos > 0) v = *reinterpret_cast<const uint4*>(halo(r + 3));
+    xr[m][0] = v.x; xr[m][1] = v.y; xr[m][2] = v.z; xr[m][3] = v.w;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float x[7];
+#pragma unroll
+    for (int m = 0; m < 7; ++m)
+      x[m] = __uint_as_float((e & 1) ? (xr[m][e >> 1] & 0xFFFF0000u) : (xr[m][e >> 1] << 16));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float a = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j <= first_pos + 4 * rg + i) a = fmaf(t[j][e], x[i + 3 - j], a);
+      y[i][e] = a;
+    }
+  }
+}
+
+// Copies this thread's chunks of raw rows 61..63 (threads of rows 60..63) into the stash.
+template <typename Halo>
+__device__ __forceinline__ void stash_rows(const uint8_t* tile, int cg, Halo halo) {
+#pragma unroll
+  for (int r = 61; r < 64; ++r)
+    *reinterpret_cast<uint4*>(halo(r - 61)) = *reinterpret_cast<const uint4*>(tile + tile_chunk(cg, r));
+}
+
+// Writes this thread's 4 rows (packed bf16) back into a staged tile.
+__device__ __forceinline__ void put_rows4(uint8_t* tile, int cg, int rg, const uint4 (&pk)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(tile + tile_chunk(cg, 4 * rg + i)) = pk[i];
+}
+
 __device__ __forceinline__ void st_pack8(uint32_t saddr, const float (&x)[8]) {
   st_shared_v4(saddr, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
                pack_bf16(x[6], x[7]));
 }
 
+// PRE: the inputs are the raw projections and the input side is computed in the kernel; POST: the
+// output side is applied in the output epilogue. The plain kernel (both false) carries neither.
+template <bool PRE, bool POST>
 __global__ void __launch_bounds__(THREADS, 1)
     chunk_tc_kernel(const __grid_constant__ TmaMaps maps, SeqParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -184,6 +247,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const size_t row0 = pr.row0;
   const bool vzero = pr.ident;              // v = 0: no v tile, U^T = -Z^T G^T
   const bool write_out = P.out != nullptr;  // outputs wanted
+  constexpr bool pre = PRE;
   const int nblocks = (len + C - 1) / C;
 
   if (tid == 0) {
@@ -288,12 +352,45 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_before();
     };
-    // after a group barrier that follows stage_o(b)
+    // after a group barrier that follows stage_o(b). With an output gate, each row of 128
+    // channels (16 lanes of a half-warp, 8 channels each) is normalised and gated on its way out:
+    // y = o~ / sqrt(mean(o~^2) + eps) * w * sigma(u), the mean by a 16-lane reduction.
+    constexpr bool gated = POST;
+    auto load_u = [&](int b, uint4 (&ur)[4]) {
+      const int tb = b * C;
+      const int nb = min(C, len - tb);
+      const __nv_bfloat16* ub = static_cast<const __nv_bfloat16*>(P.gate_u) +
+                                ((row0 + tb + (lt >> 4)) * H + h) * D + 8 * (lt & 15);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = (lt >> 4) + 16 * i;
+        ur[i] = r < nb ? *reinterpret_cast<const uint4*>(ub + (size_t)(16 * i) * H * D)
+                       : make_uint4(0, 0, 0, 0);
+      }
+    };
     auto store_o = [&](int b) {
       const int tb = b * C;
       const int nb = min(C, len - tb);
       const int q = lt & 15;  // 16-byte chunk of a row; rows lt / 16 + 16 i
-      __nv_bfloat16* ob = out + ((row0 + tb + (lt >> 4)) * H + h) * D + 8 * q;
+      const size_t off = ((row0 + tb + (lt >> 4)) * H + h) * D + 8 * q;
+      __nv_bfloat16* ob = out + off;
+      if constexpr (gated) {
+        uint4 ur[4];
+        load_u(b, ur);
+        float w8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w8[e] = P.norm_w[8 * q + e];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = (lt >> 4) + 16 * i;
+          float x[8], u8[8];
+          post::unpack8(*reinterpret_cast<const uint4*>(stg + r * 256 + 16 * (q ^ (r & 7))), x);
+          post::unpack8(ur[i], u8);
+          post::gate_chunk(x, u8, w8, P.norm_eps, D);
+          if (r < nb) *reinterpret_cast<uint4*>(ob + (size_t)(16 * i) * H * D) = post::pack8(x);
+        }
+        return;
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = (lt >> 4) + 16 * i;
@@ -321,6 +418,53 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!group_wait2(&bar_in, blk & 1, nullptr, 0, BAR_P)) { aborted = true; break; }
       pend_in = false;
+      if constexpr (pre) {
+        // ---------------- input side: k = L2Norm(ShortConv(k~)), q = L2Norm(ShortConv(q~)) and
+        // g = g_min sigma(e^A z + b) in place in the staged tiles, thread (cg, rg): channels
+        // 8 cg .. + 7 of rows 4 rg .. + 3. Every raw row is read before any is written. The last
+        // three raw rows of k~ and q~ wait for the next block in the padding columns 64..71 of WS,
+        // which no other step touches: 16-byte chunk ((tensor * 3 + row) * 16 + cg) at WS row
+        // chunk / 2, byte 256 + 16 (chunk % 2).
+        const int cg = lt & 15, rg = lt >> 4;
+        const int first_pos = pr.pos0 + t0;
+#pragma unroll
+        for (int ts = 0; ts < 2; ++ts) {  // k, then q (one tensor's results live at a time)
+          auto halo = [&](int hr) {
+            const int chunk = (ts * 3 + hr) * 16 + cg;
+            return sm + WS + (chunk >> 1) * (WLD * 4) + 64 * 4 + (chunk & 1) * 16;
+          };
+          uint8_t* tile = sm + (ts ? IN_Q : IN_K);
+          uint4 pk[4];
+          {
+            float y[4][8];
+            conv_rows4(tile, ts ? P.conv_q : P.conv_k, h, cg, rg, first_pos, halo, y);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              pre::l2norm8<D, false>(y[i]);
+              pk[i] = post::pack8(y[i]);
+            }
+          }
+          if (ts == 1) {  // the decay gate on this thread's own chunks of the z tile
+            const float eA = expf(P.A_log[h]);
+            float b8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) b8[e] = P.b_decay[(size_t)h * D + 8 * cg + e];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4* p4 = reinterpret_cast<uint4*>(sm + IN_G + tile_chunk(cg, 4 * rg + i));
+              float z[8];
+              post::unpack8(*p4, z);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) z[e] = pre::decay_gate<__nv_bfloat16>(z[e], eA, b8[e]);
+              *p4 = post::pack8(z);
+            }
+          }
+          named_sync(BAR_P, GROUP);  // every raw row of this tile (and its stash) has been read
+          if (rg == 15 && blk + 1 < nblocks) stash_rows(tile, cg, halo);
+          put_rows4(tile, cg, rg, pk);
+        }
+        named_sync(BAR_P, GROUP);
+      }
       // ---------------- operands: X, Y, (K e^Gamma)^T, (Q e^Gamma)^T; Khat^T kept packed
       // Warp w covers channels 16 w .. 16 w + 15 (channel group cg = 0, 1 of 8) over all 64 tokens:
       // lane (g, t) holds, for each 8-token block m, the tokens 8 m + 2 t, 8 m + 2 t + 1 of
@@ -789,6 +933,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!vzero) {
         if (!group_wait2(&bar_v, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
         pend_v = false;
+        if constexpr (pre) {  // input side: v = ShortConv(v~) in place in the staged tile (as for k above);
+          // the last three raw rows wait for the next block in the padding columns 16..19 of trr
+          // (16-byte chunk row * 16 + cg), which no other step touches
+          const int cg = lt & 15, rg = lt >> 4;
+          auto halo = [&](int hr) {
+            const int chunk = hr * 16 + cg;
+            return reinterpret_cast<uint8_t*>(&trr[chunk >> 4][chunk & 15][16]);
+          };
+          float y[4][8];
+          conv_rows4(sm + IN_V, P.conv_v, h, cg, rg, pr.pos0 + t0, halo, y);
+          uint4 pk[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) pk[i] = post::pack8(y[i]);
+          named_sync(BAR_S, GROUP);  // every raw row (and the stash) has been read
+          if (rg == 15 && blk + 1 < nblocks) stash_rows(sm + IN_V, cg, halo);
+          put_rows4(sm + IN_V, cg, rg, pk);
+          fence_proxy_async_smem();  // v is a tensor-core operand
+          named_sync(BAR_S, GROUP);
+        }
       } else {
         named_sync(BAR_S, GROUP);
       }
@@ -941,14 +1104,16 @@ inline kda_status_t launch_chunk_tc(const SeqParams& P, int n_problems, int C, c
     err = "cuTensorMapEncodeTiled failed";
     return KDA_ERR_CUDA;
   }
-  cudaError_t e = cudaFuncSetAttribute(tc::chunk_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const bool pre = P.conv_q != nullptr, post = P.gate_u != nullptr;
+  auto kern = pre ? (post ? tc::chunk_tc_kernel<true, true> : tc::chunk_tc_kernel<true, false>)
+                  : (post ? tc::chunk_tc_kernel<false, true> : tc::chunk_tc_kernel<false, false>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)tc::SMEM_ALLOC);
   if (e != cudaSuccess) {
     err = std::string("cudaFuncSetAttribute(chunk_tc): ") + cudaGetErrorString(e);
     return KDA_ERR_CUDA;
   }
-  tc::chunk_tc_kernel<<<n_problems, tc::THREADS, tc::SMEM_ALLOC, st>>>(maps, P);
+  kern<<<n_problems, tc::THREADS, tc::SMEM_ALLOC, st>>>(maps, P);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     err = std::string("chunk_tc launch: ") + cudaGetErrorString(e);

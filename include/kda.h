@@ -95,6 +95,86 @@ kda_status_t kda_recurrent_step(const void* q, const void* k, const void* v, con
                                 int d_v, kda_dtype_t dtype, void* stream);
 
 /*
+ * K decode tokens for each of N sequences x H heads, updating the resident states in place: the
+ * recurrence applied K times (Glossaire, entry "Decode"), with each state slice held on chip across
+ * the K tokens, so the state crosses HBM once in each direction whatever K is (verification of K
+ * speculative draft tokens, or a short run of tokens).
+ *   q, k, g : [N, K, H, d_k] dtype   v, out : [N, K, H, d_v] dtype   beta : [N, K, H] dtype
+ *   S       : [N, H, d_k, d_v] fp32, read and overwritten with the state after the K tokens
+ * out receives o_t = S_t^T q_t for every token. K = 1 gives kda_recurrent_step.
+ */
+kda_status_t kda_recurrent_steps(const void* q, const void* k, const void* v, const void* g,
+                                 const void* beta, float* S, void* out, int N, int K, int H,
+                                 int d_k, int d_v, kda_dtype_t dtype, void* stream);
+
+/*
+ * Chunkwise prefill followed by the output side of the layer (Kimi K3 wiki, "Notations
+ * mathématiques": o~_t is the raw output before the gate; table "Fonctions": RMSNorm(x) =
+ * x / sqrt(mean_i x_i^2 + eps) * w; chapter 03: RMSNorm on KDA's recurrent output; "Tableau des
+ * spécifications": RMSNorm epsilon 1e-5 and a full-rank KDA output gate). `out` receives
+ *   y_t = RMSNorm(o~_t) * norm_w * sigma(u_t)       per token and head, over the d_v channels
+ *   gate_u : the gate pre-activation u, shaped and typed like out (the full-rank gate
+ *            projection is the caller's)
+ *   norm_w : fp32 [d_v], one RMSNorm weight vector shared by the heads; norm_eps >= 0 (1e-5 in K3)
+ * cu_seqlens NULL: a dense batch (n_seq = B sequences of T tokens, the layout of kda_chunk_fwd);
+ * otherwise a packed batch (n_seq = N sequences, T = T_total, the layout and rules of
+ * kda_chunk_fwd_varlen). S0 / S_final as in those calls. The bf16 tensor-core path (d = 128,
+ * C = 64 or 128) normalises and gates each block in its output epilogue, from the bf16-rounded
+ * raw output; the other paths write o~ and apply kda_output_gate over it in place.
+ */
+kda_status_t kda_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* g,
+                                 const void* beta, const float* S0, const void* gate_u,
+                                 const float* norm_w, float norm_eps, void* out, float* S_final,
+                                 const int32_t* cu_seqlens, int n_seq, int H, int T, int d_k,
+                                 int d_v, int C, kda_dtype_t dtype, void* stream);
+
+/*
+ * The output side alone (same definition and references as kda_chunk_fwd_gated), for the raw
+ * outputs of decode steps or of any other call: y = RMSNorm(o) * norm_w * sigma(u) over each row
+ * of d_v channels. o, gate_u, y: [n_rows, d_v] of `dtype` (y may be o); norm_w fp32 [d_v];
+ * d_v in {64, 128}.
+ */
+kda_status_t kda_output_gate(const void* o, const void* gate_u, const float* norm_w,
+                             float norm_eps, void* y, long long n_rows, int d_v,
+                             kda_dtype_t dtype, void* stream);
+
+/*
+ * The input side of the layer (Kimi K3 wiki, "Notations mathématiques", table "Fonctions":
+ * ShortConv = causal convolution with a kernel of size 4, L2Norm(x) = x / ||x||_2; table
+ * "Attention et KDA": q, k L2-normalised, per-head log scale A_h, per-head decay bias b_alpha^h,
+ * decay logit z_t; "Glossaire", entry "Décroissance bornée": g = g_min sigma(e^A z), g_min = -5):
+ *   q = L2Norm(ShortConv(q_raw)), k = L2Norm(ShortConv(k_raw)), v = ShortConv(v_raw),
+ *   g = -5 sigma(e^{A_log[h]} z + b_decay[h])
+ * ShortConv is depthwise: conv_q / conv_k / conv_v are fp32 [H, 4, d], tap-major, with [h, j, c]
+ * the weight of channel c on the token j steps back (a [H * d, 1, 4] convolution weight transposed
+ * once); zeros before the first token of each sequence, no activation after it.
+ * A_log fp32 [H]; b_decay fp32 [H, d]. q_raw, k_raw, v_raw, z and the outputs q, k, v, g share
+ * the token layout of kda_chunk_fwd (cu_seqlens NULL: n_seq = B sequences of T tokens) or of
+ * kda_chunk_fwd_varlen (cu_seqlens given: n_seq = N, T = T_total). Any dtype, d in {64, 128}.
+ */
+kda_status_t kda_pre_core(const void* q_raw, const void* k_raw, const void* v_raw,
+                          const void* z, const float* conv_q, const float* conv_k,
+                          const float* conv_v, const float* A_log, const float* b_decay, void* q,
+                          void* k, void* v, void* g, const int32_t* cu_seqlens, int n_seq, int H,
+                          int T, int d, kda_dtype_t dtype, void* stream);
+
+/*
+ * The layer from the raw projections in one pass: the input side of kda_pre_core computed inside
+ * the prefill kernel (k, q, z and v are convolved, normalised and gated in shared memory as each
+ * block lands; they never return to global memory), the chunkwise recurrence, and, if gate_u is
+ * given, the output side of kda_chunk_fwd_gated in the output epilogue (gate_u NULL: out is the
+ * raw output o~). Arguments as in kda_pre_core and kda_chunk_fwd_gated. bf16, d_k = d_v = 128,
+ * C in {64, 128} only (KDA_ERR_UNSUPPORTED otherwise: use kda_pre_core and the other calls).
+ */
+kda_status_t kda_chunk_fwd_fused(const void* q_raw, const void* k_raw, const void* v_raw,
+                                 const void* z, const void* beta, const float* conv_q,
+                                 const float* conv_k, const float* conv_v, const float* A_log,
+                                 const float* b_decay, const float* S0, const void* gate_u,
+                                 const float* norm_w, float norm_eps, void* out, float* S_final,
+                                 const int32_t* cu_seqlens, int n_seq, int H, int T, int d_k,
+                                 int d_v, int C, kda_dtype_t dtype, void* stream);
+
+/*
  * Segment transitions (Kimi K3 wiki, "Notations mathématiques", table "Attention et KDA": the
  * transition M_t and S~, the state computed from S = 0; "Glossaire", entry "KCP": the pair
  * (cumulative M, local S~) of a stretch of tokens composes associatively and exactly).

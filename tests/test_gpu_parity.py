@@ -326,3 +326,58 @@ def test_host_pipeline_matches_device_call(kda):
                                     C=64, device=DEV, stream=side, pipeline=pl)
         assert torch.equal(oh, ref_out.cpu()) and torch.equal(sh, ref_S.cpu())
     kda.kda_sync_status(side)
+
+
+# ------------------------------------------------------------------ several decode tokens per call
+
+
+def _decode_tokens_inputs(N, K, H, d, dtype, seed):
+    dec = kda_synth.make_decode_inputs(N, H, d, d, dtype, seed=seed, S0_std=0.3, steps=K)
+    stack = {n: torch.stack([st[n] for st in dec["steps"]], dim=1) for n in ("q", "k", "v", "g", "beta")}
+    return dec, stack  # stack: [N, K, H, ...]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("K", [1, 3, 8])
+def test_decode_tokens_equal_single_steps_and_oracle(kda, dtype, d, K):
+    """K tokens in one call give the same bits as K single-token calls (the same arithmetic per
+    token, the state kept in fp32 on chip instead of in HBM) and match the oracle."""
+    dec, stack = _decode_tokens_inputs(5, K, 3, d, dtype, seed=K + d)
+    S1 = dec["S"].to(DEV)
+    outs = [kda.recurrent_step(*(st[n].to(DEV) for n in ("q", "k", "v", "g", "beta")), S1)
+            for st in dec["steps"]]
+    S2 = dec["S"].to(DEV)
+    out = torch.empty(5, K, 3, d, dtype=stack["q"].dtype, device=DEV)
+    kda.kda_recurrent_steps(*(stack[n].to(DEV) for n in ("q", "k", "v", "g", "beta")), S2, out)
+    kda.kda_sync_status()
+    assert torch.equal(S1, S2)
+    for t in range(K):
+        assert torch.equal(out[:, t], outs[t])
+    Sref = f64(dec["S"])
+    for t, st in enumerate(dec["steps"]):
+        o_ref, Sref = oracle.decode_step(*(f64(st[n]) for n in ("q", "k", "v", "g", "beta")), Sref)
+        check(out[:, t].float().cpu().double().numpy(), o_ref, dtype, f"o[{t}]")
+    check(S2.cpu().double().numpy(), Sref, dtype, "S")
+
+
+def test_decode_tokens_N256_H96_K4_sampled(kda):
+    """Four tokens for the full 256 x 96 state in one call; sampled problems against the oracle."""
+    N, K, H, d = 256, 4, 96, 128
+    dec = kda_synth.make_decode_inputs(N, H, d, d, "bf16", seed=7, S0_std=0.02, steps=K, device=DEV)
+    stack = {n: torch.stack([st[n] for st in dec["steps"]], dim=1).contiguous()
+             for n in ("q", "k", "v", "g", "beta")}
+    picks = [(0, 0), (100, 50), (255, 95)]
+    S_host = {p: dec["S"][p[0], p[1]].cpu().double().numpy()[None, None] for p in picks}
+    S = dec["S"]
+    out = torch.empty(N, K, H, d, dtype=torch.bfloat16, device=DEV)
+    kda.kda_recurrent_steps(*(stack[n] for n in ("q", "k", "v", "g", "beta")), S, out)
+    kda.kda_sync_status()
+    for (n, h) in picks:
+        Sref = S_host[(n, h)]
+        for t in range(K):
+            args = [f64(stack[x][n:n + 1, t, h:h + 1].cpu()) for x in ("q", "k", "v", "g", "beta")]
+            o_ref, Sref = oracle.decode_step(*args, Sref)
+            check(out[n:n + 1, t, h:h + 1].float().cpu().double().numpy(), o_ref, "bf16",
+                  f"o[t={t}, n={n}, h={h}]")
+        check(S[n:n + 1, h:h + 1].cpu().double().numpy(), Sref, "bf16", f"S[n={n},h={h}]")
