@@ -588,7 +588,7 @@ def bench_decode_tokens(kda, args, world, rank, device, stream, peaks, K=4, call
 
 def bench_nano(kda, args, world, rank, device, stream, peaks, steps=5):
     """The nano-K3 head shape (8 heads x 64 channels, context 2048), 64 sequences, bf16: the
-    d = 64 path (CUDA cores)."""
+    tensor-core kernel with 64-channel heads (run in its 128-channel tiles, upper half zero)."""
     B, T, H, d, C = 64, 2048, 8, 64, 64
     inp = kda_synth.make_prefill_inputs(B, T, H, d, d, "bf16", seed=rank, device=device)
     x = [inp[n] for n in ("q", "k", "v", "g", "beta")]

@@ -84,10 +84,8 @@ kda_status_t launch_simt(const kda::SeqParams& P, int n_problems, int C, cudaStr
 kda_status_t run_chunk(const kda::SeqParams& P, int n_problems, int d, int C, kda_dtype_t dtype,
                        cudaStream_t st) {
   if (n_problems == 0) return KDA_OK;
-  if (dtype == KDA_DTYPE_BF16 && d == 128 && kda::tc_supports(C)) {
-    kda_status_t s = kda::launch_chunk_tc(P, n_problems, C, st, t_last_error);
-    return s;
-  }
+  if (dtype == KDA_DTYPE_BF16 && kda::tc_supports(C, d, P))
+    return kda::launch_chunk_tc(P, n_problems, d, st, t_last_error);
   if (dtype == KDA_DTYPE_F32)
     return d == 128 ? launch_simt<float, 128>(P, n_problems, C, st)
                     : launch_simt<float, 64>(P, n_problems, C, st);
@@ -282,7 +280,7 @@ kda_status_t kda_chunk_fwd_gated(const void* q, const void* k, const void* v, co
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   kda::SeqParams P{q, k, v, g, beta, S0, out, S_final, cu_seqlens, n_seq, H, T};
   const int n_problems = n_seq * H;
-  if (dtype == KDA_DTYPE_BF16 && d_k == 128 && kda::tc_supports(C)) {
+  if (dtype == KDA_DTYPE_BF16 && d_k == 128 && kda::tc::tc_supports(C)) {
     // the tensor-core kernel gates each block's output on its way out
     P.gate_u = gate_u;
     P.norm_w = norm_w;

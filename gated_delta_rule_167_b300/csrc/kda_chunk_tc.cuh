@@ -39,9 +39,9 @@
 //     out of TMEM; the diagonal inverses T_RR; then, once S has finished block n, Khat^T of
 //     block n + 1 and block n's O out of TMEM.
 //   group S (warps 8-15), block n:
-//     tcgen05: Z^T = S^T (K e^Gamma)^T, O^T = S^T (Q e^Gamma)^T; meanwhile S^T <- S^T e^{Gamma_L}
-//     SIMT: Z^T -> bf16; the off-diagonal blocks of T (tf32 warp MMAs); G = T Diag(beta) (bf16)
-//     tcgen05: U^T = V^T G^T - Z^T G^T, U^T -> bf16
+//     tcgen05: Z^T = S^T (K e^Gamma)^T, O^T = S^T (Q e^Gamma)^T; while it runs, the off-diagonal
+//       blocks of T (tf32 warp MMAs) and G = T Diag(beta) (bf16); then Z^T -> bf16
+//     tcgen05: U^T = V^T G^T - Z^T G^T; while it runs, S^T <- S^T e^{Gamma_L}; U^T -> bf16
 //     tcgen05: O^T += U^T P^T;  S^T += U^T Khat;  SIMT: bf16 copy of S^T
 // Shared buffers pass between the groups through mbarriers: P may rewrite X and Y once its
 // A/P product of the previous block has completed, (K/Q e^Gamma)^T once S's first product has,
@@ -207,9 +207,17 @@ __device__ __forceinline__ void st_pack8(uint32_t saddr, const float (&x)[8]) {
 
 // PRE: the inputs are the raw projections and the input side is computed in the kernel; POST: the
 // output side is applied in the output epilogue. The plain kernel (both false) carries neither.
-template <bool PRE, bool POST>
+// DH is the head size of the tensors in memory, d_k = d_v = 128 or 64. At 64 (the plain kernel
+// only) the problem runs in the same 128-channel tiles: the TMA loads only the first 64-channel
+// box of each tile and the second box stays zero, so k, q, v and g are zero-padded (g = 0 is a
+// decay factor of 1). Padded key channels of S are never written (k = 0 there) and padded value
+// channels stay zero (v = 0 and Z = 0 there), so the first 64 x 64 block of S and the first 64
+// channels of O are those of the unpadded problem; only they are read in and written out.
+template <bool PRE, bool POST, int DH = 128>
 __global__ void __launch_bounds__(THREADS, 1)
     chunk_tc_kernel(const __grid_constant__ TmaMaps maps, SeqParams P) {
+  static_assert(DH == 128 || (DH == 64 && !PRE && !POST), "head size 64: plain kernel only");
+  constexpr int NBOX = DH / 64;  // 64-channel boxes loaded per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -268,6 +276,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     prefetch_tensormap(&maps.g);
   }
   if (warp == 0) tmem_alloc(&tmem_base_s, 512);
+  if constexpr (DH == 64) {  // the second box of every input tile is the zero padding
+#pragma unroll
+    for (uint32_t base : {IN_K, IN_Q, IN_G, IN_V})
+      for (int i = tid; i < (int)BOX_BYTES / 16; i += THREADS)
+        st_shared_v4(sb + base + BOX_BYTES + 16u * (uint32_t)i, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();  // v is a tensor-core operand
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -276,7 +291,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   auto load2 = [&](uint32_t dst, const CUtensorMap* m, int row, uint64_t* bar) {
     tma_load_3d(sm + dst, m, 0, h, row, bar);
-    tma_load_3d(sm + dst + BOX_BYTES, m, 64, h, row, bar);
+    if constexpr (NBOX == 2) tma_load_3d(sm + dst + BOX_BYTES, m, 64, h, row, bar);
   };
   bool aborted = false;
   // Waits of a whole group: one thread polls the mbarrier while the others sleep in the
@@ -295,7 +310,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const unsigned short* __restrict__ beta_u = static_cast<const unsigned short*>(P.beta);
     auto issue_in = [&](int b) {
       const int row = (int)(row0 + (size_t)b * C);
-      mbar_arrive_expect_tx(&bar_in, 6 * BOX_BYTES);
+      mbar_arrive_expect_tx(&bar_in, 3 * NBOX * BOX_BYTES);
       load2(IN_K, &maps.k, row, &bar_in);
       load2(IN_Q, &maps.q, row, &bar_in);
       load2(IN_G, &maps.g, row, &bar_in);
@@ -304,7 +319,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
           tma_prefetch_3d(mp[i], 0, h, row + C);
-          tma_prefetch_3d(mp[i], 64, h, row + C);
+          if constexpr (NBOX == 2) tma_prefetch_3d(mp[i], 64, h, row + C);
         }
       }
     };
@@ -374,7 +389,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int q = lt & 15;  // 16-byte chunk of a row; rows lt / 16 + 16 i
       const size_t off = ((row0 + tb + (lt >> 4)) * H + h) * D + 8 * q;
       __nv_bfloat16* ob = out + off;
-      if constexpr (gated) {
+      if constexpr (DH == 64) {  // the first 8 chunks of each row: chunk lt % 8 of rows lt / 8 + 32 i
+        const int q8 = lt & 7;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int r = (lt >> 3) + 32 * i;
+          if (r < nb)
+            *reinterpret_cast<uint4*>(out + ((row0 + tb + r) * H + h) * DH + 8 * q8) =
+                *reinterpret_cast<const uint4*>(stg + r * 256 + 16 * (q8 ^ (r & 7)));
+        }
+      } else if constexpr (gated) {
         uint4 ur[4];
         load_u(b, ur);
         float w8[8];
@@ -389,14 +413,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           post::gate_chunk(x, u8, w8, P.norm_eps, D);
           if (r < nb) *reinterpret_cast<uint4*>(ob + (size_t)(16 * i) * H * D) = post::pack8(x);
         }
-        return;
-      }
+      } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = (lt >> 4) + 16 * i;
-        if (r < nb)
-          *reinterpret_cast<uint4*>(ob + (size_t)(16 * i) * H * D) =
-              *reinterpret_cast<const uint4*>(stg + r * 256 + 16 * (q ^ (r & 7)));
+        for (int i = 0; i < 4; ++i) {
+          const int r = (lt >> 4) + 16 * i;
+          if (r < nb)
+            *reinterpret_cast<uint4*>(ob + (size_t)(16 * i) * H * D) =
+                *reinterpret_cast<const uint4*>(stg + r * 256 + 16 * (q ^ (r & 7)));
+        }
       }
     };
 
@@ -743,23 +767,26 @@ __global__ void __launch_bounds__(THREADS, 1)
     // =====================================================================  group S
     const bool leader = lt == 0;
     auto issue_v = [&](int b) {
-      mbar_arrive_expect_tx(&bar_v, 2 * BOX_BYTES);
+      mbar_arrive_expect_tx(&bar_v, NBOX * BOX_BYTES);
       load2(IN_V, &maps.v, (int)(row0 + (size_t)b * C), &bar_v);
       if (b + 1 < nblocks) {  // the next v tile into L2
         tma_prefetch_3d(&maps.v, 0, h, (int)(row0 + (size_t)(b + 1) * C));
-        tma_prefetch_3d(&maps.v, 64, h, (int)(row0 + (size_t)(b + 1) * C));
+        if constexpr (NBOX == 2) tma_prefetch_3d(&maps.v, 64, h, (int)(row0 + (size_t)(b + 1) * C));
       }
     };
-    // ---- initial state S^T: lane v = c, key channels 64 hh .. 64 hh + 63 (coalesced over v)
+    // ---- initial state S^T: lane v = c, key channels 64 hh .. 64 hh + 63 (coalesced over v);
+    // with DH = 64 only key and value channels below 64 exist, the rest is the zero padding
     {
-      const float* s0 = (P.S0 && !pr.ident) ? P.S0 + (size_t)pr.s0 * D * D + c : nullptr;
+      const bool real = DH == 128 || (c < DH && hh == 0);
+      const float* s0 = (P.S0 && !pr.ident && real) ? P.S0 + (size_t)pr.s0 * DH * DH + c : nullptr;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t sv[32], sbf[16];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int cc = 64 * hh + 32 * half + j;  // key channel
-          sv[j] = s0 ? __float_as_uint(s0[(size_t)cc * D]) : ((pr.ident && cc == c) ? 0x3F800000u : 0u);
+          sv[j] = s0 ? __float_as_uint(s0[(size_t)cc * DH])
+                     : ((pr.ident && real && cc == c) ? 0x3F800000u : 0u);
         }
         tmem_st32(tl + T_ST + 64 * hh + 32 * half, sv);
 #pragma unroll
@@ -810,46 +837,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         umma_commit(&bar_ZO);
       }
       pend_mma = true; last_mma = &bar_ZO; last_par = ph;
-      // ---------------- meanwhile: S^T <- S^T Diag(e^{Gamma_L}) (the product above reads the
-      // bf16 copy; Khat^T U accumulates onto this one). The issuing thread's warp waits while its
-      // products enter the tensor pipe, so the warp of the same lane quarter in the other half
-      // scales all 128 columns of those lanes.
-      if (lt >= 32) {
-        const bool both = lt >= 128 && lt < 160;  // lane quarter 0, second half
-        const int np = both ? 8 : 4;
-        const int cb = both ? 0 : 64 * hh;
-        uint32_t v[16];
-#pragma unroll 1
-        for (int part = 0; part < np; ++part) {
-          const int c0 = cb + 16 * part;
-          tmem_ld16(tl + T_ST + c0, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; j += 4) {
-            const float4 gv = *reinterpret_cast<const float4*>(&gl_s[par][c0 + j]);
-            const float2 a0 = mul2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])),
-                                   make_float2(gv.x, gv.y));
-            const float2 a1 = mul2(make_float2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])),
-                                   make_float2(gv.z, gv.w));
-            v[j] = __float_as_uint(a0.x); v[j + 1] = __float_as_uint(a0.y);
-            v[j + 2] = __float_as_uint(a1.x); v[j + 3] = __float_as_uint(a1.y);
-          }
-          tmem_st16(tl + T_ST + c0, v);
-        }
-      }
-      // ---------------- Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand; then wait for group P
-      // to have written A, P and the diagonal inverses of this block (bar_ext)
-      if (!group_wait2(&bar_ZO, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
-      pend_mma = false;
-      tc_fence_after();
-      {
-        uint32_t v[32], zb[16];
-        tmem_ld32(tl + T_ZT + 32 * hh, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) zb[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-        tmem_st16(tl + T_ZB + 16 * hh, zb);
-      }
+      // ---------------- while that product runs: the solve of this block, once group P has
+      // written A, P and the diagonal inverses (bar_ext)
       if (!group_wait2(&bar_ext, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       // ---------------- T = (I + A)^{-1} (unit lower triangular) and G = T Diag(beta) (bf16)
       // From the 16 x 16 diagonal inverses T_RR (group P, in trr) and the block-inverse identity
@@ -927,9 +916,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       fence_proxy_async_smem();  // G is a tensor-core operand
+      named_sync(BAR_S, GROUP);  // every thread of the group is done with WS
+      if (leader) mbar_arrive(&bar_wsfree);
+      // ---------------- Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand
+      if (!group_wait2(&bar_ZO, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
+      pend_mma = false;
+      tc_fence_after();
+      {
+        uint32_t v[32], zb[16];
+        tmem_ld32(tl + T_ZT + 32 * hh, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) zb[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+        tmem_st16(tl + T_ZB + 16 * hh, zb);
+      }
       tmem_st_wait();
       tc_fence_before();
-      // every thread of the group is done with WS (the v wait's group barrier, else a plain one)
+      // the v tile (its wait's group barrier orders the bf16 Z^T before the U product)
       if (!vzero) {
         if (!group_wait2(&bar_v, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
         pend_v = false;
@@ -955,7 +958,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       } else {
         named_sync(BAR_S, GROUP);
       }
-      if (leader) mbar_arrive(&bar_wsfree);  // WS is no longer read
       // ---------------- tcgen05: U^T = V^T G^T - Z^T G^T (M 128, N 64, K 64), which is
       // U = T Diag(beta) (V - Z), the solution of (I + A) U = Diag(beta) (V - Z)
       if (leader) {
@@ -972,6 +974,33 @@ __global__ void __launch_bounds__(THREADS, 1)
         umma_commit(&bar_G2);
       }
       pend_mma = true; last_mma = &bar_G2; last_par = ph;
+      // ---------------- while U runs: S^T <- S^T Diag(e^{Gamma_L}) (the first product read the
+      // bf16 copy; Khat^T U accumulates onto this one, after the barrier that follows U^T -> bf16).
+      // The issuing thread's warp waits while its products enter the tensor pipe, so the warp of
+      // the same lane quarter in the other half scales all 128 columns of those lanes.
+      if (lt >= 32) {
+        const bool both = lt >= 128 && lt < 160;  // lane quarter 0, second half
+        const int np = both ? 8 : 4;
+        const int cb = both ? 0 : 64 * hh;
+        uint32_t v[16];
+#pragma unroll 1
+        for (int part = 0; part < np; ++part) {
+          const int c0 = cb + 16 * part;
+          tmem_ld16(tl + T_ST + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; j += 4) {
+            const float4 gv = *reinterpret_cast<const float4*>(&gl_s[par][c0 + j]);
+            const float2 a0 = mul2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])),
+                                   make_float2(gv.x, gv.y));
+            const float2 a1 = mul2(make_float2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])),
+                                   make_float2(gv.z, gv.w));
+            v[j] = __float_as_uint(a0.x); v[j + 1] = __float_as_uint(a0.y);
+            v[j + 2] = __float_as_uint(a1.x); v[j + 3] = __float_as_uint(a1.y);
+          }
+          tmem_st16(tl + T_ST + c0, v);
+        }
+      }
       if (!group_wait2(&bar_G2, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       pend_mma = false;
       tc_fence_after();
@@ -993,9 +1022,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         v_blk = blk + 1;
       }
       // ---------------- tcgen05: O^T += U^T P^T (N 64) ; S^T += U^T Khat (N 128), K 64; P has
-      // stored this block's Khat^T by bar_khr. The two products have their own accumulators, so
-      // two threads in different warps issue them at the same time (a thread issues one MMA about
-      // every 120 cycles, whatever its size); both commit to bar_G3.
+      // stored this block's Khat^T by bar_khr. The two products have their own accumulators and
+      // are issued by two threads in different warps; both commit to bar_G3.
       if (!group_wait2(&bar_khr, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       if (leader) {
         tc_fence_after();
@@ -1040,15 +1068,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (pend_mma) (void)mbar_wait(last_mma, last_par);
         if (pend_v) (void)mbar_wait(&bar_v, v_blk & 1);
       }
-    } else if (pr.sf) {  // S_final[c'][v] from S^T (lane v): coalesced over v
-      float* sf = pr.sf + (size_t)pr.sf_i * D * D + c;
+    } else if (pr.sf && (DH == 128 || (c < DH && hh == 0))) {  // S_final[c'][v] from S^T (lane
+      // v): coalesced over v
+      float* sf = pr.sf + (size_t)pr.sf_i * DH * DH + c;
       uint32_t v[32];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         tmem_ld32(tl + T_ST + 64 * hh + 32 * half, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sf[(size_t)(64 * hh + 32 * half + j) * D] = __uint_as_float(v[j]);
+        for (int j = 0; j < 32; ++j) sf[(size_t)(64 * hh + 32 * half + j) * DH] = __uint_as_float(v[j]);
       }
     }
   }
@@ -1077,12 +1106,13 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [rows, H, 128] bf16 token tensor viewed as a 3-D map with 64 x 1 x 64 boxes, 128-byte swizzle.
-inline bool encode_token_map(CUtensorMap* m, const void* base, long long rows, int H) {
+// [rows, H, dh] bf16 token tensor (dh = 128 or 64) viewed as a 3-D map with 64 x 1 x 64 boxes,
+// 128-byte swizzle.
+inline bool encode_token_map(CUtensorMap* m, const void* base, long long rows, int H, int dh) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint64_t dims[3] = {(cuuint64_t)dh, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)dh * 2, (cuuint64_t)H * dh * 2};
   cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
@@ -1092,21 +1122,28 @@ inline bool encode_token_map(CUtensorMap* m, const void* base, long long rows, i
 
 }  // namespace tc
 
-inline bool tc_supports(int C) { return tc::tc_supports(C); }
+// Shapes the tensor-core kernel takes: bf16 with C = 64 or 128, and head size 128 (every mode)
+// or 64 (without the input and output sides).
+inline bool tc_supports(int C, int d, const SeqParams& P) {
+  return tc::tc_supports(C) &&
+         (d == 128 || (d == 64 && P.conv_q == nullptr && P.gate_u == nullptr));
+}
 
-inline kda_status_t launch_chunk_tc(const SeqParams& P, int n_problems, int C, cudaStream_t st,
+inline kda_status_t launch_chunk_tc(const SeqParams& P, int n_problems, int d, cudaStream_t st,
                                     std::string& err) {
-  (void)C;
   tc::TmaMaps maps;
   const long long rows = P.cu_seqlens ? (long long)P.T : (long long)P.n_seq * P.T;
-  if (!tc::encode_token_map(&maps.q, P.q, rows, P.H) || !tc::encode_token_map(&maps.k, P.k, rows, P.H) ||
-      !tc::encode_token_map(&maps.v, P.v, rows, P.H) || !tc::encode_token_map(&maps.g, P.g, rows, P.H)) {
+  if (!tc::encode_token_map(&maps.q, P.q, rows, P.H, d) ||
+      !tc::encode_token_map(&maps.k, P.k, rows, P.H, d) ||
+      !tc::encode_token_map(&maps.v, P.v, rows, P.H, d) ||
+      !tc::encode_token_map(&maps.g, P.g, rows, P.H, d)) {
     err = "cuTensorMapEncodeTiled failed";
     return KDA_ERR_CUDA;
   }
   const bool pre = P.conv_q != nullptr, post = P.gate_u != nullptr;
-  auto kern = pre ? (post ? tc::chunk_tc_kernel<true, true> : tc::chunk_tc_kernel<true, false>)
-                  : (post ? tc::chunk_tc_kernel<false, true> : tc::chunk_tc_kernel<false, false>);
+  auto kern = d == 64 ? tc::chunk_tc_kernel<false, false, 64>
+              : pre   ? (post ? tc::chunk_tc_kernel<true, true> : tc::chunk_tc_kernel<true, false>)
+                      : (post ? tc::chunk_tc_kernel<false, true> : tc::chunk_tc_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)tc::SMEM_ALLOC);
   if (e != cudaSuccess) {
