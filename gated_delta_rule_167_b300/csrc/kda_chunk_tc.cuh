@@ -76,6 +76,10 @@ constexpr int BAR_P = 1, BAR_S = 2;  // hardware barrier ids of the groups
 constexpr int BAR_PAIR0 = 3;        // ids 3..6: pairs of warps of the state group in its solve
 constexpr float LOG2E = 1.4426950408889634f;
 
+// Row stride (floats) of the fp32 64 x 64 solve workspace: 76 puts the eight 16-byte rows of a
+// matrix load, and the rows of a warp's 16-byte stores, in distinct banks.
+constexpr int WLD = 76;
+
 // ---- shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t IN_K = 0;           // k tile (two 64-channel boxes of [64 tokens][64])
 constexpr uint32_t IN_Q = 16384;       // q tile
@@ -89,8 +93,8 @@ constexpr uint32_t YP = XQ + 16384;    // [Y_B | Y_A], N = 96 columns in 2 MN-ma
 // odd blocks [(K e^Gamma)^T | (Q e^Gamma)^T] -> [Z^T | O^T]
 constexpr uint32_t KQ = YP + 32768;    // 2 x 16 KB
 constexpr uint32_t KH = KQ + 32768;    // Khat^T [c][r]: K-major B of S^T += U^T Khat
-constexpr uint32_t WS = KH + 16384;    // fp32 A, then T ([64][WLD], 18 KB)
-constexpr uint32_t PT = WS + 18432;    // P [r][j], K-major B of O^T += U^T P^T, 2 x 8 KB by parity
+constexpr uint32_t WS = KH + 16384;    // fp32 A, then T ([64][WLD], 19 KB)
+constexpr uint32_t PT = WS + 64 * WLD * 4;  // P [r][j], K-major B of O^T += U^T P^T, 2 x 8 KB by parity
 constexpr uint32_t GB = PT + 16384;    // G = T Diag(beta) [r][j] bf16, K-major B of U^T (8 KB)
 constexpr uint32_t SMEM_BYTES = GB + 8192;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for aligning the base
@@ -112,9 +116,6 @@ constexpr uint32_t T_UB = T_ZB;  // U^T bf16 (A operand), over Z^T bf16 once the
 // Columns of the A/P product: Y_B (reference rho_B) at 0..63, Y_A (rho_A) at 64..95.
 constexpr int Y_A = 64;
 
-// Row stride (floats) of the fp32 64 x 64 solve workspace: 72 makes the tf32 B-fragment loads
-// (rows t, columns g) conflict-free.
-constexpr int WLD = 72;
 constexpr int TLD = 20;  // row stride (floats) of the diagonal inverses
 struct TmaMaps {
   CUtensorMap q, k, v, g;
