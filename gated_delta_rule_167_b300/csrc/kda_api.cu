@@ -339,7 +339,8 @@ kda_status_t kda_pre_core(const void* q_raw, const void* k_raw, const void* v_ra
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int tok_per_cta = 4 * (256 / (d / 8));
   const long long tiles = (rows + tok_per_cta - 1) / tok_per_cta;
-  const dim3 grid((unsigned)H, (unsigned)(tiles < 65535 ? tiles : 65535));  // the kernel strides over tiles
+  // (head, tile, output tensor); the kernel strides over tiles
+  const dim3 grid((unsigned)H, (unsigned)(tiles < 65535 ? tiles : 65535), 4);
   using bf = __nv_bfloat16;
   if (d == 128) {
     if (dtype == KDA_DTYPE_BF16) kda::pre::pre_core_kernel<bf, 128><<<grid, 256, 0, st>>>(P, rows);

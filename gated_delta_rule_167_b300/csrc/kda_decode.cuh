@@ -20,6 +20,7 @@
 #pragma once
 
 #include "kda_common.cuh"
+#include "kda_sm100.cuh"
 
 namespace kda {
 
@@ -126,10 +127,12 @@ namespace kda {
 // decode_step_kernel applied K times while the CTA's slice of S stays in registers, so S is read
 // from and written to HBM once whatever K is (speculative verification of K draft tokens, or
 // any short run of tokens). Inputs are [N, K, H, d] (token t of sequence n at (n K + t) H + h);
-// out receives o for every token. Per token: the read-out reductions go through shared memory
-// (one barrier each), as in the single-step kernel.
+// out receives o for every token. The inputs of up to KB tokens are staged in shared memory in
+// one go (their loads overlap the state loads instead of following each token), with the q . k
+// products of the staged tokens; then each token takes one barrier: the two column reductions
+// go through shared arrays alternating by token parity.
 template <typename TIn, int DK, int DV, int THREADS>
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(THREADS, 2)
     decode_tokens_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                          const TIn* __restrict__ v, const TIn* __restrict__ g,
                          const TIn* __restrict__ beta, float* __restrict__ S,
@@ -137,88 +140,102 @@ __global__ void __launch_bounds__(THREADS)
   constexpr int CG = DV / 4;
   constexpr int RG = THREADS / CG;
   constexpr int RPT = DK / RG;
+  constexpr int KB = 8;  // tokens staged per pass
   static_assert(DV % 4 == 0 && THREADS % CG == 0 && DK % RG == 0, "bad decode tiling");
 
-  __shared__ float s_alpha[DK], s_k[DK], s_ak[DK], s_aq[DK], s_q[DK];
-  __shared__ float4 s_redc[RG][CG];
-  __shared__ float4 s_redp[RG][CG];
-  __shared__ float s_qk;
+  __shared__ float s_alpha[KB][DK], s_k[KB][DK], s_q[KB][DK];
+  __shared__ float4 s_v[KB][CG];
+  __shared__ float s_beta[KB], s_qk[KB];
+  __shared__ float4 s_redc[2][RG][CG];
+  __shared__ float4 s_redp[2][RG][CG];
 
   const int p = blockIdx.x;  // n * H + h
   const int n = p / H, h = p % H;
   const int tid = threadIdx.x;
   const int cg = tid % CG;
   const int rg = tid / CG;
+  auto token_row = [&](int t) { return ((size_t)n * K + t) * H + h; };
 
   float4* Sp = reinterpret_cast<float4*>(S + (size_t)p * DK * DV);
   float4 s[RPT];
 #pragma unroll
   for (int i = 0; i < RPT; ++i) s[i] = __ldcs(&Sp[(rg * RPT + i) * CG + cg]);
 
-  for (int t = 0; t < K; ++t) {
-    const size_t tok = ((size_t)n * K + t) * H + h;  // token row of (n, t, h)
-    if (t > 0) __syncthreads();  // the previous token's shared arrays are no longer read
-    for (int i = tid; i < DK; i += THREADS) {
-      const float a = expf(to_f32(g[tok * DK + i]));
-      const float kk = to_f32(k[tok * DK + i]);
-      const float qq = to_f32(q[tok * DK + i]);
-      s_alpha[i] = a;
-      s_k[i] = kk;
-      s_q[i] = qq;
-      s_ak[i] = a * kk;
-      s_aq[i] = a * qq;
+  for (int t0 = 0; t0 < K; t0 += KB) {
+    const int kn = min(KB, K - t0);
+    if (t0 > 0) __syncthreads();  // the previous pass's staged inputs are no longer read
+    for (int e = tid; e < kn * DK; e += THREADS) {
+      const int tt = e / DK, i = e % DK;
+      const size_t o = token_row(t0 + tt) * DK + i;
+      s_alpha[tt][i] = expf(to_f32(g[o]));
+      s_k[tt][i] = to_f32(k[o]);
+      s_q[tt][i] = to_f32(q[o]);
     }
+    for (int e = tid; e < kn * CG; e += THREADS) {
+      const int tt = e / CG, j = e % CG;
+      const TIn* vp = v + token_row(t0 + tt) * DV + 4 * j;
+      s_v[tt][j] = make_float4(to_f32(vp[0]), to_f32(vp[1]), to_f32(vp[2]), to_f32(vp[3]));
+    }
+    if (tid < kn) s_beta[tid] = to_f32(beta[token_row(t0 + tid)]);
     __syncthreads();
-    float4 c = make_float4(0.f, 0.f, 0.f, 0.f), pq = c;
-#pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-      const int r = rg * RPT + i;
-      const float ak = s_ak[r], aq = s_aq[r];
-      c.x = fmaf(ak, s[i].x, c.x); c.y = fmaf(ak, s[i].y, c.y);
-      c.z = fmaf(ak, s[i].z, c.z); c.w = fmaf(ak, s[i].w, c.w);
-      pq.x = fmaf(aq, s[i].x, pq.x); pq.y = fmaf(aq, s[i].y, pq.y);
-      pq.z = fmaf(aq, s[i].z, pq.z); pq.w = fmaf(aq, s[i].w, pq.w);
-    }
-    s_redc[rg][cg] = c;
-    s_redp[rg][cg] = pq;
-    if (tid < 32) {
+    for (int tt = tid >> 5; tt < kn; tt += THREADS / 32) {  // q . k, one warp per token
       float acc = 0.f;
-      for (int i = tid; i < DK; i += 32) acc = fmaf(s_q[i], s_k[i], acc);
+      for (int i = tid & 31; i < DK; i += 32) acc = fmaf(s_q[tt][i], s_k[tt][i], acc);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (tid == 0) s_qk = acc;
+      if ((tid & 31) == 0) s_qk[tt] = acc;
     }
-    __syncthreads();
-    float4 C = make_float4(0.f, 0.f, 0.f, 0.f), Pq = C;
+    for (int tt = 0; tt < kn; ++tt) {
+      const int pb = (t0 + tt) & 1;
+      // column sums over this thread's rows, on fp32 pairs: c = (alpha k)^T S, pq = (alpha q)^T S
+      float2 c01 = make_float2(0.f, 0.f), c23 = c01, p01 = c01, p23 = c01;
 #pragma unroll
-    for (int r = 0; r < RG; ++r) {
-      const float4 a = s_redc[r][cg], b = s_redp[r][cg];
-      C.x += a.x; C.y += a.y; C.z += a.z; C.w += a.w;
-      Pq.x += b.x; Pq.y += b.y; Pq.z += b.z; Pq.w += b.w;
-    }
-    const float bt = to_f32(beta[tok]);
-    const TIn* vp = v + tok * DV + 4 * cg;
-    float4 d;  // beta (v - c)
-    d.x = bt * (to_f32(vp[0]) - C.x);
-    d.y = bt * (to_f32(vp[1]) - C.y);
-    d.z = bt * (to_f32(vp[2]) - C.z);
-    d.w = bt * (to_f32(vp[3]) - C.w);
+      for (int i = 0; i < RPT; ++i) {
+        const int r = rg * RPT + i;
+        const float a = s_alpha[tt][r];
+        const float ak = a * s_k[tt][r], aq = a * s_q[tt][r];
+        const float2 s01 = make_float2(s[i].x, s[i].y), s23 = make_float2(s[i].z, s[i].w);
+        c01 = sm100::fma2(make_float2(ak, ak), s01, c01);
+        c23 = sm100::fma2(make_float2(ak, ak), s23, c23);
+        p01 = sm100::fma2(make_float2(aq, aq), s01, p01);
+        p23 = sm100::fma2(make_float2(aq, aq), s23, p23);
+      }
+      s_redc[pb][rg][cg] = make_float4(c01.x, c01.y, c23.x, c23.y);
+      s_redp[pb][rg][cg] = make_float4(p01.x, p01.y, p23.x, p23.y);
+      __syncthreads();
+      float4 C = make_float4(0.f, 0.f, 0.f, 0.f), Pq = C;
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-      const int r = rg * RPT + i;
-      const float a = s_alpha[r], kk = s_k[r];
-      s[i].x = fmaf(kk, d.x, a * s[i].x);
-      s[i].y = fmaf(kk, d.y, a * s[i].y);
-      s[i].z = fmaf(kk, d.z, a * s[i].z);
-      s[i].w = fmaf(kk, d.w, a * s[i].w);
-    }
-    if (rg == 0) {
-      const float qk = s_qk;
-      TIn* op = out + tok * DV + 4 * cg;
-      op[0] = from_f32<TIn>(fmaf(qk, d.x, Pq.x));
-      op[1] = from_f32<TIn>(fmaf(qk, d.y, Pq.y));
-      op[2] = from_f32<TIn>(fmaf(qk, d.z, Pq.z));
-      op[3] = from_f32<TIn>(fmaf(qk, d.w, Pq.w));
+      for (int r = 0; r < RG; ++r) {
+        const float4 a = s_redc[pb][r][cg], b = s_redp[pb][r][cg];
+        C.x += a.x; C.y += a.y; C.z += a.z; C.w += a.w;
+        Pq.x += b.x; Pq.y += b.y; Pq.z += b.z; Pq.w += b.w;
+      }
+      const float bt = s_beta[tt];
+      const float4 vv = s_v[tt][cg];
+      float4 d;  // beta (v - c)
+      d.x = bt * (vv.x - C.x);
+      d.y = bt * (vv.y - C.y);
+      d.z = bt * (vv.z - C.z);
+      d.w = bt * (vv.w - C.w);
+      const float2 d01 = make_float2(d.x, d.y), d23 = make_float2(d.z, d.w);
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {  // S <- Diag(alpha) S + k d^T
+        const int r = rg * RPT + i;
+        const float a = s_alpha[tt][r], kk = s_k[tt][r];
+        const float2 x01 = sm100::fma2(make_float2(kk, kk), d01,
+                                       sm100::mul2(make_float2(a, a), make_float2(s[i].x, s[i].y)));
+        const float2 x23 = sm100::fma2(make_float2(kk, kk), d23,
+                                       sm100::mul2(make_float2(a, a), make_float2(s[i].z, s[i].w)));
+        s[i] = make_float4(x01.x, x01.y, x23.x, x23.y);
+      }
+      if (rg == 0) {
+        const float qk = s_qk[tt];
+        TIn* op = out + token_row(t0 + tt) * DV + 4 * cg;
+        op[0] = from_f32<TIn>(fmaf(qk, d.x, Pq.x));
+        op[1] = from_f32<TIn>(fmaf(qk, d.y, Pq.y));
+        op[2] = from_f32<TIn>(fmaf(qk, d.z, Pq.z));
+        op[3] = from_f32<TIn>(fmaf(qk, d.w, Pq.w));
+      }
     }
   }
 #pragma unroll

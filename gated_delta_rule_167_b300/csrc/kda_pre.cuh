@@ -121,71 +121,102 @@ __device__ __forceinline__ void l2norm8(float (&x)[8]) {
   for (int e = 0; e < 8; ++e) x[e] *= inv;
 }
 
-// Standalone kernel: one CTA per (head, tile of 4 * 256 / (D / 8) tokens), heads fastest, so that
-// the CTAs resident at one time read neighbouring heads of the same tokens (contiguous memory);
-// D / 8 threads per token row, 8 channels and 4 consecutive tokens per thread, so each thread
-// reads the 7 rows it needs once per tensor (the rows shared with neighbouring threads hit L1).
+// Standalone kernel: one CTA per (head, tile of 4 * 256 / (D / 8) tokens, output tensor), heads
+// fastest, so that the CTAs resident at one time read neighbouring heads of the same tokens
+// (contiguous memory); blockIdx.z picks q, k, v (convolution, and the norm for q and k) or g
+// (the decay gate), so that a thread holds one tensor's rows and many CTAs fit on an SM. D / 8
+// threads per token row, 8 channels and 4 consecutive tokens per thread: each thread reads the
+// 7 rows it needs once (the rows shared with neighbouring threads hit L1).
 template <typename TIn, int D>
 __global__ void __launch_bounds__(256) pre_core_kernel(PreParams P, long long n_tok) {
   constexpr int TPR = D / 8;            // threads per token row
   constexpr int TOK = 4 * (256 / TPR);  // tokens per CTA
   const int h = blockIdx.x;
+  const int ts = blockIdx.z;  // 0 q, 1 k, 2 v, 3 g
   const int cg = threadIdx.x % TPR, rg = threadIdx.x / TPR;
   const int c0 = 8 * cg;
   const int H = P.H;
   const long long n_tiles = (n_tok + TOK - 1) / TOK;
   for (long long tile = blockIdx.y; tile < n_tiles; tile += gridDim.y) {
-  const long long tok0 = tile * TOK + 4 * rg;  // first of this thread's tokens
-  int pos[4];
-  bool live[4];
+    const long long tok0 = tile * TOK + 4 * rg;  // first of this thread's tokens
+    bool live[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    live[i] = tok0 + i < n_tok;
-    pos[i] = live[i] ? position_in_sequence(P, tok0 + i) : 0;
-  }
-  const void* raws[3] = {P.q_raw, P.k_raw, P.v_raw};
-  const float* ws[3] = {P.conv_q, P.conv_k, P.conv_v};
-  void* outs[3] = {P.q, P.k, P.v};
-#pragma unroll
-  for (int ts = 0; ts < 3; ++ts) {
-    float t[4][8], x[7][8], y[4][8];
-    load_taps<D>(ws[ts], h, c0, t);
-    const TIn* src = static_cast<const TIn*>(raws[ts]);
-#pragma unroll
-    for (int m = 0; m < 7; ++m) {
-      const long long r = tok0 + m - 3;
-      if (r >= 0 && r < n_tok) {
-        load8(src + ((size_t)r * H + h) * D + c0, x[m]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[m][e] = 0.f;
+    for (int i = 0; i < 4; ++i) live[i] = tok0 + i < n_tok;
+    if (ts == 3) {  // the decay gate
+      const float eA = expf(P.A_log[h]);
+      float b8[8];
+      {
+        const float4* bp = reinterpret_cast<const float4*>(P.b_decay + (size_t)h * D + c0);
+        const float4 a = bp[0], b = bp[1];
+        b8[0] = a.x; b8[1] = a.y; b8[2] = a.z; b8[3] = a.w; b8[4] = b.x; b8[5] = b.y; b8[6] = b.z; b8[7] = b.w;
       }
+      float z[4][8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (live[i]) load8(static_cast<const TIn*>(P.z) + ((size_t)(tok0 + i) * H + h) * D + c0, z[i]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (!live[i]) continue;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) z[i][e] = decay_gate<TIn>(z[i][e], eA, b8[e]);
+        store8(static_cast<TIn*>(P.g) + ((size_t)(tok0 + i) * H + h) * D + c0, z[i]);
+      }
+      continue;
     }
-    conv4x8(t, x, pos, y);
+    int pos[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pos[i] = live[i] ? position_in_sequence(P, tok0 + i) : 0;
+    const TIn* src = static_cast<const TIn*>(ts == 0 ? P.q_raw : (ts == 1 ? P.k_raw : P.v_raw));
+    const float* w = ts == 0 ? P.conv_q : (ts == 1 ? P.conv_k : P.conv_v);
+    TIn* dst = static_cast<TIn*>(ts == 0 ? P.q : (ts == 1 ? P.k : P.v));
+    float t[4][8], y[4][8];
+    if constexpr (sizeof(TIn) == 2) {  // rows kept packed (bf16 pairs) until used
+      uint4 xr[7];
+#pragma unroll
+      for (int m = 0; m < 7; ++m) {  // every load is issued before any arithmetic
+        const long long r = tok0 + m - 3;
+        xr[m] = (r >= 0 && r < n_tok)
+                    ? *reinterpret_cast<const uint4*>(src + ((size_t)r * H + h) * D + c0)
+                    : make_uint4(0, 0, 0, 0);
+      }
+      load_taps<D>(w, h, c0, t);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float xe[7];
+#pragma unroll
+        for (int m = 0; m < 7; ++m) {
+          const uint32_t wd = e < 2 ? xr[m].x : (e < 4 ? xr[m].y : (e < 6 ? xr[m].z : xr[m].w));
+          xe[m] = __uint_as_float((e & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float a = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (j <= pos[i]) a = fmaf(t[j][e], xe[i + 3 - j], a);
+          y[i][e] = a;
+        }
+      }
+    } else {
+      float x[7][8];
+#pragma unroll
+      for (int m = 0; m < 7; ++m) {  // every load is issued before any arithmetic
+        const long long r = tok0 + m - 3;
+        if (r >= 0 && r < n_tok) {
+          load8(src + ((size_t)r * H + h) * D + c0, x[m]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[m][e] = 0.f;
+        }
+      }
+      load_taps<D>(w, h, c0, t);
+      conv4x8(t, x, pos, y);
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       if (ts < 2) l2norm8<D, sizeof(TIn) == 4>(y[i]);  // every lane of the row joins
-      if (live[i]) store8(static_cast<TIn*>(outs[ts]) + ((size_t)(tok0 + i) * H + h) * D + c0, y[i]);
+      if (live[i]) store8(dst + ((size_t)(tok0 + i) * H + h) * D + c0, y[i]);
     }
-  }
-  // the decay gate
-  const float eA = expf(P.A_log[h]);
-  float b8[8];
-  {
-    const float4* bp = reinterpret_cast<const float4*>(P.b_decay + (size_t)h * D + c0);
-    const float4 a = bp[0], b = bp[1];
-    b8[0] = a.x; b8[1] = a.y; b8[2] = a.z; b8[3] = a.w; b8[4] = b.x; b8[5] = b.y; b8[6] = b.z; b8[7] = b.w;
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (!live[i]) continue;
-    const size_t o = ((size_t)(tok0 + i) * H + h) * D + c0;
-    float z[8];
-    load8(static_cast<const TIn*>(P.z) + o, z);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) z[e] = decay_gate<TIn>(z[e], eA, b8[e]);
-    store8(static_cast<TIn*>(P.g) + o, z);
-  }
   }  // tiles
 }
 

@@ -320,6 +320,16 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   return *reinterpret_cast<float2*>(&r);
 }
 
+// a * b + c on fp32 pairs, each rounded once (PTX fma.rn.f32x2).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+        "l"(*reinterpret_cast<uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&r);
+}
+
 // ---------------------------------------------------------------- small fp32 products
 // Warp-level m16n8k8 tf32 MMA (fp32 accumulation). Fragment layout, g = lane / 4, t = lane % 4:
 //   A (16 x 8, row-major): a0 (g, t), a1 (g + 8, t), a2 (g, t + 4), a3 (g + 8, t + 4)
