@@ -59,7 +59,7 @@ def _peaks():
 # unchanged).
 PREFILL_SOURCES = ("kda_chunk_tc.cuh", "kda_chunk_simt.cuh", "kda_sm100.cuh", "kda_common.cuh",
                    "kda_pre.cuh", "kda_post.cuh")
-DECODE_SOURCES = ("kda_decode.cuh", "kda_common.cuh")
+DECODE_SOURCES = ("kda_decode.cuh", "kda_common.cuh", "kda_sm100.cuh")
 
 
 def _kernel_source_hash(sources=PREFILL_SOURCES):
@@ -398,6 +398,26 @@ def _timed_flushed(fn, steps, warmup, device, stream):
     return sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps, cs.summary()
 
 
+def _as_graph(fn, device):
+    """Captures fn (which launches on torch's current stream) into a CUDA graph, so that a timed
+    replay is one launch from the host; None if capture is not possible here."""
+    try:
+        side = torch.cuda.Stream(device)
+        side.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream(device).wait_stream(side)
+        torch.cuda.synchronize(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            fn()
+        torch.cuda.synchronize(device)
+        return graph
+    except Exception:  # capture refused: time the direct calls instead
+        torch.cuda.synchronize(device)
+        return None
+
+
 def bench_small(kda, args, world, rank, device, stream, peaks, steps=20):
     """B=1, H=8, T=4096: eight (sequence, head) problems, far fewer than the SMs. Timed as the
     plain prefill (one CTA per problem) and segment-parallel along T (automatic segments)."""
@@ -413,25 +433,34 @@ def bench_small(kda, args, world, rank, device, stream, peaks, steps=20):
                      dtype=torch.uint8, device=device)
 
     def plain():
-        kda.kda_chunk_fwd(q, k, v, g, b, S0, out, Sf, C=C, stream=stream)
+        kda.kda_chunk_fwd(q, k, v, g, b, S0, out, Sf, C=C,
+                          stream=torch.cuda.current_stream(device))
 
     def seg():
-        kda.kda_chunk_fwd_segmented(q, k, v, g, b, S0, out, Sf, n_seg, ws, C=C, stream=stream)
+        kda.kda_chunk_fwd_segmented(q, k, v, g, b, S0, out, Sf, n_seg, ws, C=C,
+                                    stream=torch.cuda.current_stream(device))
 
-    ms_plain, _ = _timed_flushed(plain, steps, 3, device, stream)
-    ms_seg, clocks = _timed_flushed(seg, steps, 3, device, stream)
+    # A call is 0.1-0.3 ms of device work: replayed from a CUDA graph, so that the host's
+    # launch work (argument checks, tensor-map encodes) cannot leave gaps inside the timed span.
+    graphs = {name: _as_graph(fn, device) for name, fn in (("plain", plain), ("seg", seg))}
+    run = {name: (graphs[name].replay if graphs[name] is not None else fn)
+           for name, fn in (("plain", plain), ("seg", seg))}
+    ms_plain, _ = _timed_flushed(run["plain"], steps, 3, device, stream)
+    ms_seg, clocks = _timed_flushed(run["seg"], steps, 3, device, stream)
     kda.kda_sync_status(stream)
+    launch = ("CUDA graph replay" if all(gr is not None for gr in graphs.values())
+              else "direct calls (graph capture unavailable)")
     token_heads = B * T * H
     alg = token_heads * BYTES_PER_TOKEN_HEAD + 2 * B * H * STATE_BYTES  # S0 read, S_final written
     gbs = alg / (ms_seg * 1e-3) / 1e9
-    del inp, q, k, v, g, b, S0, out, ws
+    del inp, q, k, v, g, b, S0, out, ws, graphs, run
     torch.cuda.empty_cache()
     return {"workload": w["name"], "n_seg": n_seg, "ms_per_step": ms_seg,
             "ms_per_step_unsegmented": ms_plain, "tokens_per_s": world * B * T / (ms_seg * 1e-3),
             "tokens_per_s_unsegmented": world * B * T / (ms_plain * 1e-3),
             "tflops": token_heads * useful_flops_per_token_head(C) / (ms_seg * 1e-3) / 1e12,
             "l2": "flushed before every timed iteration (256 MiB write outside the timed span)",
-            "clocks": clocks,
+            "launch": launch, "clocks": clocks,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm"], "traffic": None,
                          "algorithmic_bytes_per_launch": alg,
@@ -582,7 +611,8 @@ def bench_decode_tokens(kda, args, world, rank, device, stream, peaks, K=4, call
     return {"workload": f"decode_bf16_N{N}_H{H}_K{K}", "K": K, "ms_per_call": ms,
             "tokens_per_s": world * N * K / (ms * 1e-3), "clocks": clocks,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
-                         "frac": gbs / peaks["hbm"], "traffic": None,
+                         "frac": gbs / peaks["hbm"],
+                         "traffic": _recorded_traffic(f"decode_tokens_bf16_N{N}_H{H}_K{K}"),
                          "algorithmic_bytes_per_launch": bytes_call}}
 
 
@@ -607,7 +637,8 @@ def bench_nano(kda, args, world, rank, device, stream, peaks, steps=5):
             "tflops": B * T * H * useful_flops_per_token_head(C, d, d) / (ms * 1e-3) / 1e12,
             "clocks": clocks,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
-                         "frac": gbs / peaks["hbm"], "traffic": None,
+                         "frac": gbs / peaks["hbm"],
+                         "traffic": _recorded_traffic(f"nano_bf16_B{B}_H{H}_T{T}_d{d}"),
                          "algorithmic_bytes_per_launch": alg}}
 
 
