@@ -604,7 +604,8 @@ kda_status_t kda_recurrent_steps(const void* q, const void* k, const void* v, co
   if (s != KDA_OK) return s;
   if (N < 0 || K < 0) return fail(KDA_ERR_INVALID_ARG, "N and K must be >= 0 (got %d, %d)", N, K);
   if (N == 0 || K == 0) return KDA_OK;
-  if ((long long)N * H >= (1ll << 31) || (long long)N * K * H * d_k >= (1ll << 40))
+  // two CTAs per (sequence, head) at d = 128: N * H * 2 must stay a valid grid size
+  if ((long long)N * H >= (1ll << 30) || (long long)N * K * H * d_k >= (1ll << 40))
     return fail(KDA_ERR_UNSUPPORTED, "problem too large");
   if ((s = check_ptr(q, "q", true)) || (s = check_ptr(k, "k", true)) ||
       (s = check_ptr(v, "v", true)) || (s = check_ptr(g, "g", true)) ||
@@ -618,16 +619,16 @@ kda_status_t kda_recurrent_steps(const void* q, const void* k, const void* v, co
     const float *qq = (const float*)q, *kk = (const float*)k, *vv = (const float*)v,
                 *gg = (const float*)g, *bb = (const float*)beta;
     if (d_k == 128)
-      kda::decode_tokens_kernel<float, 128, 128, 256><<<grid, 256, 0, st>>>(qq, kk, vv, gg, bb, S, (float*)out, K, H);
+      kda::decode_tokens_kernel<float, 128, 128, 64, 128><<<grid * 2, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (float*)out, K, H);
     else
-      kda::decode_tokens_kernel<float, 64, 64, 128><<<grid, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (float*)out, K, H);
+      kda::decode_tokens_kernel<float, 64, 64, 64, 128><<<grid, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (float*)out, K, H);
   } else {
     const bf *qq = (const bf*)q, *kk = (const bf*)k, *vv = (const bf*)v, *gg = (const bf*)g,
              *bb = (const bf*)beta;
     if (d_k == 128)
-      kda::decode_tokens_kernel<bf, 128, 128, 256><<<grid, 256, 0, st>>>(qq, kk, vv, gg, bb, S, (bf*)out, K, H);
+      kda::decode_tokens_kernel<bf, 128, 128, 64, 128><<<grid * 2, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (bf*)out, K, H);
     else
-      kda::decode_tokens_kernel<bf, 64, 64, 128><<<grid, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (bf*)out, K, H);
+      kda::decode_tokens_kernel<bf, 64, 64, 64, 128><<<grid, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (bf*)out, K, H);
   }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "decode_tokens launch");

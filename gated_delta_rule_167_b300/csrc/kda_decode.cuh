@@ -130,18 +130,22 @@ namespace kda {
 // out receives o for every token. The inputs of up to KB tokens are staged in shared memory in
 // one go (their loads overlap the state loads instead of following each token), with the q . k
 // products of the staged tokens; then each token takes one barrier: the two column reductions
-// go through shared arrays alternating by token parity.
-template <typename TIn, int DK, int DV, int THREADS>
-__global__ void __launch_bounds__(THREADS, 2)
+// go through shared arrays alternating by token parity. The value columns are independent (the
+// reductions run over the key channel), so a CTA takes DVC of the DV columns of one (sequence,
+// head): CTAs of 128 threads with 32 KiB of state each keep four in flight per SM.
+template <typename TIn, int DK, int DV, int DVC, int THREADS>
+__global__ void __launch_bounds__(THREADS, 512 / THREADS)
     decode_tokens_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                          const TIn* __restrict__ v, const TIn* __restrict__ g,
                          const TIn* __restrict__ beta, float* __restrict__ S,
                          TIn* __restrict__ out, int K, int H) {
-  constexpr int CG = DV / 4;
+  constexpr int CG = DVC / 4;      // float4 column groups per CTA
   constexpr int RG = THREADS / CG;
   constexpr int RPT = DK / RG;
   constexpr int KB = 8;  // tokens staged per pass
-  static_assert(DV % 4 == 0 && THREADS % CG == 0 && DK % RG == 0, "bad decode tiling");
+  constexpr int NSPLIT = DV / DVC;  // CTAs per (sequence, head)
+  static_assert(DVC % 4 == 0 && DV % DVC == 0 && THREADS % CG == 0 && DK % RG == 0,
+                "bad decode tiling");
 
   __shared__ float s_alpha[KB][DK], s_k[KB][DK], s_q[KB][DK];
   __shared__ float4 s_v[KB][CG];
@@ -149,17 +153,20 @@ __global__ void __launch_bounds__(THREADS, 2)
   __shared__ float4 s_redc[2][RG][CG];
   __shared__ float4 s_redp[2][RG][CG];
 
-  const int p = blockIdx.x;  // n * H + h
+  const int p = blockIdx.x / NSPLIT;  // n * H + h
+  const int c_off = (blockIdx.x % NSPLIT) * DVC;  // first value column of this CTA
   const int n = p / H, h = p % H;
   const int tid = threadIdx.x;
   const int cg = tid % CG;
   const int rg = tid / CG;
   auto token_row = [&](int t) { return ((size_t)n * K + t) * H + h; };
 
-  float4* Sp = reinterpret_cast<float4*>(S + (size_t)p * DK * DV);
+  // row r, column group j of this CTA's columns: float4 r * (DV / 4) + (c_off / 4) + j
+  float4* Sp = reinterpret_cast<float4*>(S + (size_t)p * DK * DV + c_off);
+  constexpr int ROW4 = DV / 4;
   float4 s[RPT];
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) s[i] = __ldcs(&Sp[(rg * RPT + i) * CG + cg]);
+  for (int i = 0; i < RPT; ++i) s[i] = __ldcs(&Sp[(rg * RPT + i) * ROW4 + cg]);
 
   for (int t0 = 0; t0 < K; t0 += KB) {
     const int kn = min(KB, K - t0);
@@ -173,7 +180,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     for (int e = tid; e < kn * CG; e += THREADS) {
       const int tt = e / CG, j = e % CG;
-      const TIn* vp = v + token_row(t0 + tt) * DV + 4 * j;
+      const TIn* vp = v + token_row(t0 + tt) * DV + c_off + 4 * j;
       s_v[tt][j] = make_float4(to_f32(vp[0]), to_f32(vp[1]), to_f32(vp[2]), to_f32(vp[3]));
     }
     if (tid < kn) s_beta[tid] = to_f32(beta[token_row(t0 + tid)]);
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       }
       if (rg == 0) {
         const float qk = s_qk[tt];
-        TIn* op = out + token_row(t0 + tt) * DV + 4 * cg;
+        TIn* op = out + token_row(t0 + tt) * DV + c_off + 4 * cg;
         op[0] = from_f32<TIn>(fmaf(qk, d.x, Pq.x));
         op[1] = from_f32<TIn>(fmaf(qk, d.y, Pq.y));
         op[2] = from_f32<TIn>(fmaf(qk, d.z, Pq.z));
@@ -239,7 +246,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
   }
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) __stcs(&Sp[(rg * RPT + i) * CG + cg], s[i]);
+  for (int i = 0; i < RPT; ++i) __stcs(&Sp[(rg * RPT + i) * ROW4 + cg], s[i]);
 }
 
 }  // namespace kda

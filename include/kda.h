@@ -57,9 +57,10 @@ typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype_t;
  *   S_final : [B, H, d_k, d_v] fp32, written with the state after token T; NULL = not written
  *   C       : chunk size (16, 32, 64 or 128); the result does not depend on it beyond rounding
  * fp32 inputs run on CUDA cores in fp32 throughout, in 16- or 32-token blocks. bf16 inputs run
- * on the tensor cores (bf16 operands, fp32 accumulation, fp32 state) when d_k = d_v = 128 and
- * C is 64 or 128; that kernel works in 64-token blocks, so a 128-token chunk is processed as
- * two consecutive 64-token blocks (the same mathematics).
+ * on the tensor cores (bf16 operands, fp32 accumulation, fp32 state) when C is 64 or 128; that
+ * kernel works in 64-token blocks, so a 128-token chunk is processed as two consecutive 64-token
+ * blocks (the same mathematics), and in 128-channel tiles, so a head of 64 channels runs with
+ * the upper half of every tile zero (the results are those of the 64-channel problem).
  */
 kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g,
                            const void* beta, const float* S0, void* out, float* S_final,
@@ -101,7 +102,8 @@ kda_status_t kda_recurrent_step(const void* q, const void* k, const void* v, con
  * speculative draft tokens, or a short run of tokens).
  *   q, k, g : [N, K, H, d_k] dtype   v, out : [N, K, H, d_v] dtype   beta : [N, K, H] dtype
  *   S       : [N, H, d_k, d_v] fp32, read and overwritten with the state after the K tokens
- * out receives o_t = S_t^T q_t for every token. K = 1 gives kda_recurrent_step.
+ * out receives o_t = S_t^T q_t for every token. K = 1 gives kda_recurrent_step. N * H must be
+ * below 2^30 (KDA_ERR_UNSUPPORTED otherwise).
  */
 kda_status_t kda_recurrent_steps(const void* q, const void* k, const void* v, const void* g,
                                  const void* beta, float* S, void* out, int N, int K, int H,
