@@ -66,13 +66,13 @@ kda_status_t launch_simt(const kda::SeqParams& P, int n_problems, int C, cudaStr
   if (C == 16) {
     using SM = kda::SimtSmem<D, D, 16>;
     auto kern = kda::chunk_simt_kernel<TIn, D, D, 16, THREADS>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM::bytes);
+    e = kda::ensure_smem_limit(reinterpret_cast<const void*>(kern), (int)SM::bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(chunk_simt)");
     kern<<<n_problems, THREADS, SM::bytes, st>>>(P);
   } else {
     using SM = kda::SimtSmem<D, D, 32>;
     auto kern = kda::chunk_simt_kernel<TIn, D, D, 32, THREADS>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM::bytes);
+    e = kda::ensure_smem_limit(reinterpret_cast<const void*>(kern), (int)SM::bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(chunk_simt)");
     kern<<<n_problems, THREADS, SM::bytes, st>>>(P);
   }
@@ -102,13 +102,13 @@ kda_status_t launch_scan(const float* M, const float* St, const float* S0, float
   if (d == 128) {
     auto kern = kda::scan::segment_scan_kernel<128, 128>;
     const int bytes = (int)kda::scan::ScanSmem<128>::bytes;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = kda::ensure_smem_limit(reinterpret_cast<const void*>(kern), bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(segment_scan)");
     kern<<<grid, kda::scan::THREADS, bytes, st>>>(M, St, S0, S_in, n_seg, BH);
   } else {
     auto kern = kda::scan::segment_scan_kernel<64, 64>;
     const int bytes = (int)kda::scan::ScanSmem<64>::bytes;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = kda::ensure_smem_limit(reinterpret_cast<const void*>(kern), bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(segment_scan)");
     kern<<<grid, kda::scan::THREADS, bytes, st>>>(M, St, S0, S_in, n_seg, BH);
   }

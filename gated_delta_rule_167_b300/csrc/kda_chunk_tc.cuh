@@ -1145,8 +1145,7 @@ inline kda_status_t launch_chunk_tc(const SeqParams& P, int n_problems, int d, c
   auto kern = d == 64 ? tc::chunk_tc_kernel<false, false, 64>
               : pre   ? (post ? tc::chunk_tc_kernel<true, true> : tc::chunk_tc_kernel<true, false>)
                       : (post ? tc::chunk_tc_kernel<false, true> : tc::chunk_tc_kernel<false, false>);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)tc::SMEM_ALLOC);
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), (int)tc::SMEM_ALLOC);
   if (e != cudaSuccess) {
     err = std::string("cudaFuncSetAttribute(chunk_tc): ") + cudaGetErrorString(e);
     return KDA_ERR_CUDA;
