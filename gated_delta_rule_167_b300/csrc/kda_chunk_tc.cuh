@@ -295,11 +295,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     if constexpr (NBOX == 2) tma_load_3d(sm + dst + BOX_BYTES, m, 64, h, row, bar);
   };
   bool aborted = false;
-  // Waits of a whole group: one thread polls the mbarrier while the others sleep in the
-  // group's hardware barrier (no issue slots spent spinning); the outcome is shared.
+  // Waits of a whole group: the group's first warp polls the mbarrier (all its lanes, so that
+  // the warp does not diverge) while the other warps sleep in the group's hardware barrier (no
+  // issue slots spent spinning); the outcome is shared through the barrier's reduction.
   auto group_wait2 = [&](uint64_t* b1, uint32_t p1, uint64_t* b2, uint32_t p2, int id) -> bool {
     bool ok = true;
-    if (lt == 0) {
+    if (lt < 32) {
       ok = mbar_wait(b1, p1);
       if (b2 != nullptr) ok = ok && mbar_wait(b2, p2);
     }
@@ -725,7 +726,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       named_sync(BAR_P, GROUP);
-      named_sync(BAR_P, GROUP);
       if (lt == 0) mbar_arrive(&bar_ext);
       // ---------------- once S's last product of the previous block is complete: Khat^T of this
       // block (that product read the previous one) and the previous block's O
@@ -917,10 +917,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       fence_proxy_async_smem();  // G is a tensor-core operand
-      named_sync(BAR_S, GROUP);  // every thread of the group is done with WS
-      if (leader) mbar_arrive(&bar_wsfree);
-      // ---------------- Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand
+      // ---------------- Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand, once the product is
+      // complete; the wait's group barrier also says that every thread is done with WS
       if (!group_wait2(&bar_ZO, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
+      if (leader) mbar_arrive(&bar_wsfree);
       pend_mma = false;
       tc_fence_after();
       {
@@ -1015,16 +1015,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_st_wait();
       }
       tc_fence_before();
-      named_sync(BAR_S, GROUP);
-      if (aborted) break;
-      if (blk + 1 < nblocks && !vzero) {  // the v tile is dead
-        if (leader) issue_v(blk + 1);
-        pend_v = true;
-        v_blk = blk + 1;
-      }
       // ---------------- tcgen05: O^T += U^T P^T (N 64) ; S^T += U^T Khat (N 128), K 64; P has
       // stored this block's Khat^T by bar_khr. The two products have their own accumulators and
       // are issued by two threads in different warps; both commit to bar_G3.
+      // (the wait's group barrier also orders every thread's U^T bf16 stores before the products)
       if (!group_wait2(&bar_khr, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       if (leader) {
         tc_fence_after();
@@ -1044,6 +1038,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         umma_commit(&bar_G3);
       }
       pend_mma = true; last_mma = &bar_G3; last_par = ph;
+      if (blk + 1 < nblocks && !vzero) {  // the v tile is dead (U is complete)
+        if (leader) issue_v(blk + 1);
+        pend_v = true;
+        v_blk = blk + 1;
+      }
       if (!group_wait2(&bar_G3, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       pend_mma = false;
       tc_fence_after();
@@ -1060,8 +1059,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tmem_st_wait();
       }
-      tc_fence_before();
-      named_sync(BAR_S, GROUP);
+      tc_fence_before();  // the next block's operand wait is the group barrier after the copy
     }
     if (aborted) {
       record_status(4u /* KDA_ERR_TIMEOUT */);

@@ -52,11 +52,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking test of the phase with the given parity (no suspend hint: cheaper than try_wait
+// when the phase has already completed, the common case).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t a, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Waits for the phase with the given parity to complete. Returns false if the time limit ran
 // out (the caller records KDA_ERR_TIMEOUT and unwinds).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  if (mbar_test_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait(a, parity)) return true;
