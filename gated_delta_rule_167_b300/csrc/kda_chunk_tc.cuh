@@ -74,6 +74,7 @@ constexpr int THREADS = 512;  // two groups of 256
 constexpr int GROUP = 256;
 constexpr int BAR_P = 1, BAR_S = 2;  // hardware barrier ids of the groups
 constexpr int BAR_PAIR0 = 3;        // ids 3..6: pairs of warps of the state group in its solve
+constexpr int kLongestFirstMax = 256;  // packed batches of up to this many sequences run longest first
 constexpr float LOG2E = 1.4426950408889634f;
 
 // Row stride (floats) of the fp32 64 x 64 solve workspace: 76 puts the eight 16-byte rows of a
@@ -249,7 +250,26 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;  // mma fragment coordinates
 
-  const int p = blockIdx.x;
+  // A packed batch is launched longest sequences first: CTAs start in blockIdx order, so giving
+  // the (sequence, head) problems of the longest sequences the lowest indices evens out the end
+  // of the launch. Thread s < n_seq ranks sequence s (length descending, index ascending on
+  // ties, a permutation whatever the offsets hold); CTA p takes the sequence of rank p / H.
+  int p = blockIdx.x;
+  if (P.cu_seqlens != nullptr && P.seg_len == 0 && P.n_ident == 0 && P.n_seq <= kLongestFirstMax) {
+    __shared__ int seq_of_rank;
+    const int r = p / P.H;
+    if (tid < P.n_seq) {
+      const int li = P.cu_seqlens[tid + 1] - P.cu_seqlens[tid];
+      int rank = 0;
+      for (int j = 0; j < P.n_seq; ++j) {
+        const int lj = P.cu_seqlens[j + 1] - P.cu_seqlens[j];
+        rank += (lj > li) || (lj == li && j < tid);
+      }
+      if (rank == r) seq_of_rank = tid;
+    }
+    __syncthreads();
+    p = seq_of_rank * P.H + p % P.H;
+  }
   Problem pr;
   if (!resolve_problem(P, p, pr)) return;
   const int H = P.H, h = pr.h, len = pr.len;
