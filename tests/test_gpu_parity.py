@@ -246,6 +246,27 @@ def test_varlen_small_edges(kda, dtype, C):
     check(Sf.cpu().double().numpy(), S_ref, dtype, "S_final")
 
 
+@pytest.mark.parametrize("N", [200, 300])
+def test_varlen_many_sequences_any_order(kda, N):
+    """Packed batches are launched longest sequence first when they have at most 256 sequences
+    (and in index order beyond): lengths 0..150 with many ties, every sequence against the
+    oracle on its own tokens, per-sequence initial and final states."""
+    gen = torch.Generator().manual_seed(N)
+    lens = torch.randint(0, 151, (N,), generator=gen)
+    lens[::7] = 64  # ties
+    cu = torch.zeros(N + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(lens, 0).to(torch.int32)
+    T = int(cu[-1])
+    inp = kda_synth.make_prefill_inputs(1, T, 2, 128, 128, "bf16", seed=N, S0_std=0.05, n_state=N)
+    q, k, v, g, b = to_dev(inp)
+    out, Sf = kda.chunk_fwd_varlen(q, k, v, g, b, cu.to(DEV), S0=inp["S0"].to(DEV), C=64)
+    kda.kda_sync_status()
+    o_ref, S_ref = oracle.recurrent_varlen(*(f64(inp[n]) for n in ("q", "k", "v", "g", "beta")),
+                                           cu.numpy(), f64(inp["S0"]))
+    check(out.float().cpu().double().numpy(), o_ref, "bf16", "out")
+    check(Sf.cpu().double().numpy(), S_ref, "bf16", "S_final")
+
+
 def test_varlen_bad_offsets_are_reported_not_read(kda):
     """Inconsistent cu_seqlens are caught on the device and reported; nothing is read."""
     T = 64
