@@ -512,15 +512,19 @@ def recurrent_step(q, k, v, g, beta, S, stream=None):
 class HostPipeline:
     """Reusable device buffers and streams for :func:`chunk_fwd_host`.
 
-    The batch is processed one sequence row at a time on two alternating streams, so that the
-    host-to-device copy of row i + 1, the kernel of row i and the device-to-host copy of row
-    i - 1 can run at the same time (PCIe copies in the two directions use separate engines).
-    Every row's copies and its kernel are ordered on that row's stream; the caller's stream
-    waits for both streams before the call returns."""
+    The batch is processed one sequence row at a time as a three-stage pipeline on three
+    streams: every host-to-device copy on one stream, back to back; each row's kernel on a
+    second stream once its inputs have landed; each row's device-to-host copies on a third once
+    its kernel is done. The copies in the two directions use separate engines, so the input copy
+    of row i + 1, the kernel of row i and the output copy of row i - 1 run at the same time; the
+    caller's stream waits for all three before the call returns."""
 
-    def __init__(self, device, n_streams: int = 2):
+    def __init__(self, device):
         self.device = torch.device(device)
-        self.streams = [torch.cuda.Stream(device=self.device) for _ in range(n_streams)]
+        self.h2d = torch.cuda.Stream(device=self.device)
+        self.compute = torch.cuda.Stream(device=self.device)
+        self.d2h = torch.cuda.Stream(device=self.device)
+        self.streams = [self.h2d, self.compute, self.d2h]
         self.bufs = {}
 
     def buffer(self, name, shape, dtype):
@@ -561,15 +565,21 @@ def chunk_fwd_host(q, k, v, g, beta, S0=None, C: int = 64, device=None, stream=N
     for s in pl.streams:  # earlier work of the caller (e.g. on the buffers) comes first
         s.wait_stream(caller)
     for b in range(B):
-        s = pl.streams[b % len(pl.streams)]
-        with torch.cuda.stream(s):
+        with torch.cuda.stream(pl.h2d):
             for src, dst in ((q, dq), (k, dk_), (v, dv_), (g, dg), (beta, db)):
                 dst[b:b + 1].copy_(src[b:b + 1], non_blocking=True)
             if S0 is not None:
                 dS0[b:b + 1].copy_(S0[b:b + 1], non_blocking=True)
-            kda_chunk_fwd(dq[b:b + 1], dk_[b:b + 1], dv_[b:b + 1], dg[b:b + 1], db[b:b + 1],
-                          None if S0 is None else dS0[b:b + 1], dout[b:b + 1], dSf[b:b + 1],
-                          C=C, stream=s)
+            landed = torch.cuda.Event()
+            landed.record(pl.h2d)
+        pl.compute.wait_event(landed)
+        kda_chunk_fwd(dq[b:b + 1], dk_[b:b + 1], dv_[b:b + 1], dg[b:b + 1], db[b:b + 1],
+                      None if S0 is None else dS0[b:b + 1], dout[b:b + 1], dSf[b:b + 1],
+                      C=C, stream=pl.compute)
+        done = torch.cuda.Event()
+        done.record(pl.compute)
+        pl.d2h.wait_event(done)
+        with torch.cuda.stream(pl.d2h):
             out_host[b:b + 1].copy_(dout[b:b + 1], non_blocking=True)
             state_host[b:b + 1].copy_(dSf[b:b + 1], non_blocking=True)
     for s in pl.streams:
