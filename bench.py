@@ -55,19 +55,33 @@ def _peaks():
         return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
 
 
-# The sources each timed kernel is compiled from (its DRAM counters stay valid while these are
-# unchanged).
+# The sources each timed kernel is compiled from (its DRAM counters stay valid while their code
+# is unchanged).
 PREFILL_SOURCES = ("kda_chunk_tc.cuh", "kda_chunk_simt.cuh", "kda_sm100.cuh", "kda_common.cuh",
                    "kda_pre.cuh", "kda_post.cuh")
 DECODE_SOURCES = ("kda_decode.cuh", "kda_common.cuh", "kda_sm100.cuh")
+
+
+def _code_lines(text):
+    """The lines of a source file with `//` comments, trailing blanks and empty lines removed: an
+    edit to the comments leaves the hash, like the compiled kernel, unchanged. A line holding a
+    string literal is kept whole."""
+    out = []
+    for line in text.splitlines():
+        if '"' not in line and "//" in line:
+            line = line[:line.index("//")]
+        line = line.rstrip()
+        if line:
+            out.append(line)
+    return "\n".join(out)
 
 
 def _kernel_source_hash(sources=PREFILL_SOURCES):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_167_b300", "csrc")
     for name in sources:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + _code_lines(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,4 +1,6 @@
-// Tensor-core chunkwise KDA prefill for bf16 inputs (d_k = d_v = 128, C = 64), sm_103a.
+// Tensor-core chunkwise KDA prefill for bf16 inputs in 64-token blocks, sm_103a: d_k = d_v = 128
+// (64-channel heads run in the same tiles, zero-padded in shared memory), with the input side
+// (short convolution, L2 norm, gate) and the output side (RMSNorm, output gate) optionally fused.
 //
 // Mathematics (Kimi K3 wiki: "Notations mathématiques", table "Attention et KDA" for the
 // recurrence; "Glossaire", entries "Chunkwise", "UT" and "Décroissance bornée"). For one block
