@@ -619,16 +619,16 @@ kda_status_t kda_recurrent_steps(const void* q, const void* k, const void* v, co
     const float *qq = (const float*)q, *kk = (const float*)k, *vv = (const float*)v,
                 *gg = (const float*)g, *bb = (const float*)beta;
     if (d_k == 128)
-      kda::decode_tokens_kernel<float, 128, 128, 64, 128><<<grid * 2, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (float*)out, K, H);
+      kda::decode_tokens_kernel<float, 128, 128, 128><<<grid * 2, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (float*)out, K, H);
     else
-      kda::decode_tokens_kernel<float, 64, 64, 64, 128><<<grid, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (float*)out, K, H);
+      kda::decode_tokens_kernel<float, 64, 64, 128><<<grid, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (float*)out, K, H);
   } else {
     const bf *qq = (const bf*)q, *kk = (const bf*)k, *vv = (const bf*)v, *gg = (const bf*)g,
              *bb = (const bf*)beta;
     if (d_k == 128)
-      kda::decode_tokens_kernel<bf, 128, 128, 64, 128><<<grid * 2, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (bf*)out, K, H);
+      kda::decode_tokens_kernel<bf, 128, 128, 128><<<grid * 2, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (bf*)out, K, H);
     else
-      kda::decode_tokens_kernel<bf, 64, 64, 64, 128><<<grid, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (bf*)out, K, H);
+      kda::decode_tokens_kernel<bf, 64, 64, 128><<<grid, 128, 0, st>>>(qq, kk, vv, gg, bb, S, (bf*)out, K, H);
   }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "decode_tokens launch");

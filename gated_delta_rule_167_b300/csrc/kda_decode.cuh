@@ -33,7 +33,8 @@ __global__ void __launch_bounds__(THREADS)
   constexpr int CG = DV / 4;        // float4 column groups per row
   constexpr int RG = THREADS / CG;  // row groups
   constexpr int RPT = DK / RG;      // rows per thread
-  static_assert(DV % 4 == 0 && THREADS % CG == 0 && DK % RG == 0, "bad decode tiling");
+  static_assert(DV % 4 == 0 && THREADS % CG == 0 && DK % RG == 0 && (RG & (RG - 1)) == 0,
+                "bad decode tiling");
 
   __shared__ float s_alpha[DK], s_k[DK], s_ak[DK], s_aq[DK], s_q[DK];
   __shared__ float4 s_redc[RG][CG];
@@ -83,13 +84,22 @@ __global__ void __launch_bounds__(THREADS)
   }
   __syncthreads();
 
-  float4 C = make_float4(0.f, 0.f, 0.f, 0.f), P = C;
+  // the row groups' partial sums added pairwise, ((p0 + p1) + (p2 + p3)) + ..., the order in
+  // which decode_tokens_kernel adds them with warp shuffles, so that both give the same bits
+  float4 pc[RG], pp[RG];
 #pragma unroll
   for (int r = 0; r < RG; ++r) {
-    const float4 a = s_redc[r][cg], b = s_redp[r][cg];
-    C.x += a.x; C.y += a.y; C.z += a.z; C.w += a.w;
-    P.x += b.x; P.y += b.y; P.z += b.z; P.w += b.w;
+    pc[r] = s_redc[r][cg];
+    pp[r] = s_redp[r][cg];
   }
+#pragma unroll
+  for (int w = 1; w < RG; w <<= 1)
+#pragma unroll
+    for (int r = 0; r + w < RG; r += 2 * w) {
+      pc[r].x += pc[r + w].x; pc[r].y += pc[r + w].y; pc[r].z += pc[r + w].z; pc[r].w += pc[r + w].w;
+      pp[r].x += pp[r + w].x; pp[r].y += pp[r + w].y; pp[r].z += pp[r + w].z; pp[r].w += pp[r + w].w;
+    }
+  const float4 C = pc[0], P = pp[0];
   const float bt = to_f32(beta[p]);
   const TIn* vp = v + (size_t)p * DV + 4 * cg;
   float4 d;  // beta (v - c)
@@ -129,44 +139,46 @@ namespace kda {
 // any short run of tokens). Inputs are [N, K, H, d] (token t of sequence n at (n K + t) H + h);
 // out receives o for every token. The inputs of up to KB tokens are staged in shared memory in
 // one go (their loads overlap the state loads instead of following each token), with the q . k
-// products of the staged tokens; then each token takes one barrier: the two column reductions
-// go through shared arrays alternating by token parity. The value columns are independent (the
-// reductions run over the key channel), so a CTA takes DVC of the DV columns of one (sequence,
-// head): CTAs of 128 threads with 32 KiB of state each keep four in flight per SM.
-template <typename TIn, int DK, int DV, int DVC, int THREADS>
+// products of the staged tokens. The value columns are independent (the reductions run over the
+// key channel), so each warp owns 16 value columns over all DK rows: lane = row group rg (8) x
+// column group (4), rows rg RPT .. rg RPT + RPT - 1 of lane rg (the row slabs of
+// decode_step_kernel; the staged rows are padded by one word per slab, so that the eight row
+// groups' reads fall in distinct banks). The two column sums of a token are xor-shuffles inside
+// the warp, which add the row groups' partial sums in the pairwise order of decode_step_kernel:
+// K tokens give the same bits as K single steps, and tokens take no barrier of the CTA. CTAs of
+// 128 threads (64 columns, 32 KiB of state) keep four in flight per SM.
+template <typename TIn, int DK, int DV, int THREADS>
 __global__ void __launch_bounds__(THREADS, 512 / THREADS)
     decode_tokens_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                          const TIn* __restrict__ v, const TIn* __restrict__ g,
                          const TIn* __restrict__ beta, float* __restrict__ S,
                          TIn* __restrict__ out, int K, int H) {
-  constexpr int CG = DVC / 4;      // float4 column groups per CTA
-  constexpr int RG = THREADS / CG;
-  constexpr int RPT = DK / RG;
-  constexpr int KB = 8;  // tokens staged per pass
+  constexpr int WARPS = THREADS / 32;
+  constexpr int DVC = 16 * WARPS;   // value columns per CTA
   constexpr int NSPLIT = DV / DVC;  // CTAs per (sequence, head)
-  static_assert(DVC % 4 == 0 && DV % DVC == 0 && THREADS % CG == 0 && DK % RG == 0,
-                "bad decode tiling");
+  constexpr int RPT = DK / 8;       // rows per lane
+  constexpr int KB = 8;             // tokens staged per pass
+  constexpr int DKP = DK + 8;       // staged row stride: one pad word after each row slab
+  static_assert(THREADS % 32 == 0 && DV % DVC == 0 && DK % 8 == 0, "bad decode tiling");
 
-  __shared__ float s_alpha[KB][DK], s_k[KB][DK], s_q[KB][DK];
-  __shared__ float4 s_v[KB][CG];
+  __shared__ float s_alpha[KB][DKP], s_k[KB][DKP], s_q[KB][DKP];
+  __shared__ float4 s_v[KB][DVC / 4];
   __shared__ float s_beta[KB], s_qk[KB];
-  __shared__ float4 s_redc[2][RG][CG];
-  __shared__ float4 s_redp[2][RG][CG];
 
-  const int p = blockIdx.x / NSPLIT;  // n * H + h
+  const int p = blockIdx.x / NSPLIT;              // n * H + h
   const int c_off = (blockIdx.x % NSPLIT) * DVC;  // first value column of this CTA
   const int n = p / H, h = p % H;
-  const int tid = threadIdx.x;
-  const int cg = tid % CG;
-  const int rg = tid / CG;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cgl = lane & 3, rg = lane >> 2;
+  const int col4 = c_off / 4 + 4 * warp + cgl;  // this lane's float4 column in a row of S
   auto token_row = [&](int t) { return ((size_t)n * K + t) * H + h; };
 
-  // row r, column group j of this CTA's columns: float4 r * (DV / 4) + (c_off / 4) + j
-  float4* Sp = reinterpret_cast<float4*>(S + (size_t)p * DK * DV + c_off);
+  float4* Sp = reinterpret_cast<float4*>(S + (size_t)p * DK * DV);
   constexpr int ROW4 = DV / 4;
   float4 s[RPT];
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) s[i] = __ldcs(&Sp[(rg * RPT + i) * ROW4 + cg]);
+  for (int i = 0; i < RPT; ++i) s[i] = __ldcs(&Sp[(rg * RPT + i) * ROW4 + col4]);
+  auto slot = [](int r) { return r + r / RPT; };  // padded position of row r
 
   for (int t0 = 0; t0 < K; t0 += KB) {
     const int kn = min(KB, K - t0);
@@ -174,31 +186,31 @@ __global__ void __launch_bounds__(THREADS, 512 / THREADS)
     for (int e = tid; e < kn * DK; e += THREADS) {
       const int tt = e / DK, i = e % DK;
       const size_t o = token_row(t0 + tt) * DK + i;
-      s_alpha[tt][i] = expf(to_f32(g[o]));
-      s_k[tt][i] = to_f32(k[o]);
-      s_q[tt][i] = to_f32(q[o]);
+      s_alpha[tt][slot(i)] = expf(to_f32(g[o]));
+      s_k[tt][slot(i)] = to_f32(k[o]);
+      s_q[tt][slot(i)] = to_f32(q[o]);
     }
-    for (int e = tid; e < kn * CG; e += THREADS) {
-      const int tt = e / CG, j = e % CG;
+    for (int e = tid; e < kn * (DVC / 4); e += THREADS) {
+      const int tt = e / (DVC / 4), j = e % (DVC / 4);
       const TIn* vp = v + token_row(t0 + tt) * DV + c_off + 4 * j;
       s_v[tt][j] = make_float4(to_f32(vp[0]), to_f32(vp[1]), to_f32(vp[2]), to_f32(vp[3]));
     }
     if (tid < kn) s_beta[tid] = to_f32(beta[token_row(t0 + tid)]);
     __syncthreads();
-    for (int tt = tid >> 5; tt < kn; tt += THREADS / 32) {  // q . k, one warp per token
+    for (int tt = warp; tt < kn; tt += WARPS) {  // q . k, one warp per token
       float acc = 0.f;
-      for (int i = tid & 31; i < DK; i += 32) acc = fmaf(s_q[tt][i], s_k[tt][i], acc);
+      for (int i = lane; i < DK; i += 32) acc = fmaf(s_q[tt][slot(i)], s_k[tt][slot(i)], acc);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if ((tid & 31) == 0) s_qk[tt] = acc;
+      if (lane == 0) s_qk[tt] = acc;
     }
+    __syncthreads();
     for (int tt = 0; tt < kn; ++tt) {
-      const int pb = (t0 + tt) & 1;
-      // column sums over this thread's rows, on fp32 pairs: c = (alpha k)^T S, pq = (alpha q)^T S
+      // column sums over this lane's rows, on fp32 pairs: c = (alpha k)^T S, pq = (alpha q)^T S
       float2 c01 = make_float2(0.f, 0.f), c23 = c01, p01 = c01, p23 = c01;
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
-        const int r = rg * RPT + i;
+        const int r = slot(rg * RPT + i);
         const float a = s_alpha[tt][r];
         const float ak = a * s_k[tt][r], aq = a * s_q[tt][r];
         const float2 s01 = make_float2(s[i].x, s[i].y), s23 = make_float2(s[i].z, s[i].w);
@@ -207,27 +219,20 @@ __global__ void __launch_bounds__(THREADS, 512 / THREADS)
         p01 = sm100::fma2(make_float2(aq, aq), s01, p01);
         p23 = sm100::fma2(make_float2(aq, aq), s23, p23);
       }
-      s_redc[pb][rg][cg] = make_float4(c01.x, c01.y, c23.x, c23.y);
-      s_redp[pb][rg][cg] = make_float4(p01.x, p01.y, p23.x, p23.y);
-      __syncthreads();
-      float4 C = make_float4(0.f, 0.f, 0.f, 0.f), Pq = C;
+      // over the eight row groups of the warp (lane bits 2..4), pairwise
+      float red[8] = {c01.x, c01.y, c23.x, c23.y, p01.x, p01.y, p23.x, p23.y};
 #pragma unroll
-      for (int r = 0; r < RG; ++r) {
-        const float4 a = s_redc[pb][r][cg], b = s_redp[pb][r][cg];
-        C.x += a.x; C.y += a.y; C.z += a.z; C.w += a.w;
-        Pq.x += b.x; Pq.y += b.y; Pq.z += b.z; Pq.w += b.w;
-      }
+      for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) red[j] += __shfl_xor_sync(0xffffffffu, red[j], off);
       const float bt = s_beta[tt];
-      const float4 vv = s_v[tt][cg];
-      float4 d;  // beta (v - c)
-      d.x = bt * (vv.x - C.x);
-      d.y = bt * (vv.y - C.y);
-      d.z = bt * (vv.z - C.z);
-      d.w = bt * (vv.w - C.w);
-      const float2 d01 = make_float2(d.x, d.y), d23 = make_float2(d.z, d.w);
+      const float4 vv = s_v[tt][4 * warp + cgl];
+      // beta (v - c)
+      const float2 d01 = make_float2(bt * (vv.x - red[0]), bt * (vv.y - red[1]));
+      const float2 d23 = make_float2(bt * (vv.z - red[2]), bt * (vv.w - red[3]));
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {  // S <- Diag(alpha) S + k d^T
-        const int r = rg * RPT + i;
+        const int r = slot(rg * RPT + i);
         const float a = s_alpha[tt][r], kk = s_k[tt][r];
         const float2 x01 = sm100::fma2(make_float2(kk, kk), d01,
                                        sm100::mul2(make_float2(a, a), make_float2(s[i].x, s[i].y)));
@@ -235,18 +240,18 @@ __global__ void __launch_bounds__(THREADS, 512 / THREADS)
                                        sm100::mul2(make_float2(a, a), make_float2(s[i].z, s[i].w)));
         s[i] = make_float4(x01.x, x01.y, x23.x, x23.y);
       }
-      if (rg == 0) {
+      if (rg == 0) {  // o = S'^T q = pq + (q . k) d
         const float qk = s_qk[tt];
-        TIn* op = out + token_row(t0 + tt) * DV + c_off + 4 * cg;
-        op[0] = from_f32<TIn>(fmaf(qk, d.x, Pq.x));
-        op[1] = from_f32<TIn>(fmaf(qk, d.y, Pq.y));
-        op[2] = from_f32<TIn>(fmaf(qk, d.z, Pq.z));
-        op[3] = from_f32<TIn>(fmaf(qk, d.w, Pq.w));
+        TIn* op = out + token_row(t0 + tt) * DV + 4 * col4;
+        op[0] = from_f32<TIn>(fmaf(qk, d01.x, red[4]));
+        op[1] = from_f32<TIn>(fmaf(qk, d01.y, red[5]));
+        op[2] = from_f32<TIn>(fmaf(qk, d23.x, red[6]));
+        op[3] = from_f32<TIn>(fmaf(qk, d23.y, red[7]));
       }
     }
   }
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) __stcs(&Sp[(rg * RPT + i) * ROW4 + cg], s[i]);
+  for (int i = 0; i < RPT; ++i) __stcs(&Sp[(rg * RPT + i) * ROW4 + col4], s[i]);
 }
 
 }  // namespace kda
