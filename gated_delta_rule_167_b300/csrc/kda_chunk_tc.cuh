@@ -527,7 +527,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       // the fp32 range.
       uint32_t kh[2][8];  // Khat^T: [channel group][8-token block], bf16 pairs
       {
-        const int cw = 16 * warp;  // first channel of this warp
+        // first channel of this warp; with DH = 64 warps w and w + 4 take the same 16 channels,
+        // tokens 0..31 and 32..63 (hf = w / 4)
+        const int cw = 16 * (DH == 64 ? (warp & 3) : warp);
+        const int hf_only = DH == 64 ? (warp >> 2) : -1;
         const uint32_t boxo = (uint32_t)(cw >> 6) * BOX_BYTES, cin = (uint32_t)(cw & 63);
         const int lr = lane & 7, li = lane >> 3;  // row and matrix of this lane's matrix address
         auto live = [&](int m) -> uint32_t {      // keeps the tokens of block m that exist
@@ -561,7 +564,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int cg = 0; cg < 2; ++cg)
             sg[cg][R] = __shfl_sync(0xffffffffu, Lr[R][1][2 * cg + 1], (lane & ~3) | 3) * LOG2E;
-        if (t == 0) {  // e^{Gamma_L} per key channel for the state decay
+        if (t == 0 && (DH == 128 || warp < 4)) {  // e^{Gamma_L} per key channel for the state decay
 #pragma unroll
           for (int cg = 0; cg < 2; ++cg)
             gl_s[par][cw + 8 * cg + g] = ex2(sg[cg][0] + sg[cg][1] + sg[cg][2] + sg[cg][3]);
@@ -574,6 +577,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const float f0 = ex2(-sg[cg][0]), f2 = ex2(-sg[cg][2]);
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {  // tokens 32 hf .. 32 hf + 31: sub-blocks 2 hf, 2 hf + 1
+            if (DH == 64 && hf != hf_only) continue;
             uint32_t kw[4], qw[4];
             const uint32_t lo = boxo + sw128_off(32 * hf + 8 * li + lr, cin + 8 * cg);
             ldsm_x4_trans(sb + IN_K + lo, kw);
@@ -640,7 +644,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t id_d = idesc_bf16(128, 96, 1, 1, 0);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
+        for (int kk = 0; kk < DH / 16; ++kk)  // K = the real key channels
           umma_bf16(tmem + T_D, desc_sw128(sb + XK + 2048u * kk, 16384, 1024),
                     desc_sw128(sb + YP + 2048u * kk, 16384, 1024), id_d, kk > 0);
         umma_commit(&bar_D);
@@ -758,9 +762,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int cg = 0; cg < 2; ++cg)
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-          stsm_x4(sb + KH + sw128_off((uint32_t)(16 * warp + 8 * cg + (lane & 7)), (uint32_t)(8 * (4 * hf + (lane >> 3)))),
+        for (int hf = 0; hf < 2; ++hf) {
+          if (DH == 64 && hf != (warp >> 2)) continue;  // the other warp of the pair holds it
+          const int cw = 16 * (DH == 64 ? (warp & 3) : warp);
+          stsm_x4(sb + KH + sw128_off((uint32_t)(cw + 8 * cg + (lane & 7)), (uint32_t)(8 * (4 * hf + (lane >> 3)))),
                   kh[cg][4 * hf], kh[cg][4 * hf + 1], kh[cg][4 * hf + 2], kh[cg][4 * hf + 3]);
+        }
       fence_proxy_async_smem();
       if (blk > 0 && write_out) stage_o(blk - 1);
       named_sync(BAR_P, GROUP);
@@ -854,7 +861,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t id_zo = idesc_bf16(128, 128, 0, 1, 0);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
+        for (int kk = 0; kk < DH / 16; ++kk)  // K = the real key channels
           umma_bf16_tmem_a(tmem + (par ? T_ZT : t_ot), tmem + T_SB + 8u * kk,
                            desc_sw128(sb + KQ + 2048u * kk, 16384, 1024), id_zo, kk > 0);
         umma_commit(&bar_ZO);
@@ -1003,8 +1010,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       // the same lane quarter in the other half scales all 128 columns of those lanes.
       if (lt >= 32) {
         const bool both = lt >= 128 && lt < 160;  // lane quarter 0, second half
-        const int np = both ? 8 : 4;
-        const int cb = both ? 0 : 64 * hh;
+        // 16-column parts; with DH = 64 only key channels below 64 (and value lanes below 64) exist
+        constexpr int NC = DH;  // key channels to scale
+        const int np = (DH == 64 && c >= 64) ? 0 : (both ? NC / 16 : NC / 32);
+        const int cb = both ? 0 : (NC / 2) * hh;
         uint32_t v[16];
 #pragma unroll 1
         for (int part = 0; part < np; ++part) {
@@ -1044,7 +1053,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!group_wait2(&bar_khr, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
       if (leader) {
         tc_fence_after();
-        const uint32_t id_s = idesc_bf16(128, 128, 0, 0, 0);
+        const uint32_t id_s = idesc_bf16(128, DH, 0, 0, 0);  // N = the real key channels
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           umma_bf16_tmem_a(tmem + T_ST, tmem + T_UB + 8u * kk,
@@ -1070,14 +1079,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       // ---------------- bf16 copy of the new state for the next block (group P writes O)
       {
+        // with DH = 64 only value lanes and key columns below 64 exist: each half copies 32
+        // columns of them (the rest of the copy keeps the zeros it started with)
+        constexpr int CPH = DH / 2;  // columns per half
+        const int nparts = (DH == 64 && c >= 64) ? 0 : CPH / 16;
 #pragma unroll 1
-        for (int part = 0; part < 4; ++part) {
+        for (int part = 0; part < nparts; ++part) {
           uint32_t v[16], sbf[8];
-          tmem_ld16(tl + T_ST + 64 * hh + 16 * part, v);
+          tmem_ld16(tl + T_ST + CPH * hh + 16 * part, v);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 8; ++j) sbf[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-          tmem_st8(tl + T_SB + 32 * hh + 8 * part, sbf);
+          tmem_st8(tl + T_SB + CPH / 2 * hh + 8 * part, sbf);
         }
         tmem_st_wait();
       }
