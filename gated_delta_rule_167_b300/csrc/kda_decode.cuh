@@ -33,8 +33,7 @@ __global__ void __launch_bounds__(THREADS)
   constexpr int CG = DV / 4;        // float4 column groups per row
   constexpr int RG = THREADS / CG;  // row groups
   constexpr int RPT = DK / RG;      // rows per thread
-  static_assert(DV % 4 == 0 && THREADS % CG == 0 && DK % RG == 0 && (RG & (RG - 1)) == 0,
-                "bad decode tiling");
+  static_assert(DV % 4 == 0 && THREADS % CG == 0 && DK % RG == 0, "bad decode tiling");
 
   __shared__ float s_alpha[DK], s_k[DK], s_ak[DK], s_aq[DK], s_q[DK];
   __shared__ float4 s_redc[RG][CG];
@@ -84,22 +83,13 @@ __global__ void __launch_bounds__(THREADS)
   }
   __syncthreads();
 
-  // the row groups' partial sums added pairwise, ((p0 + p1) + (p2 + p3)) + ..., the order in
-  // which decode_tokens_kernel adds them with warp shuffles, so that both give the same bits
-  float4 pc[RG], pp[RG];
+  float4 C = make_float4(0.f, 0.f, 0.f, 0.f), P = C;
 #pragma unroll
   for (int r = 0; r < RG; ++r) {
-    pc[r] = s_redc[r][cg];
-    pp[r] = s_redp[r][cg];
+    const float4 a = s_redc[r][cg], b = s_redp[r][cg];
+    C.x += a.x; C.y += a.y; C.z += a.z; C.w += a.w;
+    P.x += b.x; P.y += b.y; P.z += b.z; P.w += b.w;
   }
-#pragma unroll
-  for (int w = 1; w < RG; w <<= 1)
-#pragma unroll
-    for (int r = 0; r + w < RG; r += 2 * w) {
-      pc[r].x += pc[r + w].x; pc[r].y += pc[r + w].y; pc[r].z += pc[r + w].z; pc[r].w += pc[r + w].w;
-      pp[r].x += pp[r + w].x; pp[r].y += pp[r + w].y; pp[r].z += pp[r + w].z; pp[r].w += pp[r + w].w;
-    }
-  const float4 C = pc[0], P = pp[0];
   const float bt = to_f32(beta[p]);
   const TIn* vp = v + (size_t)p * DV + 4 * cg;
   float4 d;  // beta (v - c)
@@ -144,9 +134,9 @@ namespace kda {
 // column group (4), rows rg RPT .. rg RPT + RPT - 1 of lane rg (the row slabs of
 // decode_step_kernel; the staged rows are padded by one word per slab, so that the eight row
 // groups' reads fall in distinct banks). The two column sums of a token are xor-shuffles inside
-// the warp, which add the row groups' partial sums in the pairwise order of decode_step_kernel:
-// K tokens give the same bits as K single steps, and tokens take no barrier of the CTA. CTAs of
-// 128 threads (64 columns, 32 KiB of state) keep four in flight per SM.
+// the warp (the row groups' partial sums added pairwise, where decode_step_kernel adds them in
+// sequence: the two agree to fp32 rounding, not bit for bit), and tokens take no barrier of the
+// CTA. CTAs of 128 threads (64 columns, 32 KiB of state) keep four in flight per SM.
 template <typename TIn, int DK, int DV, int THREADS>
 __global__ void __launch_bounds__(THREADS, 512 / THREADS)
     decode_tokens_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,

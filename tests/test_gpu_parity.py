@@ -362,8 +362,9 @@ def _decode_tokens_inputs(N, K, H, d, dtype, seed):
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("K", [1, 3, 8])
 def test_decode_tokens_equal_single_steps_and_oracle(kda, dtype, d, K):
-    """K tokens in one call give the same bits as K single-token calls (the same arithmetic per
-    token, the state kept in fp32 on chip instead of in HBM) and match the oracle."""
+    """K tokens in one call agree with K single-token calls to fp32 rounding (the same arithmetic
+    per token, the state kept in fp32 on chip instead of in HBM; the column sums over the key
+    channel add the row groups' partial sums in another order) and match the oracle."""
     dec, stack = _decode_tokens_inputs(5, K, 3, d, dtype, seed=K + d)
     S1 = dec["S"].to(DEV)
     outs = [kda.recurrent_step(*(st[n].to(DEV) for n in ("q", "k", "v", "g", "beta")), S1)
@@ -372,9 +373,12 @@ def test_decode_tokens_equal_single_steps_and_oracle(kda, dtype, d, K):
     out = torch.empty(5, K, 3, d, dtype=stack["q"].dtype, device=DEV)
     kda.kda_recurrent_steps(*(stack[n].to(DEV) for n in ("q", "k", "v", "g", "beta")), S2, out)
     kda.kda_sync_status()
-    assert torch.equal(S1, S2)
+    # fp32 state: a reassociated sum of eight partials; outputs may differ by one rounding of
+    # the output type (bf16: 2^-8 relative)
+    assert torch.allclose(S1, S2, rtol=1e-5, atol=1e-6)
+    o_rtol = 1e-5 if dtype == "f32" else 2.0 ** -7
     for t in range(K):
-        assert torch.equal(out[:, t], outs[t])
+        assert torch.allclose(out[:, t].float(), outs[t].float(), rtol=o_rtol, atol=1e-6)
     Sref = f64(dec["S"])
     for t, st in enumerate(dec["steps"]):
         o_ref, Sref = oracle.decode_step(*(f64(st[n]) for n in ("q", "k", "v", "g", "beta")), Sref)
