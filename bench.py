@@ -244,9 +244,20 @@ def _max_over_ranks(x, world, device):
     return float(t.item())
 
 
-def _timed(fn, steps, warmup, world, device, stream):
+def _hold_stream(stream, ms=50.0):
+    """Queues a spin kernel of about `ms` on `stream` (outside any timed span), so that the
+    launches that follow are all submitted while the GPU is still busy with it: the events then
+    time the device work back to back, without gaps from the host's launch latency or from the
+    clock sampler starting up."""
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(ms * 1e-3 * 2.0e9))
+
+
+def _timed(fn, steps, warmup, world, device, stream, hold=True):
     """W untimed warm-up calls, then K timed calls bracketed by barrier + synchronize; the
-    duration comes from CUDA events on the launching stream. Returns (total_ms, clocks)."""
+    duration comes from CUDA events on the launching stream. `hold`: the timed calls are queued
+    behind a spin kernel (see _hold_stream); not for calls that synchronize with the host.
+    Returns (total_ms, clocks)."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize(device)
@@ -255,6 +266,8 @@ def _timed(fn, steps, warmup, world, device, stream):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(device) as cs:
+        if hold:
+            _hold_stream(stream)
         e0.record(stream)
         for _ in range(steps):
             fn()
@@ -382,7 +395,7 @@ def bench_prefill(kda, args, world, rank, device, stream, peaks):
                            pipeline=pipe)
 
     e2e_steps = max(1, min(args.steps, 3))
-    e2e_ms, _ = _timed(e2e_step, e2e_steps, 1, world, device, stream)
+    e2e_ms, _ = _timed(e2e_step, e2e_steps, 1, world, device, stream, hold=False)
     res["e2e"] = {"value": world * B * T / (e2e_ms / e2e_steps * 1e-3), "unit": "tokens/s",
                   "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin.values()),
                   "d2h_bytes_per_step": out_h.numel() * 2 + st_h.numel() * 4,
@@ -402,6 +415,7 @@ def _timed_flushed(fn, steps, warmup, device, stream):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     with ClockSampler(device) as cs:
+        _hold_stream(stream)
         for e0, e1 in ev:
             flush.fill_(1)
             e0.record(stream)
