@@ -102,8 +102,9 @@ kda_status_t kda_recurrent_step(const void* q, const void* k, const void* v, con
  * speculative draft tokens, or a short run of tokens).
  *   q, k, g : [N, K, H, d_k] dtype   v, out : [N, K, H, d_v] dtype   beta : [N, K, H] dtype
  *   S       : [N, H, d_k, d_v] fp32, read and overwritten with the state after the K tokens
- * out receives o_t = S_t^T q_t for every token. K = 1 gives kda_recurrent_step. N * H must be
- * below 2^30 (KDA_ERR_UNSUPPORTED otherwise).
+ * out receives o_t = S_t^T q_t for every token. K = 1 computes what kda_recurrent_step computes
+ * (to fp32 rounding: the column sums over the key channel are added in another order). N * H
+ * must be below 2^30 (KDA_ERR_UNSUPPORTED otherwise).
  */
 kda_status_t kda_recurrent_steps(const void* q, const void* k, const void* v, const void* g,
                                  const void* beta, float* S, void* out, int N, int K, int H,
