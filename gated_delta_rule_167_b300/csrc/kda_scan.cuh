@@ -7,7 +7,8 @@
 //   S_in(0) = S0,   S_in(sigma + 1) = M_sigma S_in(sigma) + S~_sigma.
 // Columns of S are independent, so one CTA owns (sequence, head, 1024 / d_k value columns) and walks
 // the segments in order. M_sigma (fp32, d_k x d_k) is staged in shared memory by asynchronous
-// copies one segment ahead; the NC columns of S_in stay in shared memory; fp32 FMAs throughout.
+// copies one segment ahead, S~ one segment ahead in registers; the NC columns of S_in stay in
+// shared memory; fp32 FMAs throughout.
 //
 // Layouts (fp32, row-major): M [n_seg - 1, BH, DK, DK]; St [n_seg - 1, BH, DK, DV];
 // S0 [BH, DK, DV] or null (zeros); S_in [n_seg, BH, DK, DV].
@@ -81,7 +82,17 @@ __global__ void __launch_bounds__(THREADS)
       acc[j] = x.x; acc[j + 1] = x.y; acc[j + 2] = x.z; acc[j + 3] = x.w;
     }
   }
-  if (n_seg > 1) load_m(0, sm);
+  // S~ of the step in flight, loaded one step ahead so that its latency overlaps a step's products
+  float4 stn[CPT / 4];
+  auto load_st = [&](int sigma) {
+    const float* st_row = St + ((size_t)sigma * BH + bh) * st + (size_t)i * DV + c_base + c0;
+#pragma unroll
+    for (int j = 0; j < CPT; j += 4) stn[j / 4] = *reinterpret_cast<const float4*>(st_row + j);
+  };
+  if (n_seg > 1) {
+    load_m(0, sm);
+    load_st(0);
+  }
   for (int sigma = 0;; ++sigma) {
     float* out = S_in + ((size_t)sigma * BH + bh) * st + (size_t)i * DV + c_base + c0;
 #pragma unroll
@@ -99,12 +110,12 @@ __global__ void __launch_bounds__(THREADS)
       cp_async_wait<0>();
     }
     __syncthreads();  // M_sigma and the tile are in place
-    const float* st_row = St + ((size_t)sigma * BH + bh) * st + (size_t)i * DV + c_base + c0;
 #pragma unroll
     for (int j = 0; j < CPT; j += 4) {
-      const float4 x = *reinterpret_cast<const float4*>(st_row + j);
+      const float4 x = stn[j / 4];
       acc[j] = x.x; acc[j + 1] = x.y; acc[j + 2] = x.z; acc[j + 3] = x.w;
     }
+    if (sigma + 2 < n_seg) load_st(sigma + 1);
     const float* mrow = sm + (sigma & 1) * SM::m_floats + i * LDM;
 #pragma unroll 4
     for (int k = 0; k < DK; k += 4) {
