@@ -126,9 +126,10 @@ __device__ __forceinline__ void l2norm8(float (&x)[8]) {
 // (contiguous memory); blockIdx.z picks q, k, v (convolution, and the norm for q and k) or g
 // (the decay gate), so that a thread holds one tensor's rows and many CTAs fit on an SM. D / 8
 // threads per token row, 8 channels and 4 consecutive tokens per thread: each thread reads the
-// 7 rows it needs once (the rows shared with neighbouring threads hit L1).
+// 7 rows it needs once (the rows shared with neighbouring threads hit L1). With bf16 inputs
+// three CTAs share an SM (registers capped at 85, a few spills): more loads in flight per SM.
 template <typename TIn, int D>
-__global__ void __launch_bounds__(256) pre_core_kernel(PreParams P, long long n_tok) {
+__global__ void __launch_bounds__(256, sizeof(TIn) == 2 ? 3 : 2) pre_core_kernel(PreParams P, long long n_tok) {
   constexpr int TPR = D / 8;            // threads per token row
   constexpr int TOK = 4 * (256 / TPR);  // tokens per CTA
   const int h = blockIdx.x;
