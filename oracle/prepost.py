@@ -14,7 +14,7 @@ module; the product never does. Definitions (Kimi K3 wiki):
   gate: yes". Chapter 03: RMSNorm on the recurrent output of KDA; L2Norm on KDA's queries and
   keys.
 
-Readings of what the pages leave open (each one listed in the design doc):
+Readings of what the pages leave open:
 
 * gate: g = g_min * sigma(e^{A_h} z + b_alpha^h) -- the bias of the notation table added to the
   scaled logit of the glossary's formula;
