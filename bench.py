@@ -249,6 +249,8 @@ def _hold_stream(stream, ms=50.0):
     launches that follow are all submitted while the GPU is still busy with it: the events then
     time the device work back to back, without gaps from the host's launch latency or from the
     clock sampler starting up."""
+    if not hasattr(torch.cuda, "_sleep"):
+        return
     with torch.cuda.stream(stream):
         torch.cuda._sleep(int(ms * 1e-3 * 2.0e9))
 
