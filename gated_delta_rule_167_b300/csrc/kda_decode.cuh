@@ -132,8 +132,9 @@ namespace kda {
 // products of the staged tokens. The value columns are independent (the reductions run over the
 // key channel), so each warp owns 16 value columns over all DK rows: lane = row group rg (8) x
 // column group (4), rows rg RPT .. rg RPT + RPT - 1 of lane rg (the row slabs of
-// decode_step_kernel; the staged rows are padded by one word per slab, so that the eight row
-// groups' reads fall in distinct banks). The two column sums of a token are xor-shuffles inside
+// decode_step_kernel; the staged rows, with alpha k and alpha q formed once per token and
+// channel, are read as float4 and padded by four words per slab, so that the eight row groups'
+// reads fall in distinct banks). The two column sums of a token are xor-shuffles inside
 // the warp (the row groups' partial sums added pairwise, where decode_step_kernel adds them in
 // sequence: the two agree to fp32 rounding, not bit for bit), and tokens take no barrier of the
 // CTA. CTAs of 128 threads (64 columns, 32 KiB of state) keep four in flight per SM.
@@ -148,10 +149,13 @@ __global__ void __launch_bounds__(THREADS, 512 / THREADS)
   constexpr int NSPLIT = DV / DVC;  // CTAs per (sequence, head)
   constexpr int RPT = DK / 8;       // rows per lane
   constexpr int KB = 8;             // tokens staged per pass
-  constexpr int DKP = DK + 8;       // staged row stride: one pad word after each row slab
-  static_assert(THREADS % 32 == 0 && DV % DVC == 0 && DK % 8 == 0, "bad decode tiling");
+  constexpr int DKP = DK + 32;      // staged row stride: four pad words after each row slab
+  static_assert(THREADS % 32 == 0 && DV % DVC == 0 && DK % 8 == 0 && RPT % 4 == 0,
+                "bad decode tiling");
 
-  __shared__ float s_alpha[KB][DKP], s_k[KB][DKP], s_q[KB][DKP];
+  // per staged token and key channel: alpha, k, q and the products alpha k, alpha q
+  __shared__ __align__(16) float s_alpha[KB][DKP], s_k[KB][DKP], s_q[KB][DKP];
+  __shared__ __align__(16) float s_ak[KB][DKP], s_aq[KB][DKP];
   __shared__ float4 s_v[KB][DVC / 4];
   __shared__ float s_beta[KB], s_qk[KB];
 
@@ -168,7 +172,10 @@ __global__ void __launch_bounds__(THREADS, 512 / THREADS)
   float4 s[RPT];
 #pragma unroll
   for (int i = 0; i < RPT; ++i) s[i] = __ldcs(&Sp[(rg * RPT + i) * ROW4 + col4]);
-  auto slot = [](int r) { return r + r / RPT; };  // padded position of row r
+  // padded position of row r: a lane's slab starts on 16 bytes (read as float4), and the eight
+  // slabs of a warp's row groups fall in distinct banks
+  auto slot = [](int r) { return r + 4 * (r / RPT); };
+  const int slab = slot(rg * RPT);  // this lane's first row
 
   for (int t0 = 0; t0 < K; t0 += KB) {
     const int kn = min(KB, K - t0);
@@ -176,9 +183,12 @@ __global__ void __launch_bounds__(THREADS, 512 / THREADS)
     for (int e = tid; e < kn * DK; e += THREADS) {
       const int tt = e / DK, i = e % DK;
       const size_t o = token_row(t0 + tt) * DK + i;
-      s_alpha[tt][slot(i)] = expf(to_f32(g[o]));
-      s_k[tt][slot(i)] = to_f32(k[o]);
-      s_q[tt][slot(i)] = to_f32(q[o]);
+      const float a = expf(to_f32(g[o])), kk = to_f32(k[o]), qq = to_f32(q[o]);
+      s_alpha[tt][slot(i)] = a;
+      s_k[tt][slot(i)] = kk;
+      s_q[tt][slot(i)] = qq;
+      s_ak[tt][slot(i)] = a * kk;
+      s_aq[tt][slot(i)] = a * qq;
     }
     for (int e = tid; e < kn * (DVC / 4); e += THREADS) {
       const int tt = e / (DVC / 4), j = e % (DVC / 4);
@@ -199,15 +209,20 @@ __global__ void __launch_bounds__(THREADS, 512 / THREADS)
       // column sums over this lane's rows, on fp32 pairs: c = (alpha k)^T S, pq = (alpha q)^T S
       float2 c01 = make_float2(0.f, 0.f), c23 = c01, p01 = c01, p23 = c01;
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) {
-        const int r = slot(rg * RPT + i);
-        const float a = s_alpha[tt][r];
-        const float ak = a * s_k[tt][r], aq = a * s_q[tt][r];
-        const float2 s01 = make_float2(s[i].x, s[i].y), s23 = make_float2(s[i].z, s[i].w);
-        c01 = sm100::fma2(make_float2(ak, ak), s01, c01);
-        c23 = sm100::fma2(make_float2(ak, ak), s23, c23);
-        p01 = sm100::fma2(make_float2(aq, aq), s01, p01);
-        p23 = sm100::fma2(make_float2(aq, aq), s23, p23);
+      for (int i4 = 0; i4 < RPT; i4 += 4) {
+        const float4 ak4 = *reinterpret_cast<const float4*>(&s_ak[tt][slab + i4]);
+        const float4 aq4 = *reinterpret_cast<const float4*>(&s_aq[tt][slab + i4]);
+        const float akv[4] = {ak4.x, ak4.y, ak4.z, ak4.w}, aqv[4] = {aq4.x, aq4.y, aq4.z, aq4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float ak = akv[u], aq = aqv[u];
+          const float4 si = s[i4 + u];
+          const float2 s01 = make_float2(si.x, si.y), s23 = make_float2(si.z, si.w);
+          c01 = sm100::fma2(make_float2(ak, ak), s01, c01);
+          c23 = sm100::fma2(make_float2(ak, ak), s23, c23);
+          p01 = sm100::fma2(make_float2(aq, aq), s01, p01);
+          p23 = sm100::fma2(make_float2(aq, aq), s23, p23);
+        }
       }
       // over the eight row groups of the warp (lane bits 2..4), pairwise
       float red[8] = {c01.x, c01.y, c23.x, c23.y, p01.x, p01.y, p23.x, p23.y};
@@ -221,14 +236,20 @@ __global__ void __launch_bounds__(THREADS, 512 / THREADS)
       const float2 d01 = make_float2(bt * (vv.x - red[0]), bt * (vv.y - red[1]));
       const float2 d23 = make_float2(bt * (vv.z - red[2]), bt * (vv.w - red[3]));
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) {  // S <- Diag(alpha) S + k d^T
-        const int r = slot(rg * RPT + i);
-        const float a = s_alpha[tt][r], kk = s_k[tt][r];
-        const float2 x01 = sm100::fma2(make_float2(kk, kk), d01,
-                                       sm100::mul2(make_float2(a, a), make_float2(s[i].x, s[i].y)));
-        const float2 x23 = sm100::fma2(make_float2(kk, kk), d23,
-                                       sm100::mul2(make_float2(a, a), make_float2(s[i].z, s[i].w)));
-        s[i] = make_float4(x01.x, x01.y, x23.x, x23.y);
+      for (int i4 = 0; i4 < RPT; i4 += 4) {  // S <- Diag(alpha) S + k d^T
+        const float4 a4 = *reinterpret_cast<const float4*>(&s_alpha[tt][slab + i4]);
+        const float4 k4 = *reinterpret_cast<const float4*>(&s_k[tt][slab + i4]);
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float a = av[u], kk = kv[u];
+          const int i = i4 + u;
+          const float2 x01 = sm100::fma2(make_float2(kk, kk), d01,
+                                         sm100::mul2(make_float2(a, a), make_float2(s[i].x, s[i].y)));
+          const float2 x23 = sm100::fma2(make_float2(kk, kk), d23,
+                                         sm100::mul2(make_float2(a, a), make_float2(s[i].z, s[i].w)));
+          s[i] = make_float4(x01.x, x01.y, x23.x, x23.y);
+        }
       }
       if (rg == 0) {  // o = S'^T q = pq + (q . k) d
         const float qk = s_qk[tt];
