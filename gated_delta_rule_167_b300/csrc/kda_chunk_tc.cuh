@@ -235,6 +235,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   // bar_D, bar_ZO, bar_G2, bar_G3: tcgen05 products complete
   __shared__ uint64_t bar_in, bar_v, bar_prep, bar_ext, bar_wsfree, bar_khr, bar_D, bar_ZO, bar_G2,
       bar_G3;
+  // bar_qg (input side fused): group S has formed a block's q and g in place in the staged tiles
+  __shared__ uint64_t bar_qg;
   __shared__ uint32_t tmem_base_s;
   __shared__ __align__(16) float beta_s[2][C];  // by block parity
   __shared__ __align__(16) float gl_s[2][D];    // e^{Gamma_L} per key channel, by block parity
@@ -279,6 +281,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const bool vzero = pr.ident;              // v = 0: no v tile, U^T = -Z^T G^T
   const bool write_out = P.out != nullptr;  // outputs wanted
   constexpr bool pre = PRE;
+  // input side fused: group P forms k; group S forms q, and g as well when the output side is
+  // fused too (group P then also runs the output epilogue), so that the two groups' chains per
+  // block come out closest
+  constexpr bool s_takes_q = true;
+  constexpr bool s_takes_g = POST;
   const int nblocks = (len + C - 1) / C;
 
   if (tid == 0) {
@@ -292,6 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bar_ZO, 1);
     mbar_init(&bar_G2, 1);
     mbar_init(&bar_G3, 2);  // the two issuers of the last product commit to it
+    mbar_init(&bar_qg, 1);
     fence_mbar_init();
     prefetch_tensormap(&maps.q);
     prefetch_tensormap(&maps.k);
@@ -327,6 +335,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (b2 != nullptr) ok = ok && mbar_wait(b2, p2);
     }
     return !named_sync_or(id, GROUP, !ok);
+  };
+
+  // input side fused: g = g_min sigma(e^A z + b) on thread (cg, rg)'s chunks of the staged z tile
+  auto gate_rows4 = [&](int cg, int rg) {
+    const float eA = expf(P.A_log[h]);
+    float b8[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) b8[e] = P.b_decay[(size_t)h * D + 8 * cg + e];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4* p4 = reinterpret_cast<uint4*>(sm + IN_G + tile_chunk(cg, 4 * rg + i));
+      float z[8];
+      post::unpack8(*p4, z);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) z[e] = pre::decay_gate<__nv_bfloat16>(z[e], eA, b8[e]);
+      *p4 = post::pack8(z);
+    }
   };
 
   if (isP) {
@@ -467,16 +492,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!group_wait2(&bar_in, blk & 1, nullptr, 0, BAR_P)) { aborted = true; break; }
       pend_in = false;
       if constexpr (pre) {
-        // ---------------- input side: k = L2Norm(ShortConv(k~)), q = L2Norm(ShortConv(q~)) and
-        // g = g_min sigma(e^A z + b) in place in the staged tiles, thread (cg, rg): channels
-        // 8 cg .. + 7 of rows 4 rg .. + 3. Every raw row is read before any is written. The last
-        // three raw rows of k~ and q~ wait for the next block in the padding columns 64..71 of WS,
-        // which no other step touches: 16-byte chunk ((tensor * 3 + row) * 16 + cg) at WS row
-        // chunk / 2, byte 256 + 16 (chunk % 2).
+        // ---------------- input side: k = L2Norm(ShortConv(k~)) in place in the staged tile (and
+        // g = g_min sigma(e^A z + b) unless group S forms it), thread (cg, rg): channels 8 cg .. + 7
+        // of rows 4 rg .. + 3; group S forms q meanwhile (bar_qg). Every raw row is read before any
+        // is written. The last three raw rows of k~ (and
+        // of q~, group S) wait for the next block in the padding columns 64..71 of WS, which no other
+        // step touches: 16-byte chunk ((tensor * 3 + row) * 16 + cg) at WS row chunk / 2, byte
+        // 256 + 16 (chunk % 2).
         const int cg = lt & 15, rg = lt >> 4;
         const int first_pos = pr.pos0 + t0;
 #pragma unroll
-        for (int ts = 0; ts < 2; ++ts) {  // k, then q (one tensor's results live at a time)
+        for (int ts = 0; ts < (s_takes_q ? 1 : 2); ++ts) {  // k (and q), one tensor at a time
           auto halo = [&](int hr) {
             const int chunk = (ts * 3 + hr) * 16 + cg;
             return sm + WS + (chunk >> 1) * (WLD * 4) + 64 * 4 + (chunk & 1) * 16;
@@ -492,26 +518,13 @@ __global__ void __launch_bounds__(THREADS, 1)
               pk[i] = post::pack8(y[i]);
             }
           }
-          if (ts == 1) {  // the decay gate on this thread's own chunks of the z tile
-            const float eA = expf(P.A_log[h]);
-            float b8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) b8[e] = P.b_decay[(size_t)h * D + 8 * cg + e];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4* p4 = reinterpret_cast<uint4*>(sm + IN_G + tile_chunk(cg, 4 * rg + i));
-              float z[8];
-              post::unpack8(*p4, z);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) z[e] = pre::decay_gate<__nv_bfloat16>(z[e], eA, b8[e]);
-              *p4 = post::pack8(z);
-            }
-          }
+          if (!s_takes_g && ts == 0) gate_rows4(cg, rg);
           named_sync(BAR_P, GROUP);  // every raw row of this tile (and its stash) has been read
           if (rg == 15 && blk + 1 < nblocks) stash_rows(tile, cg, halo);
           put_rows4(tile, cg, rg, pk);
         }
-        named_sync(BAR_P, GROUP);
+        // q and g of this block from group S (the wait's group barrier also orders the k rows)
+        if (!group_wait2(&bar_qg, blk & 1, nullptr, 0, BAR_P)) { aborted = true; break; }
       }
       // ---------------- operands: X, Y, (K e^Gamma)^T, (Q e^Gamma)^T; Khat^T kept packed
       // Warp w covers channels 16 w .. 16 w + 15 (channel group cg = 0, 1 of 8) over all 64 tokens:
@@ -826,6 +839,39 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_st_wait();
       tc_fence_before();
     }
+    // input side fused: q = L2Norm(ShortConv(q~)) and g = g_min sigma(e^A z + b) of block b in
+    // place in the staged tiles, once they have landed (group P forms k meanwhile); thread
+    // (cg, rg) as in group P's pass, the last three raw rows of q~ stashed in the WS padding
+    auto transform_qg = [&](int b) -> bool {
+      if (!group_wait2(&bar_in, b & 1, nullptr, 0, BAR_S)) return false;
+      const int cg = lt & 15, rg = lt >> 4;
+      if constexpr (s_takes_q) {
+        auto halo = [&](int hr) {
+          const int chunk = (3 + hr) * 16 + cg;
+          return sm + WS + (chunk >> 1) * (WLD * 4) + 64 * 4 + (chunk & 1) * 16;
+        };
+        uint8_t* tile = sm + IN_Q;
+        uint4 pk[4];
+        {
+          float y[4][8];
+          conv_rows4(tile, P.conv_q, h, cg, rg, pr.pos0 + b * C, halo, y);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            pre::l2norm8<D, false>(y[i]);
+            pk[i] = post::pack8(y[i]);
+          }
+        }
+        if constexpr (s_takes_g) gate_rows4(cg, rg);
+        named_sync(BAR_S, GROUP);  // every raw row of the q tile (and its stash) has been read
+        if (rg == 15 && b + 1 < nblocks) stash_rows(tile, cg, halo);
+        put_rows4(tile, cg, rg, pk);
+      } else {
+        gate_rows4(cg, rg);
+      }
+      named_sync(BAR_S, GROUP);
+      if (leader) mbar_arrive(&bar_qg);
+      return true;
+    };
     bool pend_v = false, pend_mma = false;
     int v_blk = 0;  // block of the last v load issued
     uint64_t* last_mma = &bar_ZO;
@@ -838,8 +884,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = lt; i < 8192 / 16; i += GROUP) st_shared_v4(sb + GB + 16u * (uint32_t)i, 0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     named_sync(BAR_S, GROUP);
+    int nb_run = nblocks;  // blocks to run (none if the first block's q and g timed out)
+    if constexpr (pre) {
+      if (nblocks > 0 && !transform_qg(0)) {
+        aborted = true;
+        nb_run = 0;
+      }
+    }
 
-    for (int blk = 0; blk < nblocks; ++blk) {
+    for (int blk = 0; blk < nb_run; ++blk) {
       const int t0 = blk * C;
       const int n = min(C, len - t0);
       const int par = blk & 1;
@@ -946,6 +999,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       fence_proxy_async_smem();  // G is a tensor-core operand
+      if constexpr (pre) {  // the next block's q and g, which group P's operand phase waits for
+        if (blk + 1 < nblocks && !transform_qg(blk + 1)) { aborted = true; break; }
+      }
       // ---------------- Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand, once the product is
       // complete; the wait's group barrier also says that every thread is done with WS
       if (!group_wait2(&bar_ZO, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
