@@ -432,7 +432,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                        : make_uint4(0, 0, 0, 0);
       }
     };
-    auto store_o = [&](int b) {
+    // (with the output side alone, the caller loads the gate rows ahead into ur; with both sides
+    // fused the registers are short and they are loaded here)
+    auto store_o = [&](int b, const uint4 (&ur_ahead)[4]) {
       const int tb = b * C;
       const int nb = min(C, len - tb);
       const int q = lt & 15;  // 16-byte chunk of a row; rows lt / 16 + 16 i
@@ -449,7 +451,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else if constexpr (gated) {
         uint4 ur[4];
-        load_u(b, ur);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ur[i] = ur_ahead[i];
+        if constexpr (pre) load_u(b, ur);
         float w8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) w8[e] = P.norm_w[8 * q + e];
@@ -766,6 +770,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       named_sync(BAR_P, GROUP);
       if (lt == 0) mbar_arrive(&bar_ext);
+      // the previous block's gate rows: their loads run under the waits and the staging below
+      uint4 ur[4];
+      if constexpr (gated && !pre) {
+        if (blk > 0 && write_out) load_u(blk - 1, ur);
+      }
       // ---------------- once S's last product of the previous block is complete: Khat^T of this
       // block (that product read the previous one) and the previous block's O
       if (blk > 0) {
@@ -787,15 +796,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       // Khat^T is stored and the previous block's O is out of TMEM; its global stores follow (the
       // release of this arrive does not wait for them)
       if (lt == 0) mbar_arrive(&bar_khr);
-      if (blk > 0 && write_out) store_o(blk - 1);
+      if (blk > 0 && write_out) store_o(blk - 1, ur);
     }
     if (!aborted && nblocks > 0) {  // the last block's O
       if (group_wait2(&bar_G3, (nblocks - 1) & 1, nullptr, 0, BAR_P)) {
         tc_fence_after();
         if (write_out) {
+          uint4 ur[4];
+          if constexpr (gated && !pre) load_u(nblocks - 1, ur);
           stage_o(nblocks - 1);
           named_sync(BAR_P, GROUP);
-          store_o(nblocks - 1);
+          store_o(nblocks - 1, ur);
         }
       } else {
         aborted = true;
