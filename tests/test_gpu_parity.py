@@ -360,7 +360,7 @@ def _decode_tokens_inputs(N, K, H, d, dtype, seed):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("K", [1, 3, 8])
+@pytest.mark.parametrize("K", [1, 3, 8, 11])
 def test_decode_tokens_equal_single_steps_and_oracle(kda, dtype, d, K):
     """K tokens in one call agree with K single-token calls to fp32 rounding (the same arithmetic
     per token, the state kept in fp32 on chip instead of in HBM; the column sums over the key
