@@ -52,8 +52,9 @@
 // blocks ago (O^T and P are double-buffered by block parity). Transposed products keep every
 // tcgen05 product at M = 128 (TMEM lane = row). Only the bf16 copy of the state feeds the tensor
 // cores; the fp32 state accumulates in TMEM, so rounding does not accumulate in S itself. Every
-// wait is bounded; a timeout latches KDA_ERR_TIMEOUT, lets issued copies and products land,
-// frees TMEM and returns.
+// wait is bounded; after a timeout the CTA's later waits return at once, the groups run through
+// their remaining blocks, and the kernel latches KDA_ERR_TIMEOUT, lets issued copies and products
+// land, frees TMEM and returns.
 #pragma once
 
 #include <cuda.h>
@@ -238,6 +239,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // bar_qg (input side fused): group S has formed a block's q and g in place in the staged tiles
   __shared__ uint64_t bar_qg;
   __shared__ uint32_t tmem_base_s;
+  __shared__ int cta_abort;  // a wait of this CTA ran out of time
   __shared__ __align__(16) float beta_s[2][C];  // by block parity
   __shared__ __align__(16) float gl_s[2][D];    // e^{Gamma_L} per key channel, by block parity
   // diagonal blocks T_RR of the solve (written by group P, read by group S); rows of 20 floats:
@@ -289,6 +291,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nblocks = (len + C - 1) / C;
 
   if (tid == 0) {
+    cta_abort = 0;
     mbar_init(&bar_in, 1);
     mbar_init(&bar_v, 1);
     mbar_init(&bar_prep, 1);
@@ -324,17 +327,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_load_3d(sm + dst, m, 0, h, row, bar);
     if constexpr (NBOX == 2) tma_load_3d(sm + dst + BOX_BYTES, m, 64, h, row, bar);
   };
-  bool aborted = false;
   // Waits of a whole group: the group's first warp polls the mbarrier (all its lanes, so that
   // the warp does not diverge) while the other warps sleep in the group's hardware barrier (no
-  // issue slots spent spinning); the outcome is shared through the barrier's reduction.
-  auto group_wait2 = [&](uint64_t* b1, uint32_t p1, uint64_t* b2, uint32_t p2, int id) -> bool {
-    bool ok = true;
+  // issue slots spent spinning). The block loops take no branch on a wait's outcome (a branch
+  // at every wait cost ≈ 6 % of the kernel's time): a wait that runs out of time marks the CTA
+  // (cta_abort), every later wait of the CTA returns at once, the groups run through their
+  // remaining blocks on whatever the buffers hold (every address stays valid), and the error is
+  // latched at the end.
+  volatile int* const abort_flag = &cta_abort;
+  auto group_wait2 = [&](uint64_t* b1, uint32_t p1, uint64_t* b2, uint32_t p2, int id) {
     if (lt < 32) {
-      ok = mbar_wait(b1, p1);
-      if (b2 != nullptr) ok = ok && mbar_wait(b2, p2);
+      mbar_wait_or_abort(b1, p1, abort_flag);
+      if (b2 != nullptr) mbar_wait_or_abort(b2, p2, abort_flag);
     }
-    return !named_sync_or(id, GROUP, !ok);
+    named_sync(id, GROUP);
   };
 
   // input side fused: g = g_min sigma(e^A z + b) on thread (cg, rg)'s chunks of the staged z tile
@@ -372,12 +378,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     };
-    bool pend_in = false;
-    int in_blk = 0, d_blk = -1;  // block of the last input load / A/P product issued
-    if (nblocks > 0) {
-      if (lt == 0) issue_in(0);
-      pend_in = true;
-    }
+    if (nblocks > 0 && lt == 0) issue_in(0);
     // beta of the next block is loaded one block ahead, kept as raw bits so that nothing waits
     // on the load until the block that needs it
     unsigned short beta_next = 0;
@@ -484,17 +485,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       // S has started the previous block (its first product read (K/Q e^Gamma)^T and the
       // per-parity arrays of two blocks ago are no longer read) and the previous A/P product
       // has released X and Y.
-      if (blk > 0 && !group_wait2(&bar_ZO, (blk - 1) & 1, &bar_D, (blk - 1) & 1, BAR_P)) {
-        aborted = true;
-        break;
-      }
+      if (blk > 0) group_wait2(&bar_ZO, (blk - 1) & 1, &bar_D, (blk - 1) & 1, BAR_P);
       if (lt < C) {
         beta_s[par][lt] = __uint_as_float((uint32_t)beta_next << 16);  // zero past the end
         beta_next = 0;
         if (lt < len - t0 - C) beta_next = beta_u[(row0 + t0 + C + lt) * H + h];
       }
-      if (!group_wait2(&bar_in, blk & 1, nullptr, 0, BAR_P)) { aborted = true; break; }
-      pend_in = false;
+      group_wait2(&bar_in, blk & 1, nullptr, 0, BAR_P);
       if constexpr (pre) {
         // ---------------- input side: k = L2Norm(ShortConv(k~)) in place in the staged tile (and
         // g = g_min sigma(e^A z + b) unless group S forms it), thread (cg, rg): channels 8 cg .. + 7
@@ -528,7 +525,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           put_rows4(tile, cg, rg, pk);
         }
         // q and g of this block from group S (the wait's group barrier also orders the k rows)
-        if (!group_wait2(&bar_qg, blk & 1, nullptr, 0, BAR_P)) { aborted = true; break; }
+        group_wait2(&bar_qg, blk & 1, nullptr, 0, BAR_P);
       }
       // ---------------- operands: X, Y, (K e^Gamma)^T, (Q e^Gamma)^T; Khat^T kept packed
       // Warp w covers channels 16 w .. 16 w + 15 (channel group cg = 0, 1 of 8) over all 64 tokens:
@@ -668,16 +665,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_arrive(&bar_prep);
         if (blk + 1 < nblocks) issue_in(blk + 1);  // the k, q and g tiles are dead
       }
-      if (blk + 1 < nblocks) {
-        pend_in = true;
-        in_blk = blk + 1;
-      }
-      d_blk = blk;
       // A goes into WS once S has read the previous block's A out of it
-      if (!group_wait2(&bar_D, blk & 1, blk > 0 ? &bar_wsfree : nullptr, (blk - 1) & 1, BAR_P)) {
-        aborted = true;
-        break;
-      }
+      group_wait2(&bar_D, blk & 1, blk > 0 ? &bar_wsfree : nullptr, (blk - 1) & 1, BAR_P);
       tc_fence_after();
       // ---------------- A (fp32, into WS) and P (bf16, into PT) out of TMEM
       // Lane m: rows 0..63 are the k side (A), 64..127 the q side (P); row r = m & 63 reads the
@@ -778,7 +767,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // ---------------- once S's last product of the previous block is complete: Khat^T of this
       // block (that product read the previous one) and the previous block's O
       if (blk > 0) {
-        if (!group_wait2(&bar_G3, (blk - 1) & 1, nullptr, 0, BAR_P)) { aborted = true; break; }
+        group_wait2(&bar_G3, (blk - 1) & 1, nullptr, 0, BAR_P);
         tc_fence_after();
       }
 #pragma unroll
@@ -798,24 +787,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lt == 0) mbar_arrive(&bar_khr);
       if (blk > 0 && write_out) store_o(blk - 1, ur);
     }
-    if (!aborted && nblocks > 0) {  // the last block's O
-      if (group_wait2(&bar_G3, (nblocks - 1) & 1, nullptr, 0, BAR_P)) {
-        tc_fence_after();
-        if (write_out) {
-          uint4 ur[4];
-          if constexpr (gated && !pre) load_u(nblocks - 1, ur);
-          stage_o(nblocks - 1);
-          named_sync(BAR_P, GROUP);
-          store_o(nblocks - 1, ur);
-        }
-      } else {
-        aborted = true;
+    if (nblocks > 0) {  // the last block's O
+      group_wait2(&bar_G3, (nblocks - 1) & 1, nullptr, 0, BAR_P);
+      tc_fence_after();
+      if (write_out) {
+        uint4 ur[4];
+        if constexpr (gated && !pre) load_u(nblocks - 1, ur);
+        stage_o(nblocks - 1);
+        named_sync(BAR_P, GROUP);
+        store_o(nblocks - 1, ur);
       }
-    }
-    if (aborted) record_status(4u /* KDA_ERR_TIMEOUT */);
-    if (lt == 0) {  // let anything already issued land before the CTA's memory goes away
-      if (aborted && pend_in) (void)mbar_wait(&bar_in, in_blk & 1);
-      if (d_blk >= 0) (void)mbar_wait(&bar_D, d_blk & 1);
     }
   } else {
     // =====================================================================  group S
@@ -853,8 +834,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // input side fused: q = L2Norm(ShortConv(q~)) and g = g_min sigma(e^A z + b) of block b in
     // place in the staged tiles, once they have landed (group P forms k meanwhile); thread
     // (cg, rg) as in group P's pass, the last three raw rows of q~ stashed in the WS padding
-    auto transform_qg = [&](int b) -> bool {
-      if (!group_wait2(&bar_in, b & 1, nullptr, 0, BAR_S)) return false;
+    auto transform_qg = [&](int b) {
+      group_wait2(&bar_in, b & 1, nullptr, 0, BAR_S);
       const int cg = lt & 15, rg = lt >> 4;
       if constexpr (s_takes_q) {
         auto halo = [&](int hr) {
@@ -881,29 +862,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       named_sync(BAR_S, GROUP);
       if (leader) mbar_arrive(&bar_qg);
-      return true;
     };
-    bool pend_v = false, pend_mma = false;
-    int v_blk = 0;  // block of the last v load issued
-    uint64_t* last_mma = &bar_ZO;
-    uint32_t last_par = 0;
-    if (nblocks > 0 && !vzero) {
-      if (leader) issue_v(0);
-      pend_v = true;
-    }
+    if (nblocks > 0 && !vzero && leader) issue_v(0);
     // G is zero above the diagonal blocks; those entries are never written again
     for (int i = lt; i < 8192 / 16; i += GROUP) st_shared_v4(sb + GB + 16u * (uint32_t)i, 0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     named_sync(BAR_S, GROUP);
-    int nb_run = nblocks;  // blocks to run (none if the first block's q and g timed out)
     if constexpr (pre) {
-      if (nblocks > 0 && !transform_qg(0)) {
-        aborted = true;
-        nb_run = 0;
-      }
+      if (nblocks > 0) transform_qg(0);
     }
 
-    for (int blk = 0; blk < nb_run; ++blk) {
+    for (int blk = 0; blk < nblocks; ++blk) {
       const int t0 = blk * C;
       const int n = min(C, len - t0);
       const int par = blk & 1;
@@ -913,10 +882,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // before the previous block's last product. Waiting for it again here could alias: P may
       // already have completed the next phase of bar_khr, and a parity wait would then look
       // for the phase after it.)
-      if (!group_wait2(&bar_prep, ph, nullptr, 0, BAR_S)) {
-        aborted = true;
-        break;
-      }
+      group_wait2(&bar_prep, ph, nullptr, 0, BAR_S);
       tc_fence_after();
       const uint32_t t_ot = t_ot_of(blk);  // this block's O^T columns
       // ---------------- tcgen05: [O^T | Z^T] (even) or [Z^T | O^T] (odd) =
@@ -930,10 +896,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                            desc_sw128(sb + KQ + 2048u * kk, 16384, 1024), id_zo, kk > 0);
         umma_commit(&bar_ZO);
       }
-      pend_mma = true; last_mma = &bar_ZO; last_par = ph;
       // ---------------- while that product runs: the solve of this block, once group P has
       // written A, P and the diagonal inverses (bar_ext)
-      if (!group_wait2(&bar_ext, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
+      group_wait2(&bar_ext, ph, nullptr, 0, BAR_S);
       // ---------------- T = (I + A)^{-1} (unit lower triangular) and G = T Diag(beta) (bf16)
       // From the 16 x 16 diagonal inverses T_RR (group P, in trr) and the block-inverse identity
       // [[P, 0], [C, Q]]^{-1} = [[P^{-1}, 0], [-Q^{-1} C P^{-1}, Q^{-1}]]: the off-diagonal
@@ -1011,13 +976,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       fence_proxy_async_smem();  // G is a tensor-core operand
       if constexpr (pre) {  // the next block's q and g, which group P's operand phase waits for
-        if (blk + 1 < nblocks && !transform_qg(blk + 1)) { aborted = true; break; }
+        if (blk + 1 < nblocks) transform_qg(blk + 1);
       }
       // ---------------- Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand, once the product is
       // complete; the wait's group barrier also says that every thread is done with WS
-      if (!group_wait2(&bar_ZO, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
+      group_wait2(&bar_ZO, ph, nullptr, 0, BAR_S);
       if (leader) mbar_arrive(&bar_wsfree);
-      pend_mma = false;
       tc_fence_after();
       {
         uint32_t v[32], zb[16];
@@ -1031,8 +995,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       // the v tile (its wait's group barrier orders the bf16 Z^T before the U product)
       if (!vzero) {
-        if (!group_wait2(&bar_v, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
-        pend_v = false;
+        group_wait2(&bar_v, ph, nullptr, 0, BAR_S);
         if constexpr (pre) {  // input side: v = ShortConv(v~) in place in the staged tile (as for k above);
           // the last three raw rows wait for the next block in the padding columns 16..19 of trr
           // (16-byte chunk row * 16 + cg), which no other step touches
@@ -1070,7 +1033,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         umma_commit(&bar_G2);
       }
-      pend_mma = true; last_mma = &bar_G2; last_par = ph;
       // ---------------- while U runs: S^T <- S^T Diag(e^{Gamma_L}) (the first product read the
       // bf16 copy; Khat^T U accumulates onto this one, after the barrier that follows U^T -> bf16).
       // The issuing thread's warp waits while its products enter the tensor pipe, so the warp of
@@ -1100,8 +1062,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_st16(tl + T_ST + c0, v);
         }
       }
-      if (!group_wait2(&bar_G2, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
-      pend_mma = false;
+      group_wait2(&bar_G2, ph, nullptr, 0, BAR_S);
       tc_fence_after();
       {  // U^T (lane v, tokens 32 hh ..) -> bf16 A operand, over Z^T bf16 (read by the product)
         uint32_t v[32], ub[16];
@@ -1117,7 +1078,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // stored this block's Khat^T by bar_khr. The two products have their own accumulators and
       // are issued by two threads in different warps; both commit to bar_G3.
       // (the wait's group barrier also orders every thread's U^T bf16 stores before the products)
-      if (!group_wait2(&bar_khr, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
+      group_wait2(&bar_khr, ph, nullptr, 0, BAR_S);
       if (leader) {
         tc_fence_after();
         const uint32_t id_s = idesc_bf16(128, DH, 0, 0, 0);  // N = the real key channels
@@ -1135,14 +1096,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                            desc_sw128(sb + PT + 8192u * (uint32_t)par + 32u * kk, 16, 1024), id_o, 1);
         umma_commit(&bar_G3);
       }
-      pend_mma = true; last_mma = &bar_G3; last_par = ph;
-      if (blk + 1 < nblocks && !vzero) {  // the v tile is dead (U is complete)
-        if (leader) issue_v(blk + 1);
-        pend_v = true;
-        v_blk = blk + 1;
-      }
-      if (!group_wait2(&bar_G3, ph, nullptr, 0, BAR_S)) { aborted = true; break; }
-      pend_mma = false;
+      if (blk + 1 < nblocks && !vzero && leader) issue_v(blk + 1);  // the v tile is dead (U is complete)
+      group_wait2(&bar_G3, ph, nullptr, 0, BAR_S);
       tc_fence_after();
       // ---------------- bf16 copy of the new state for the next block (group P writes O)
       {
@@ -1163,13 +1118,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_before();  // the next block's operand wait is the group barrier after the copy
     }
-    if (aborted) {
-      record_status(4u /* KDA_ERR_TIMEOUT */);
-      if (leader) {  // let anything already issued land before the CTA's memory goes away
-        if (pend_mma) (void)mbar_wait(last_mma, last_par);
-        if (pend_v) (void)mbar_wait(&bar_v, v_blk & 1);
-      }
-    } else if (pr.sf && (DH == 128 || (c < DH && hh == 0))) {  // S_final[c'][v] from S^T (lane
+    if (pr.sf && (DH == 128 || (c < DH && hh == 0))) {  // S_final[c'][v] from S^T (lane
       // v): coalesced over v
       float* sf = pr.sf + (size_t)pr.sf_i * DH * DH + c;
       uint32_t v[32];
@@ -1184,6 +1133,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    // the copies and products already issued land before TMEM and the CTA's memory go away:
+    // each completes within microseconds
+    if (tid == 0) {
+      record_status(4u /* KDA_ERR_TIMEOUT */);
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
+    }
+    __syncthreads();
+  }
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 

@@ -78,6 +78,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// As mbar_wait, for waits whose callers do not branch on the outcome: a wait that runs out of
+// time sets *cta_abort (shared by the CTA) and returns, and once it is set every later wait of
+// the CTA that would have to spin returns at once (a wait already spinning runs to its own
+// limit), so that a CTA whose producer failed runs through its remaining work and ends. The
+// caller reports *cta_abort.
+__device__ __forceinline__ void mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
+                                                   volatile int* cta_abort) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_test_wait(a, parity) || *cta_abort) return;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(a, parity)) return;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *cta_abort = 1;
+      return;
+    }
+  }
+}
+
 // Arrives once on `bar` with release semantics (orders this thread's earlier memory accesses,
 // and those it has observed through a barrier, before a waiter's acquire).
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
