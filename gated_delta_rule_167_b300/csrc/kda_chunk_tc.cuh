@@ -52,9 +52,9 @@
 // blocks ago (O^T and P are double-buffered by block parity). Transposed products keep every
 // tcgen05 product at M = 128 (TMEM lane = row). Only the bf16 copy of the state feeds the tensor
 // cores; the fp32 state accumulates in TMEM, so rounding does not accumulate in S itself. Every
-// wait is bounded; after a timeout the CTA's later waits return at once, the groups run through
-// their remaining blocks, and the kernel latches KDA_ERR_TIMEOUT, lets issued copies and products
-// land, frees TMEM and returns.
+// wait ends by a per-CTA deadline; after a wait gives up the later ones end at once, the groups
+// run through their remaining blocks, and the kernel latches KDA_ERR_TIMEOUT, lets issued copies
+// and products land, frees TMEM and returns.
 #pragma once
 
 #include <cuda.h>
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // bar_qg (input side fused): group S has formed a block's q and g in place in the staged tiles
   __shared__ uint64_t bar_qg;
   __shared__ uint32_t tmem_base_s;
-  __shared__ int cta_abort;  // a wait of this CTA ran out of time
+  __shared__ int cta_abort;  // this CTA ran past its deadline (a wait gave up)
   __shared__ __align__(16) float beta_s[2][C];  // by block parity
   __shared__ __align__(16) float gl_s[2][D];    // e^{Gamma_L} per key channel, by block parity
   // diagonal blocks T_RR of the solve (written by group P, read by group S); rows of 20 floats:
@@ -329,16 +329,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   };
   // Waits of a whole group: the group's first warp polls the mbarrier (all its lanes, so that
   // the warp does not diverge) while the other warps sleep in the group's hardware barrier (no
-  // issue slots spent spinning). The block loops take no branch on a wait's outcome (a branch
-  // at every wait cost ≈ 6 % of the kernel's time): a wait that runs out of time marks the CTA
-  // (cta_abort), every later wait of the CTA returns at once, the groups run through their
-  // remaining blocks on whatever the buffers hold (every address stays valid), and the error is
-  // latched at the end.
+  // issue slots spent spinning). Every wait of the CTA ends by one deadline, 2 s plus 50 us per
+  // block (about ten times a block's normal time). Nothing branches on a wait's outcome (a
+  // branch, or any use of the outcome, at the waits cost 4-8 % of the kernel's time): after a
+  // wait gives up, every later wait ends at once, the groups run through their remaining blocks
+  // on whatever the buffers hold (every address stays valid), and at the end a CTA that is past
+  // its deadline latches KDA_ERR_TIMEOUT.
   volatile int* const abort_flag = &cta_abort;
+  const uint64_t deadline = globaltimer_ns() + kWaitLimitNs + 50000ull * (uint64_t)nblocks;
   auto group_wait2 = [&](uint64_t* b1, uint32_t p1, uint64_t* b2, uint32_t p2, int id) {
     if (lt < 32) {
-      mbar_wait_or_abort(b1, p1, abort_flag);
-      if (b2 != nullptr) mbar_wait_or_abort(b2, p2, abort_flag);
+      mbar_wait_until(b1, p1, deadline);
+      if (b2 != nullptr) mbar_wait_until(b2, p2, deadline);
     }
     named_sync(id, GROUP);
   };
@@ -1131,6 +1133,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   }
+  // a CTA that ran past its deadline had a wait give up: its results are not to be trusted
+  if (tid == 0 && globaltimer_ns() > deadline) *abort_flag = 1;
   tc_fence_before();
   __syncthreads();
   if (*abort_flag) {

@@ -78,22 +78,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// As mbar_wait, for waits whose callers do not branch on the outcome: a wait that runs out of
-// time sets *cta_abort (shared by the CTA) and returns, and once it is set every later wait of
-// the CTA that would have to spin returns at once (a wait already spinning runs to its own
-// limit), so that a CTA whose producer failed runs through its remaining work and ends. The
-// caller reports *cta_abort.
-__device__ __forceinline__ void mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
-                                                   volatile int* cta_abort) {
+// Waits for the phase with the given parity, until `deadline` (global timer, ns) at the latest.
+// No outcome is returned: the spin has a single exit and no side effect, which keeps the code
+// around it free of branches (the caller judges a failure by the deadline having passed).
+__device__ __forceinline__ void mbar_wait_until(uint64_t* bar, uint32_t parity, uint64_t deadline) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_test_wait(a, parity) || *cta_abort) return;
-  const uint64_t t0 = globaltimer_ns();
+  if (mbar_test_wait(a, parity)) return;
   for (;;) {
     if (mbar_try_wait(a, parity)) return;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *cta_abort = 1;
-      return;
-    }
+    if (globaltimer_ns() > deadline) return;
   }
 }
 
