@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bar_in, 1);
     mbar_init(&bar_v, 1);
     mbar_init(&bar_prep, 1);
-    mbar_init(&bar_ext, 1);
+    mbar_init(&bar_ext, GROUP / 32);  // one arrive per warp of group P
     mbar_init(&bar_wsfree, 1);
     mbar_init(&bar_khr, 1);
     mbar_init(&bar_D, 1);
@@ -341,6 +341,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lt < 32) {
       mbar_wait_until(b1, p1, deadline);
       if (b2 != nullptr) mbar_wait_until(b2, p2, deadline);
+    }
+    named_sync(id, GROUP);
+  };
+  // up to three hand-offs under one group barrier (each group barrier costs the chain ~0.1 K cycles)
+  auto group_wait3 = [&](uint64_t* b1, uint32_t p1, uint64_t* b2, uint32_t p2, uint64_t* b3, uint32_t p3, int id) {
+    if (lt < 32) {
+      if (b1 != nullptr) mbar_wait_until(b1, p1, deadline);
+      if (b2 != nullptr) mbar_wait_until(b2, p2, deadline);
+      mbar_wait_until(b3, p3, deadline);
     }
     named_sync(id, GROUP);
   };
@@ -485,15 +494,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int n = min(C, len - t0);
       const int par = blk & 1;
       // S has started the previous block (its first product read (K/Q e^Gamma)^T and the
-      // per-parity arrays of two blocks ago are no longer read) and the previous A/P product
-      // has released X and Y.
-      if (blk > 0) group_wait2(&bar_ZO, (blk - 1) & 1, &bar_D, (blk - 1) & 1, BAR_P);
+      // per-parity arrays of two blocks ago are no longer read), the previous A/P product has
+      // released X and Y, and this block's k, q, g tiles have landed: one wait for the three.
+      // (beta of this block is first read after the operand phase's group barrier.)
+      group_wait3(blk > 0 ? &bar_ZO : nullptr, (blk - 1) & 1, blk > 0 ? &bar_D : nullptr, (blk - 1) & 1,
+                  &bar_in, blk & 1, BAR_P);
       if (lt < C) {
         beta_s[par][lt] = __uint_as_float((uint32_t)beta_next << 16);  // zero past the end
         beta_next = 0;
         if (lt < len - t0 - C) beta_next = beta_u[(row0 + t0 + C + lt) * H + h];
       }
-      group_wait2(&bar_in, blk & 1, nullptr, 0, BAR_P);
       if constexpr (pre) {
         // ---------------- input side: k = L2Norm(ShortConv(k~)) in place in the staged tile (and
         // g = g_min sigma(e^A z + b) unless group S forms it), thread (cg, rg): channels 8 cg .. + 7
@@ -759,8 +769,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      named_sync(BAR_P, GROUP);
-      if (lt == 0) mbar_arrive(&bar_ext);
+      // each warp hands its part to group S as it finishes (no group barrier on this chain:
+      // nothing below reads WS or trr before the next block's bar_wsfree)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_ext);
       // the previous block's gate rows: their loads run under the waits and the staging below
       uint4 ur[4];
       if constexpr (gated && !pre) {
@@ -981,8 +993,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (blk + 1 < nblocks) transform_qg(blk + 1);
       }
       // ---------------- Z^T (lane v = c, tokens 32 hh ..) -> bf16 A operand, once the product is
-      // complete; the wait's group barrier also says that every thread is done with WS
-      group_wait2(&bar_ZO, ph, nullptr, 0, BAR_S);
+      // complete; the wait's group barrier also says that every thread is done with WS. The v tile
+      // (issued a block ago) is waited for here too, one group barrier for both.
+      group_wait2(&bar_ZO, ph, vzero ? nullptr : &bar_v, ph, BAR_S);
       if (leader) mbar_arrive(&bar_wsfree);
       tc_fence_after();
       {
@@ -995,9 +1008,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      // the v tile (its wait's group barrier orders the bf16 Z^T before the U product)
+      // a group barrier orders the bf16 Z^T before the U product (the v tile has landed)
       if (!vzero) {
-        group_wait2(&bar_v, ph, nullptr, 0, BAR_S);
+        named_sync(BAR_S, GROUP);
         if constexpr (pre) {  // input side: v = ShortConv(v~) in place in the staged tile (as for k above);
           // the last three raw rows wait for the next block in the padding columns 16..19 of trr
           // (16-byte chunk row * 16 + cg), which no other step touches
