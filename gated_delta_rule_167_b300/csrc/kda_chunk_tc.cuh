@@ -77,6 +77,7 @@ constexpr int THREADS = 512;  // two groups of 256
 constexpr int GROUP = 256;
 constexpr int BAR_P = 1, BAR_S = 2;  // hardware barrier ids of the groups
 constexpr int BAR_PAIR0 = 3;        // ids 3..6: pairs of warps of the state group in its solve
+constexpr int BAR_TILE0 = 7;        // ids 7, 8: the two warps of a diagonal tile in the solve
 constexpr int kLongestFirstMax = 256;  // packed batches of up to this many sequences run longest first
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -946,6 +947,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           __syncwarp();
           float acc2[4] = {0.f, 0.f, 0.f, 0.f};
           tile_mma(acc2, &trr[2 * tile + 1][0][0], TLD, y, WLD, 2);
+          // T_10 goes over A_10, which the other warp of the tile reads whole (all 16 columns)
+          named_sync(BAR_TILE0 + tile, 64);
           float* o = ws + (16 + 32 * tile) * WLD + 32 * tile + 8 * nh + 2 * t;
           o[g * WLD] = tf32r(-acc2[0]);
           o[g * WLD + 1] = tf32r(-acc2[1]);
