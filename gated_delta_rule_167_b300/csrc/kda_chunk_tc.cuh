@@ -124,6 +124,7 @@ constexpr int Y_A = 64;
 constexpr int TLD = 20;  // row stride (floats) of the diagonal inverses
 struct TmaMaps {
   CUtensorMap q, k, v, g;
+  CUtensorMap u;  // output gate rows (output side fused only)
 };
 
 using namespace sm100;
@@ -238,7 +239,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   __shared__ uint64_t bar_in, bar_v, bar_prep, bar_ext, bar_wsfree, bar_khr, bar_D, bar_ZO, bar_G2,
       bar_G3;
   // bar_qg (input side fused): group S has formed a block's q and g in place in the staged tiles
-  __shared__ uint64_t bar_qg;
+  // bar_u (output side fused): a block's gate rows u have landed in XQ
+  __shared__ uint64_t bar_qg, bar_u;
   __shared__ uint32_t tmem_base_s;
   __shared__ int cta_abort;  // this CTA ran past its deadline (a wait gave up)
   __shared__ __align__(16) float beta_s[2][C];  // by block parity
@@ -304,11 +306,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bar_G2, 1);
     mbar_init(&bar_G3, 2);  // the two issuers of the last product commit to it
     mbar_init(&bar_qg, 1);
+    mbar_init(&bar_u, 1);
     fence_mbar_init();
     prefetch_tensormap(&maps.q);
     prefetch_tensormap(&maps.k);
     prefetch_tensormap(&maps.v);
     prefetch_tensormap(&maps.g);
+    if constexpr (POST) prefetch_tensormap(&maps.u);
   }
   if (warp == 0) tmem_alloc(&tmem_base_s, 512);
   if constexpr (DH == 64) {  // the second box of every input tile is the zero padding
@@ -433,21 +437,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     // channels (16 lanes of a half-warp, 8 channels each) is normalised and gated on its way out:
     // y = o~ / sqrt(mean(o~^2) + eps) * w * sigma(u), the mean by a 16-lane reduction.
     constexpr bool gated = POST;
-    auto load_u = [&](int b, uint4 (&ur)[4]) {
-      const int tb = b * C;
-      const int nb = min(C, len - tb);
-      const __nv_bfloat16* ub = static_cast<const __nv_bfloat16*>(P.gate_u) +
-                                ((row0 + tb + (lt >> 4)) * H + h) * D + 8 * (lt & 15);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = (lt >> 4) + 16 * i;
-        ur[i] = r < nb ? *reinterpret_cast<const uint4*>(ub + (size_t)(16 * i) * H * D)
-                       : make_uint4(0, 0, 0, 0);
+    // The gate rows u of block b come by TMA into XQ (the q-side X panel, free from the completion
+    // of the A/P product that read it until the next block's operands are written), issued as
+    // soon as that product completes; the rows of the block after it go into L2 meanwhile.
+    auto issue_u = [&](int b, uint32_t dst) {
+      const int row = (int)(row0 + (size_t)b * C);
+      mbar_arrive_expect_tx(&bar_u, NBOX * BOX_BYTES);
+      load2(dst, &maps.u, row, &bar_u);
+      if (b + 1 < nblocks) {
+        tma_prefetch_3d(&maps.u, 0, h, row + C);
+        tma_prefetch_3d(&maps.u, 64, h, row + C);
       }
     };
-    // (with the output side alone, the caller loads the gate rows ahead into ur; with both sides
-    // fused the registers are short and they are loaded here)
-    auto store_o = [&](int b, const uint4 (&ur_ahead)[4]) {
+    auto store_o = [&](int b, uint32_t ubase) {
       const int tb = b * C;
       const int nb = min(C, len - tb);
       const int q = lt & 15;  // 16-byte chunk of a row; rows lt / 16 + 16 i
@@ -462,11 +464,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             *reinterpret_cast<uint4*>(out + ((row0 + tb + r) * H + h) * DH + 8 * q8) =
                 *reinterpret_cast<const uint4*>(stg + r * 256 + 16 * (q8 ^ (r & 7)));
         }
-      } else if constexpr (gated) {
-        uint4 ur[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ur[i] = ur_ahead[i];
-        if constexpr (pre) load_u(b, ur);
+      } else if constexpr (gated) {  // u from the tile at ubase, after bar_u
         float w8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) w8[e] = P.norm_w[8 * q + e];
@@ -475,7 +473,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int r = (lt >> 4) + 16 * i;
           float x[8], u8[8];
           post::unpack8(*reinterpret_cast<const uint4*>(stg + r * 256 + 16 * (q ^ (r & 7))), x);
-          post::unpack8(ur[i], u8);
+          post::unpack8(*reinterpret_cast<const uint4*>(sm + ubase + tile_chunk(q, r)), u8);
           post::gate_chunk(x, u8, w8, P.norm_eps, D);
           if (r < nb) *reinterpret_cast<uint4*>(ob + (size_t)(16 * i) * H * D) = post::pack8(x);
         }
@@ -681,6 +679,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       // A goes into WS once S has read the previous block's A out of it
       group_wait2(&bar_D, blk & 1, blk > 0 ? &bar_wsfree : nullptr, (blk - 1) & 1, BAR_P);
       tc_fence_after();
+      if constexpr (gated) {  // XQ is free now: the previous block's gate rows
+        if (lt == 0 && blk > 0 && write_out) issue_u(blk - 1, XQ);
+      }
       // ---------------- A (fp32, into WS) and P (bf16, into PT) out of TMEM
       // Lane m: rows 0..63 are the k side (A), 64..127 the q side (P); row r = m & 63 reads the
       // Y_A columns in the first half of the block, the Y_B columns in the second (warp-uniform).
@@ -774,15 +775,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       // nothing below reads WS or trr before the next block's bar_wsfree)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_ext);
-      // the previous block's gate rows: their loads run under the waits and the staging below
-      uint4 ur[4];
-      if constexpr (gated && !pre) {
-        if (blk > 0 && write_out) load_u(blk - 1, ur);
-      }
       // ---------------- once S's last product of the previous block is complete: Khat^T of this
       // block (that product read the previous one) and the previous block's O
       if (blk > 0) {
-        group_wait2(&bar_G3, (blk - 1) & 1, nullptr, 0, BAR_P);
+        group_wait2(&bar_G3, (blk - 1) & 1, (gated && write_out) ? &bar_u : nullptr, (blk - 1) & 1, BAR_P);
         tc_fence_after();
       }
 #pragma unroll
@@ -800,17 +796,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       // Khat^T is stored and the previous block's O is out of TMEM; its global stores follow (the
       // release of this arrive does not wait for them)
       if (lt == 0) mbar_arrive(&bar_khr);
-      if (blk > 0 && write_out) store_o(blk - 1, ur);
+      if (blk > 0 && write_out) store_o(blk - 1, XQ);
     }
-    if (nblocks > 0) {  // the last block's O
-      group_wait2(&bar_G3, (nblocks - 1) & 1, nullptr, 0, BAR_P);
+    if (nblocks > 0) {  // the last block's O (its gate rows into the k tile, which no one reads
+      // any more, while XQ may still be read for the block before it)
+      if (gated && write_out && lt == 0) issue_u(nblocks - 1, IN_K);
+      group_wait2(&bar_G3, (nblocks - 1) & 1, (gated && write_out) ? &bar_u : nullptr,
+                  (nblocks - 1) & 1, BAR_P);
       tc_fence_after();
       if (write_out) {
-        uint4 ur[4];
-        if constexpr (gated && !pre) load_u(nblocks - 1, ur);
         stage_o(nblocks - 1);
         named_sync(BAR_P, GROUP);
-        store_o(nblocks - 1, ur);
+        store_o(nblocks - 1, IN_K);
       }
     }
   } else {
@@ -1212,11 +1209,13 @@ inline bool tc_supports(int C, int d, const SeqParams& P) {
 inline kda_status_t launch_chunk_tc(const SeqParams& P, int n_problems, int d, cudaStream_t st,
                                     std::string& err) {
   tc::TmaMaps maps;
+  memset(&maps, 0, sizeof(maps));
   const long long rows = P.cu_seqlens ? (long long)P.T : (long long)P.n_seq * P.T;
   if (!tc::encode_token_map(&maps.q, P.q, rows, P.H, d) ||
       !tc::encode_token_map(&maps.k, P.k, rows, P.H, d) ||
       !tc::encode_token_map(&maps.v, P.v, rows, P.H, d) ||
-      !tc::encode_token_map(&maps.g, P.g, rows, P.H, d)) {
+      !tc::encode_token_map(&maps.g, P.g, rows, P.H, d) ||
+      (P.gate_u != nullptr && !tc::encode_token_map(&maps.u, P.gate_u, rows, P.H, d))) {
     err = "cuTensorMapEncodeTiled failed";
     return KDA_ERR_CUDA;
   }

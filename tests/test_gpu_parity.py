@@ -311,6 +311,29 @@ def test_prefill_then_decode_continues_the_sequence(kda):
     check(Sf.cpu().double().numpy(), S_ref, "f32", "S")
 
 
+@pytest.mark.parametrize("d,B,H", [(128, 2, 160), (64, 4, 80)])
+def test_prefill_bits_repeat(kda, d, B, H):
+    """The tensor-core prefill gives the same bits on every call: more problems than SMs (two
+    waves, the second partial) and several blocks each, so that its warps and groups meet each
+    hand-off at varying times. A race between the warps would show here as a few differing
+    elements; the output is compared with the oracle on one sampled problem as well."""
+    inp = kda_synth.make_prefill_inputs(B, 640, H, d, d, "bf16", seed=d + 5, S0_std=0.05,
+                                        g_bias=True)
+    x = to_dev(inp)
+    S0 = inp["S0"].to(DEV)
+    ref_out, ref_S = kda.chunk_fwd(*x, S0, C=64)
+    for _ in range(6):
+        out, Sf = kda.chunk_fwd(*x, S0, C=64)
+        assert torch.equal(out, ref_out) and torch.equal(Sf, ref_S)
+    kda.kda_sync_status()
+    b, h = B - 1, H - 1
+    sub = {n: inp[n][b:b + 1, :, h:h + 1] for n in ("q", "k", "v", "g", "beta")}
+    o_ref, S_ref = oracle.recurrent(*(f64(sub[n]) for n in ("q", "k", "v", "g", "beta")),
+                                    f64(inp["S0"][b:b + 1, h:h + 1]))
+    check(ref_out[b:b + 1, :, h:h + 1].float().cpu().double().numpy(), o_ref, "bf16", "out")
+    check(ref_S[b:b + 1, h:h + 1].cpu().double().numpy(), S_ref, "bf16", "S_final")
+
+
 # ------------------------------------------------------------------ streams and host buffers
 
 
