@@ -29,7 +29,7 @@ import kda_synth  # noqa: E402
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("kind", choices=["prefill", "varlen", "decode", "segmented", "fused",
+    ap.add_argument("kind", choices=["prefill", "gated", "varlen", "decode", "segmented", "fused",
                                      "decode_tokens"])
     ap.add_argument("--K", type=int, default=4)
     ap.add_argument("--n_seg", type=int, default=0)
@@ -54,6 +54,17 @@ def main(argv=None):
         Sf = torch.empty(a.B, a.H, a.d, a.d, dtype=torch.float32, device=dev)
         for _ in range(a.iters):
             kda.kda_chunk_fwd(*x, None, out, Sf, C=a.C)
+    elif a.kind == "gated":  # the prefill with the output side in its epilogue
+        inp = kda_synth.make_prefill_inputs(a.B, a.T, a.H, a.d, a.d, a.dtype, seed=0,
+                                            g_bias=True, device=dev)
+        x = [inp[n] for n in ("q", "k", "v", "g", "beta")]
+        gen = torch.Generator(device=dev).manual_seed(1)
+        u = torch.randn(a.B, a.T, a.H, a.d, generator=gen, device=dev).to(x[0].dtype)
+        w = 1.0 + 0.1 * torch.randn(a.d, generator=gen, device=dev)
+        out = torch.empty(a.B, a.T, a.H, a.d, dtype=x[0].dtype, device=dev)
+        Sf = torch.empty(a.B, a.H, a.d, a.d, dtype=torch.float32, device=dev)
+        for _ in range(a.iters):
+            kda.kda_chunk_fwd_gated(*x, None, u, w, out, Sf, C=a.C)
     elif a.kind == "varlen":
         inp = kda_synth.make_varlen_inputs(a.T, a.H, a.d, a.d, a.nseq, a.dtype, seed=0, device=dev)
         x = [inp[n] for n in ("q", "k", "v", "g", "beta")]
