@@ -466,8 +466,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else if constexpr (gated) {  // u from the tile at ubase, after bar_u
         float w8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w8[e] = P.norm_w[8 * q + e];
+        post::load_w8(P.norm_w + 8 * q, w8);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = (lt >> 4) + 16 * i;

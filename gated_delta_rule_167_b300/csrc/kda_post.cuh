@@ -61,6 +61,12 @@ __device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// The 8 weights of one chunk (16-byte aligned: w is, and chunks start at multiples of 8)
+__device__ __forceinline__ void load_w8(const float* p, float (&w)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
+
 // y = o / sqrt(mean(o^2) + eps) * w * sigma(u) for one 8-channel chunk of a 128-channel row held
 // by 16 lanes; `valid` rows take part in the reduction either way (their lanes are in the same
 // half-warp) but their values are only used when valid.
@@ -71,7 +77,10 @@ __device__ __forceinline__ void gate_chunk(float (&x)[8], const float (&u)[8], c
 #pragma unroll
   for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
   ss = sum16(ss);
-  const float inv = 1.f / sqrtf(ss / (float)d + eps);
+  // bf16 outputs: the hardware reciprocal square root (about 2 ulp of fp32, far below the
+  // output's rounding) instead of a correctly rounded square root and division
+  const float ms = ss / (float)d + eps;
+  const float inv = sizeof(TIn) == 2 ? rsqrtf(ms) : 1.f / sqrtf(ms);
 #pragma unroll
   for (int e = 0; e < 8; ++e) x[e] = x[e] * inv * w[e] * sigmoid_for<TIn>(u[e]);
 }
@@ -87,8 +96,7 @@ __global__ void __launch_bounds__(256)
   const bool valid = row < n_rows;
   const size_t base = (size_t)(valid ? row : 0) * 128 + 8 * q;
   float x[8], uu[8], ww[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) ww[e] = w[8 * q + e];
+  load_w8(w + 8 * q, ww);
   if constexpr (sizeof(TIn) == 2) {
     uint4 ro = make_uint4(0, 0, 0, 0), ru = ro;
     if (valid) {
@@ -138,7 +146,8 @@ __global__ void __launch_bounds__(256)
   for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
 #pragma unroll
   for (int off = 4; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  const float inv = 1.f / sqrtf(ss / 64.f + eps);
+  const float ms = ss / 64.f + eps;
+  const float inv = sizeof(TIn) == 2 ? rsqrtf(ms) : 1.f / sqrtf(ms);  // as gate_chunk
   if (!valid) return;
 #pragma unroll
   for (int e = 0; e < 8; ++e)

@@ -62,6 +62,11 @@ def test_gated_prefill_dense(kda, dtype, d, C):
     y_epi = prepost.post_core(raw.float().cpu().double().numpy(), f64(u), f64(w), eps=1e-5)
     check_gated(out.float().cpu().double().numpy(), y_ref, dtype, "y", y_epi if dtype == "bf16" else None)
     check(Sf.cpu().double().numpy(), S_ref, dtype, "S_final")
+    if dtype == "bf16" and d == 128:  # the epilogue and the standalone kernel: the same function
+        y2 = torch.empty_like(raw)
+        kda.kda_output_gate(raw, u.to(DEV), w.to(DEV), y2)
+        kda.kda_sync_status()
+        assert torch.equal(out, y2)
 
 
 @pytest.mark.parametrize("C", [64, 128])
