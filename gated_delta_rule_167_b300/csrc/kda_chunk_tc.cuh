@@ -176,19 +176,22 @@ __device__ __forceinline__ void conv_rows4(const uint8_t* tile, const float* w, 
     else if (first_pos > 0) v = *reinterpret_cast<const uint4*>(halo(r + 3));
     xr[m][0] = v.x; xr[m][1] = v.y; xr[m][2] = v.z; xr[m][3] = v.w;
   }
+  // channels in pairs (e, e + 1), one packed fma per tap: each lane rounds as fmaf does, in the
+  // same tap order
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    float x[7];
+  for (int e = 0; e < 8; e += 2) {
+    float2 x[7];
 #pragma unroll
     for (int m = 0; m < 7; ++m)
-      x[m] = __uint_as_float((e & 1) ? (xr[m][e >> 1] & 0xFFFF0000u) : (xr[m][e >> 1] << 16));
+      x[m] = make_float2(__uint_as_float(xr[m][e >> 1] << 16), __uint_as_float(xr[m][e >> 1] & 0xFFFF0000u));
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      float a = 0.f;
+      float2 a = make_float2(0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        if (j <= first_pos + 4 * rg + i) a = fmaf(t[j][e], x[i + 3 - j], a);
-      y[i][e] = a;
+        if (j <= first_pos + 4 * rg + i) a = fma2(make_float2(t[j][e], t[j][e + 1]), x[i + 3 - j], a);
+      y[i][e] = a.x;
+      y[i][e + 1] = a.y;
     }
   }
 }
@@ -363,8 +366,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto gate_rows4 = [&](int cg, int rg) {
     const float eA = expf(P.A_log[h]);
     float b8[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) b8[e] = P.b_decay[(size_t)h * D + 8 * cg + e];
+    post::load_w8(P.b_decay + (size_t)h * D + 8 * cg, b8);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       uint4* p4 = reinterpret_cast<uint4*>(sm + IN_G + tile_chunk(cg, 4 * rg + i));
