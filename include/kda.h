@@ -123,7 +123,10 @@ kda_status_t kda_recurrent_steps(const void* q, const void* k, const void* v, co
  * otherwise a packed batch (n_seq = N sequences, T = T_total, the layout and rules of
  * kda_chunk_fwd_varlen). S0 / S_final as in those calls. The bf16 tensor-core path (d = 128,
  * C = 64 or 128) normalises and gates each block in its output epilogue, from the bf16-rounded
- * raw output; the other paths write o~ and apply kda_output_gate over it in place.
+ * raw output; the other paths write o~ and apply kda_output_gate over it in place. Both give the
+ * same bits for the same raw output. Precision: with bf16 tensors 1/sqrt(mean + eps) is the
+ * hardware reciprocal square root and sigma the hardware tanh form (errors far below the bf16
+ * rounding of y); with fp32 tensors both are computed to fp32 accuracy.
  */
 kda_status_t kda_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* g,
                                  const void* beta, const float* S0, const void* gate_u,
