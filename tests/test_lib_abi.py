@@ -140,3 +140,24 @@ def test_noalloc_entry_point_refuses_oversized_requests_on_the_host(lib):
     assert lib.kda_chunk_fwd_segmented_noalloc(*a, 1, 96, 8192, 128, 128, 64, 8, 1, None) == 2
     assert b"scratch" in lib.kda_last_error()
     assert lib.kda_chunk_fwd_segmented_noalloc(*a, 1, 96, 8192, 128, 128, 64, 0, 1, None) == 1
+
+
+def test_binding_refuses_host_tensors(lib):
+    """No CPU fallback: the binding sends host tensors to no kernel and computes nothing itself;
+    every mirror of a compute entry point raises before the call."""
+    import torch
+    import gated_delta_rule_167_b300 as kda
+
+    B, T, H, d = 1, 8, 2, 64
+    bf = torch.bfloat16
+    q, k, v, g = (torch.zeros(B, T, H, d, dtype=bf) for _ in range(4))
+    beta = torch.zeros(B, T, H, dtype=bf)
+    out = torch.empty(B, T, H, d, dtype=bf)
+    with pytest.raises(ValueError, match="must be on"):
+        kda.kda_chunk_fwd(q, k, v, g, beta, None, out, None)
+    S = torch.zeros(B, H, d, d)
+    with pytest.raises(ValueError, match="must be on"):
+        kda.kda_recurrent_step(q[:, 0], k[:, 0], v[:, 0], g[:, 0], beta[:, 0], S, out[:, 0])
+    u, w = torch.zeros(T, d, dtype=bf), torch.ones(d)
+    with pytest.raises(ValueError, match="must be on"):
+        kda.kda_output_gate(out[0, :, 0], u, w, out[0, :, 0].clone())
